@@ -1,0 +1,350 @@
+"""Pins for the fp64 oracle, against things other than the oracle itself.
+
+The pages print no worked numeric example for these kernels, so the oracle is
+pinned by: library routines (numpy / torch number-format conversions, torch
+scaled_dot_product_attention in fp64 on materialised tensors), closed forms
+(two-token sigmoid form, one-hot limits, means), invariants the pages fix
+(paged == materialised contiguous, MiniLLM Runtime "Key benchmark results";
+physical block relabelling), and brute force on tiny integer inputs.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+import torch.nn.functional as F
+
+import oracle
+import workloads as wl
+from workloads import BF16, F16
+
+
+def f64(bits, dtype):
+    return oracle.to_double(bits, dtype)
+
+
+def materialise(pool_cache, bt_row, L):
+    """Contiguous [L, Hkv, D] gather via numpy fancy indexing (independent of the oracle)."""
+    nb, bs, hkv, d = pool_cache.shape
+    t = np.arange(L)
+    return pool_cache[bt_row[t // bs], t % bs]
+
+
+def sdpa_decode(q_bits, k_bits, v_bits, bt, cl, scale, dtype, n_kv_heads):
+    """torch SDPA (fp64) over materialised K/V, GQA by repeat_interleave (head h -> kv head h // G)."""
+    S, Hq, D = q_bits.shape
+    G = Hq // n_kv_heads
+    out = np.zeros((S, Hq, D))
+    for s in range(S):
+        L = int(cl[s])
+        K = torch.from_numpy(f64(materialise(k_bits, bt[s], L), dtype))  # [L, Hkv, D]
+        V = torch.from_numpy(f64(materialise(v_bits, bt[s], L), dtype))
+        q = torch.from_numpy(f64(q_bits[s], dtype))                       # [Hq, D]
+        Kx = K.permute(1, 0, 2).repeat_interleave(G, dim=0)               # [Hq, L, D]
+        Vx = V.permute(1, 0, 2).repeat_interleave(G, dim=0)
+        o = F.scaled_dot_product_attention(q[:, None, :], Kx, Vx, scale=scale)
+        out[s] = o[:, 0, :].numpy()
+    return out
+
+
+def small_decode(seed, lens, hq=4, hkv=2, d=16, dtype=BF16, **kw):
+    return wl.build_workload("t", seed, dtype=dtype, n_q_heads=hq, n_kv_heads=hkv, head_dim=d, decode_lens=lens, **kw)
+
+
+# --------------------------------------------------------------- number formats
+
+
+def test_f16_widening_matches_numpy_all_patterns():
+    bits = np.arange(65536, dtype=np.uint16)
+    ref = bits.view(np.float16).astype(np.float64)
+    got = f64(bits, F16)
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(got), nan)
+    assert np.array_equal(got[~nan], ref[~nan])
+
+
+def test_bf16_widening_matches_torch_all_patterns():
+    bits = np.arange(65536, dtype=np.uint16)
+    ref = torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).to(torch.float64).numpy()
+    got = f64(bits, BF16)
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(got), nan)
+    assert np.array_equal(got[~nan], ref[~nan])
+
+
+def test_f16_rounding_matches_numpy():
+    rng = np.random.default_rng(0)
+    x = np.concatenate([
+        rng.standard_normal(20000) * 10.0 ** rng.integers(-8, 5, 20000),
+        # exact ties between neighbouring fp16 values, normal and subnormal
+        (np.arange(0, 4096, dtype=np.float64) + 0.5) * 2.0 ** -24,
+        (np.arange(1024, 2048, dtype=np.float64) + 0.5) * 2.0 ** -10,
+        np.array([65504.0, 65519.99, 65520.0, 1e6, -1e6, 0.0, -0.0, 2.0 ** -25, 2.0 ** -26]),
+    ])
+    ref = x.astype(np.float16).view(np.uint16)
+    got = oracle.round_to(x, F16)
+    assert np.array_equal(got, ref)
+
+
+def test_bf16_rounding_matches_torch():
+    rng = np.random.default_rng(1)
+    # float32-representable inputs, so torch's float->bf16 rounding is the exact reference
+    x = (rng.standard_normal(50000) * 10.0 ** rng.integers(-30, 30, 50000)).astype(np.float32)
+    ties = ((np.arange(0x3F80, 0x4000, dtype=np.uint32) << 16) | 0x8000).view(np.float32)
+    x = np.concatenate([x, ties, np.array([0.0, -0.0, 1e-40], dtype=np.float32)])
+    ref = torch.from_numpy(x).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    got = oracle.round_to(x.astype(np.float64), BF16)
+    assert np.array_equal(got, ref)
+
+
+# --------------------------------------------------------------- KV-cache write
+
+
+def test_kv_write_lands_at_block_and_offset():
+    w = wl.write_rows_case(7, 300, n_kv_heads=2, head_dim=16, block_size=16, pad_frac=0.1)
+    p, wr = w.pool, w.write
+    k, v, st = oracle.kv_write(p.k_cache, p.v_cache, wr.key, wr.value, wr.slot_mapping, 16)
+    assert st == oracle.OK
+    touched = np.zeros((p.num_blocks, 16), dtype=bool)
+    for i, slot in enumerate(wr.slot_mapping):
+        if slot < 0:
+            continue
+        b, o = divmod(int(slot), 16)          # slot = block_id * block_size + offset
+        assert np.array_equal(k[b, o], wr.key[i]) and np.array_equal(v[b, o], wr.value[i])
+        touched[b, o] = True
+    assert (wr.slot_mapping == -1).sum() == 30
+    assert np.array_equal(k[~touched], p.k_cache[~touched])
+    assert np.array_equal(v[~touched], p.v_cache[~touched])
+
+
+def test_kv_write_out_of_pool_slot_is_reported_and_skipped():
+    w = wl.write_rows_case(8, 4, n_kv_heads=1, head_dim=8, pad_frac=0.0, extra_blocks=0)
+    p, wr = w.pool, w.write
+    sm = wr.slot_mapping.copy()
+    sm[1] = p.num_blocks * 16          # one past the pool
+    k, v, st = oracle.kv_write(p.k_cache, p.v_cache, wr.key, wr.value, sm, 16, check=False)
+    assert st == oracle.EBOUNDS
+    for i in (0, 2, 3):
+        b, o = divmod(int(sm[i]), 16)
+        assert np.array_equal(k[b, o], wr.key[i])
+
+
+# --------------------------------------------------------------- decode
+
+
+@pytest.mark.parametrize("dtype,hq,hkv,d", [(BF16, 4, 2, 16), (F16, 2, 2, 64), (BF16, 8, 2, 32), (F16, 3, 1, 8)])
+def test_decode_matches_torch_sdpa_fp64(dtype, hq, hkv, d):
+    w = small_decode(11 + d, [1, 15, 16, 17, 40, 100], hq=hq, hkv=hkv, d=d, dtype=dtype)
+    p, b = w.pool, w.decode
+    got = oracle.decode(b.q, p.k_cache, p.v_cache, b.block_tables, b.context_lens, b.scale, dtype)
+    ref = sdpa_decode(b.q, p.k_cache, p.v_cache, b.block_tables, b.context_lens, b.scale, dtype, hkv)
+    np.testing.assert_allclose(got, ref, rtol=0, atol=1e-12)
+
+
+def test_paged_equals_materialised_contiguous():
+    w = small_decode(21, [3, 16, 33, 64, 129], hq=6, hkv=3, d=32)
+    p, b = w.pool, w.decode
+    a = oracle.decode(b.q, p.k_cache, p.v_cache, b.block_tables, b.context_lens, b.scale, BF16)
+    c = oracle.naive_contiguous(b.q, p.k_cache, p.v_cache, b.block_tables, b.context_lens, b.scale, BF16)
+    np.testing.assert_allclose(a, c, rtol=0, atol=1e-12)
+    assert np.isfinite(a).all()        # NaN canaries in unowned slots and the poison block were never read
+
+
+def test_block_relabelling_invariance():
+    w = small_decode(22, [5, 31, 48, 77], hq=4, hkv=2, d=16, extra_blocks=6)
+    p, b = w.pool, w.decode
+    pi = wl.permutation(99, p.num_blocks)
+    k2 = np.empty_like(p.k_cache)
+    v2 = np.empty_like(p.v_cache)
+    k2[pi] = p.k_cache
+    v2[pi] = p.v_cache
+    bt2 = pi[b.block_tables].astype(np.int32)
+    a = oracle.decode(b.q, p.k_cache, p.v_cache, b.block_tables, b.context_lens, b.scale, BF16)
+    c = oracle.decode(b.q, k2, v2, bt2, b.context_lens, b.scale, BF16)
+    assert np.array_equal(a, c)
+
+
+def test_single_token_returns_v_exactly():
+    w = small_decode(23, [1, 1, 1], hq=4, hkv=2, d=16)
+    p, b = w.pool, w.decode
+    out = oracle.decode(b.q, p.k_cache, p.v_cache, b.block_tables, b.context_lens, b.scale, BF16)
+    for s in range(3):
+        v0 = f64(p.v_cache[b.block_tables[s, 0], 0], BF16)  # [Hkv, D]
+        for h in range(4):
+            assert np.array_equal(out[s, h], v0[h // 2])
+
+
+def test_uniform_v_returns_that_v():
+    w = small_decode(24, [50], hq=2, hkv=1, d=8)
+    p, b = w.pool, w.decode
+    vrow = wl.normal_bits(5, 8, BF16)
+    v = p.v_cache.copy()
+    v[:, :, 0, :] = vrow
+    out = oracle.decode(b.q, p.k_cache, v, b.block_tables, b.context_lens, b.scale, BF16)
+    np.testing.assert_allclose(out[0], np.broadcast_to(f64(vrow, BF16), (2, 8)), rtol=1e-12, atol=1e-15)
+
+
+def test_equal_scores_give_mean_of_v():
+    w = small_decode(25, [37], hq=2, hkv=1, d=8)
+    p, b = w.pool, w.decode
+    k = p.k_cache.copy()
+    k[:, :, 0, :] = wl.normal_bits(6, 8, BF16)        # every key row identical
+    out = oracle.decode(b.q, k, p.v_cache, b.block_tables, b.context_lens, b.scale, BF16)
+    V = f64(materialise(p.v_cache, b.block_tables[0], 37), BF16)[:, 0, :]
+    np.testing.assert_allclose(out[0, 0], V.mean(axis=0), rtol=0, atol=1e-13)
+
+
+def _manual_case(kvals, vvals, qvals, scale, dtype=F16, bs=4):
+    """One sequence, one head, exact small-integer inputs written straight into a pool."""
+    L, D = len(kvals), len(qvals)
+    nb = -(-L // bs) + 1
+    k = np.zeros((nb, bs, 1, D), np.uint16)
+    v = np.zeros((nb, bs, 1, D), np.uint16)
+    bt = np.array([[nb - 1 - i for i in range(nb - 1)]], np.int32)  # reversed physical order
+    for t in range(L):
+        k[bt[0, t // bs], t % bs, 0] = np.asarray(kvals[t], np.float16).view(np.uint16)
+        v[bt[0, t // bs], t % bs, 0] = np.asarray(vvals[t], np.float16).view(np.uint16)
+    q = np.asarray([[qvals]], np.float16).view(np.uint16)
+    return oracle.decode(q, k, v, bt, np.array([L], np.int32), scale, dtype, want_weights=True)
+
+
+def test_two_token_sigmoid_closed_form():
+    # s0 = scale*(q.k0) = 0.5*1 ; s1 = 0.5*3  ->  o = V0 + (V1 - V0) * sigmoid(s1 - s0)
+    out, w = _manual_case([[1, 0], [1, 1]], [[2, -1], [-4, 3]], [1, 2], 0.5)
+    sig = 1.0 / (1.0 + math.exp(-(1.5 - 0.5)))
+    expect = np.array([2 + (-6) * sig, -1 + 4 * sig])
+    np.testing.assert_allclose(out[0, 0], expect, rtol=0, atol=1e-14)
+    np.testing.assert_allclose(w[0, 0, :2], [1 - sig, sig], rtol=0, atol=1e-15)
+
+
+def test_weights_sum_to_one_and_follow_score_differences():
+    # integer q, k: s_t = scale * (q . k_t) exactly; ratio w_i / w_j = exp(s_i - s_j)
+    ks = [[1, 0, 0], [0, 1, 0], [0, 0, 1], [1, 1, 1], [-2, 0, 1]]
+    q = [1, -1, 2]
+    scores = [0.25 * sum(a * b for a, b in zip(q, kk)) for kk in ks]
+    out, w = _manual_case(ks, [[1, 0, 0]] * 5, q, 0.25)
+    w = w[0, 0, :5]
+    assert abs(w.sum() - 1.0) < 1e-15
+    for i in range(5):
+        for j in range(5):
+            assert abs(w[i] / w[j] - math.exp(scores[i] - scores[j])) < 1e-13
+
+
+def test_large_scores_are_stable_and_pick_the_max():
+    # scores of +-1000: a naive exp would overflow; the max-subtracted form gives a one-hot result
+    ks = [[10, 0], [0, 10], [-10, 0]]
+    vs = [[1, 2], [3, 4], [5, 6]]
+    out, w = _manual_case(ks, vs, [100, 1], 1.0)   # scores 1000, 10, -1000
+    assert np.isfinite(out).all()
+    np.testing.assert_allclose(out[0, 0], [1, 2], rtol=0, atol=1e-12)
+
+
+def test_brute_force_tiny_integer_inputs():
+    # every (L, D) with tiny integer inputs: exact scores; compare with a Fraction-free
+    # sum of exp over explicit scores (math.fsum), independently of the oracle's loops.
+    rng = np.random.default_rng(5)
+    for D in (1, 2, 4):
+        for L in range(1, 6):
+            ks = rng.integers(-3, 4, (L, D)).tolist()
+            vs = rng.integers(-3, 4, (L, D)).tolist()
+            q = rng.integers(-3, 4, D).tolist()
+            out, _ = _manual_case(ks, vs, q, 0.5)
+            s = [0.5 * sum(a * b for a, b in zip(q, kk)) for kk in ks]
+            e = [math.exp(x) for x in s]
+            den = math.fsum(e)
+            expect = [math.fsum(e[t] * vs[t][d] for t in range(L)) / den for d in range(D)]
+            np.testing.assert_allclose(out[0, 0], expect, rtol=1e-13, atol=1e-13)
+
+
+def test_gqa_groups_are_consecutive_heads():
+    # kv head 0 holds V = +1 everywhere, kv head 1 holds V = -1: query heads 0,1 must read +1, 2,3 must read -1
+    w = small_decode(26, [20, 9], hq=4, hkv=2, d=8)
+    p, b = w.pool, w.decode
+    v = p.v_cache.copy()
+    v[:, :, 0, :] = np.float32(1.0).view(np.uint32) >> 16
+    v[:, :, 1, :] = np.float32(-1.0).view(np.uint32) >> 16
+    out = oracle.decode(b.q, p.k_cache, v, b.block_tables, b.context_lens, b.scale, BF16)
+    assert np.array_equal(out[:, :2], np.ones((2, 2, 8)))
+    assert np.array_equal(out[:, 2:], -np.ones((2, 2, 8)))
+
+
+def test_zero_length_context_gives_zeros():
+    w = small_decode(27, [0 + 1, 5], hq=2, hkv=1, d=8)
+    p, b = w.pool, w.decode
+    cl = b.context_lens.copy()
+    cl[0] = 0
+    out = oracle.decode(b.q, p.k_cache, p.v_cache, b.block_tables, cl, b.scale, BF16)
+    assert np.array_equal(out[0], np.zeros((2, 8)))
+
+
+# --------------------------------------------------------------- split-K pieces
+
+
+def test_partitions_merge_to_the_full_result():
+    w = small_decode(31, [1, 255, 256, 257, 700, 1030], hq=4, hkv=2, d=16)
+    p, b = w.pool, w.decode
+    m, l, o = oracle.decode_partitions(b.q, p.k_cache, p.v_cache, b.block_tables, b.context_lens, b.scale, BF16, 256)
+    full = oracle.decode(b.q, p.k_cache, p.v_cache, b.block_tables, b.context_lens, b.scale, BF16)
+    np.testing.assert_allclose(oracle.merge_partitions(m, l, o), full, rtol=0, atol=1e-12)
+
+
+def test_each_partition_is_attention_over_its_token_range():
+    w = small_decode(32, [600], hq=2, hkv=1, d=16)
+    p, b = w.pool, w.decode
+    m, l, o = oracle.decode_partitions(b.q, p.k_cache, p.v_cache, b.block_tables, b.context_lens, b.scale, BF16, 256)
+    assert m.shape[2] == 3
+    for part in range(3):
+        n = min(256, 600 - 256 * part)
+        bt = np.ascontiguousarray(b.block_tables[:, 16 * part:])        # 256 tokens = 16 blocks of 16
+        ref = oracle.decode(b.q, p.k_cache, p.v_cache, bt, np.array([n], np.int32), b.scale, BF16)
+        np.testing.assert_allclose(o[0, :, part], ref[0], rtol=0, atol=1e-13)
+        # l_p = sum exp(s_t - m_p) >= 1 (the max term contributes exactly 1)
+        assert np.all(l[0, :, part] >= 1.0) and np.all(l[0, :, part] <= n)
+
+
+# --------------------------------------------------------------- prefill chunk
+
+
+def sdpa_prefill(pre, pool, n_kv_heads, dtype):
+    T, Hq, D = pre.q.shape
+    G = Hq // n_kv_heads
+    out = np.zeros((T, Hq, D))
+    for c in range(pre.num_chunks):
+        r0, r1 = int(pre.query_start_loc[c]), int(pre.query_start_loc[c + 1])
+        kv = int(pre.seq_lens[c])
+        ctx = kv - (r1 - r0)
+        K = torch.from_numpy(f64(materialise(pool.k_cache, pre.block_tables[c], kv), dtype)).permute(1, 0, 2)
+        V = torch.from_numpy(f64(materialise(pool.v_cache, pre.block_tables[c], kv), dtype)).permute(1, 0, 2)
+        q = torch.from_numpy(f64(pre.q[r0:r1], dtype)).permute(1, 0, 2)       # [Hq, q_len, D]
+        j = torch.arange(r1 - r0)[:, None]
+        t = torch.arange(kv)[None, :]
+        mask = t <= ctx + j                                                     # bottom-right causal
+        o = F.scaled_dot_product_attention(q, K.repeat_interleave(G, 0), V.repeat_interleave(G, 0),
+                                           attn_mask=mask, scale=pre.scale)
+        out[r0:r1] = o.permute(1, 0, 2).numpy()
+    return out
+
+
+def test_prefill_matches_torch_sdpa_bottom_right_mask():
+    w = wl.build_workload("p", 41, dtype=BF16, n_q_heads=4, n_kv_heads=2, head_dim=16,
+                          prefill_q_lens=[1, 7, 16, 33], prefill_ctx_lens=[0, 20, 5, 64])
+    got = oracle.prefill_chunk(w.prefill.q, w.pool.k_cache, w.pool.v_cache, w.prefill.block_tables,
+                               w.prefill.query_start_loc, w.prefill.seq_lens, w.prefill.scale, BF16)
+    ref = sdpa_prefill(w.prefill, w.pool, 2, BF16)
+    np.testing.assert_allclose(got, ref, rtol=0, atol=1e-12)
+
+
+def test_prefill_row_is_a_decode_row_with_shorter_context():
+    w = wl.build_workload("p", 42, dtype=BF16, n_q_heads=4, n_kv_heads=2, head_dim=16,
+                          prefill_q_lens=[9, 1], prefill_ctx_lens=[23, 0])
+    pre, p = w.prefill, w.pool
+    got = oracle.prefill_chunk(pre.q, p.k_cache, p.v_cache, pre.block_tables, pre.query_start_loc, pre.seq_lens,
+                               pre.scale, BF16)
+    for j in range(9):
+        ref = oracle.decode(pre.q[j:j + 1], p.k_cache, p.v_cache, pre.block_tables[:1],
+                            np.array([23 + j + 1], np.int32), pre.scale, BF16)
+        assert np.array_equal(got[j], ref[0])
+    # chunk with no cached context and one query row: attends to its own key only -> V0
+    v0 = f64(p.v_cache[pre.block_tables[1, 0], 0], BF16)
+    for h in range(4):
+        assert np.array_equal(got[9, h], v0[h // 2])
