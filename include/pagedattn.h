@@ -1,0 +1,191 @@
+/*
+ * pagedattn.h -- C ABI of libpagedattn: paged-KV-cache attention kernels for
+ * NVIDIA GB300 (sm_103a).
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - All tensor arguments are DEVICE pointers to contiguous row-major arrays
+ *    owned by the caller; the library never frees or keeps them past the call.
+ *  - dtype is PA_F16 (IEEE binary16) or PA_BF16 (bfloat16); q, key, value,
+ *    caches and out all share it.  Arithmetic is fp32 inside the kernels.
+ *  - The paged cache layout is k_cache, v_cache: [num_blocks, block_size,
+ *    n_kv_heads, head_dim] (MiniLLM Runtime, "CUDA PagedAttention scope" and
+ *    mini_engine, "Custom CUDA kernels": fixed-size KV blocks, per-request block
+ *    tables).  Token t of a sequence lives at physical block
+ *    block_tables[seq][t / block_size], offset t % block_size (MiniLLM Runtime,
+ *    "Core class relationships": logical token -> logical block + offset ->
+ *    block_table -> physical address).
+ *  - Supported shapes: block_size 16; head_dim 64 or 128; n_q_heads a multiple
+ *    of n_kv_heads with group size G = n_q_heads / n_kv_heads in {1, 2, 4, 8};
+ *    query head h reads KV head h / G.
+ *  - stream is a cudaStream_t (NULL = legacy default stream).  Calls only
+ *    validate on the host and enqueue kernels; they return before the GPU work
+ *    finishes.  A non-zero return means nothing was launched.
+ *  - Device pointers must be 16-byte aligned (PA_ERR_ALIGN otherwise).
+ *  - Values the host cannot see (slots, block ids, lengths) are checked in the
+ *    kernels: an out-of-range one is skipped (its reads return zeros, its write
+ *    is dropped) and a bit is set in the per-device error word read by
+ *    pa_device_errors().  No kernel traps or faults on bad indices.
+ */
+#ifndef PAGEDATTN_H
+#define PAGEDATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* dtype codes */
+#define PA_F16 0
+#define PA_BF16 1
+
+/* status codes returned by every entry point */
+#define PA_OK 0
+#define PA_ERR_NULL (-1)        /* a required pointer is NULL */
+#define PA_ERR_SHAPE (-2)       /* inconsistent sizes (e.g. n_q_heads % n_kv_heads != 0, negative counts) */
+#define PA_ERR_UNSUPPORTED (-3) /* a valid but unsupported shape or dtype */
+#define PA_ERR_CUDA (-4)        /* a CUDA runtime / driver call failed (launch, tensor-map encode) */
+#define PA_ERR_BOUNDS (-5)      /* host-visible sizes out of range (e.g. max_context_len > table capacity) */
+#define PA_ERR_ALIGN (-6)       /* a pointer is not 16-byte aligned */
+#define PA_ERR_WORKSPACE (-7)   /* split-K workspace missing or smaller than pa_decode_workspace_size() */
+
+/* bits of the per-device error word (pa_device_errors) */
+#define PA_DEVERR_SLOT 1u    /* a slot_mapping entry outside [0, num_blocks*block_size) and not -1 */
+#define PA_DEVERR_BLOCK 2u   /* a block-table entry outside [0, num_blocks) was needed */
+#define PA_DEVERR_LENGTH 4u  /* a context / kv length outside its allowed range */
+#define PA_DEVERR_TIMEOUT 8u /* a pipeline wait in a kernel exceeded its time limit; the kernel gave up */
+
+/* split-K piece length the pages use (mini_engine, "Custom CUDA kernels", v2) */
+#define PA_DEFAULT_PARTITION_TOKENS 256
+
+/*
+ * pa_reshape_and_cache -- KV-cache write.
+ * Source: mini_engine, "Custom CUDA kernels" (KV-cache write: scatters new K/V
+ * rows into their paged slots, skipping padded slots); miniserve, "Engine"
+ * (slot = block_id * block_size + offset).
+ *
+ *  key, value      [num_tokens, n_kv_heads, head_dim]            read
+ *  k_cache, v_cache [num_blocks, block_size, n_kv_heads, head_dim] written at the slots
+ *  slot_mapping    [num_tokens] int64; row i is copied to flat slot slot_mapping[i]
+ *                  of the cache viewed as [num_blocks*block_size, n_kv_heads, head_dim];
+ *                  -1 marks a padded row, which is skipped.  Slots must be distinct.
+ *  The copy is bit-exact.  num_tokens == 0 launches nothing and returns PA_OK.
+ */
+int pa_reshape_and_cache(const void* key, const void* value, void* k_cache, void* v_cache,
+                         const int64_t* slot_mapping, int64_t num_tokens, int n_kv_heads, int head_dim,
+                         int block_size, int64_t num_blocks, int dtype, void* stream);
+
+/*
+ * Split-K workspace size in bytes for pa_decode / pa_decode_splitk with these
+ * sizes (partition_tokens <= 0 means PA_DEFAULT_PARTITION_TOKENS).  Layout, each
+ * region starting on a 256-byte boundary, P = ceil(max_context_len / partition_tokens):
+ *   m [num_seqs, n_q_heads, P] float  -- per-piece max of scale*q.K (natural-log units)
+ *   l [num_seqs, n_q_heads, P] float  -- per-piece sum of exp(s - m)
+ *   o [num_seqs, n_q_heads, P, head_dim] float -- per-piece normalised output
+ * The caller owns it; its contents between calls are unspecified.
+ */
+size_t pa_decode_workspace_size(int num_seqs, int n_q_heads, int head_dim, int max_context_len,
+                                int partition_tokens);
+
+/*
+ * pa_decode -- decode attention over the paged cache, one query token per
+ * sequence, with the dispatcher choosing between the one-pass kernel
+ * (pa_decode_v1) and split-K (pa_decode_splitk).
+ * Source: mini_engine, "Custom CUDA kernels" (paged decode attention v1 / v2 and
+ * the dispatcher that takes v2 when few sequences or long contexts cannot fill
+ * the GPU); MiniLLM Runtime, "Core class relationships" (direct reads through
+ * the block table, no materialisation).
+ *
+ *  out   [num_seqs, n_q_heads, head_dim]   written
+ *  q     [num_seqs, n_q_heads, head_dim]   read
+ *  block_tables [num_seqs, max_blocks_per_seq] int32 physical block ids; entries
+ *                past ceil(context_lens[s]/block_size) are never read
+ *  context_lens [num_seqs] int32, tokens in the cache for each sequence (including
+ *                the one just written); 0 gives an all-zero output row
+ *  max_context_len  host-side upper bound of context_lens (sizes the split-K grid);
+ *                must be <= max_blocks_per_seq * block_size
+ *  scale       multiplier of q.K before the softmax (1/sqrt(head_dim) usually)
+ *  workspace   device scratch of at least pa_decode_workspace_size(num_seqs,
+ *              n_q_heads, head_dim, max_context_len, 0) bytes (may be NULL only
+ *              when the dispatcher picks the one-pass kernel; see pa_decode_plan)
+ *  out[s, h] = sum_t softmax_t(scale * q[s,h].K_t) V_t over t < context_lens[s],
+ *  K_t / V_t read from KV head h / G.  Stored as dtype, rounded to nearest even.
+ */
+int pa_decode(void* out, const void* q, const void* k_cache, const void* v_cache, const int32_t* block_tables,
+              int max_blocks_per_seq, const int32_t* context_lens, int max_context_len, int num_seqs,
+              int n_q_heads, int n_kv_heads, int head_dim, int block_size, int64_t num_blocks, float scale,
+              int dtype, void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * The dispatcher's decision for these sizes on the current device, without
+ * launching: returns 1 for the one-pass kernel, 2 for split-K, or a negative
+ * status.  *partition_tokens (if not NULL) receives the split-K piece length.
+ */
+int pa_decode_plan(int num_seqs, int n_kv_heads, int max_context_len, int* partition_tokens);
+
+/*
+ * pa_decode_v1 -- the one-pass decode kernel: one CTA per (sequence, KV head)
+ * streams the whole context, all G query heads of the group sharing each K/V
+ * load (mini_engine, "Custom CUDA kernels", v1).  Arguments as pa_decode; no
+ * workspace.
+ */
+int pa_decode_v1(void* out, const void* q, const void* k_cache, const void* v_cache, const int32_t* block_tables,
+                 int max_blocks_per_seq, const int32_t* context_lens, int num_seqs, int n_q_heads,
+                 int n_kv_heads, int head_dim, int block_size, int64_t num_blocks, float scale, int dtype,
+                 void* stream);
+
+/*
+ * pa_decode_splitk -- split-K decode (mini_engine, "Custom CUDA kernels", v2):
+ * the context is cut into pieces of partition_tokens tokens (a multiple of
+ * block_size; <= 0 means 256) processed by separate CTAs, each writing its max,
+ * exp-sum and normalised output to the workspace; a reduce kernel merges them
+ * with weights l_p * exp(m_p - max m).  Sequences with one piece are written
+ * directly.  Arguments as pa_decode.
+ */
+int pa_decode_splitk(void* out, const void* q, const void* k_cache, const void* v_cache,
+                     const int32_t* block_tables, int max_blocks_per_seq, const int32_t* context_lens,
+                     int max_context_len, int num_seqs, int n_q_heads, int n_kv_heads, int head_dim,
+                     int block_size, int64_t num_blocks, float scale, int dtype, int partition_tokens,
+                     void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * pa_prefill_chunk -- attention for ragged prefill chunks that attend to their
+ * earlier cached context, on the tcgen05 tensor cores (head_dim 128 only).
+ * Source: mini_engine, "Custom CUDA kernels" (paged prefill attention: tiled,
+ * online softmax, K/V straight from the paged cache, ragged batches, prefix
+ * hits and chunks over earlier chunks in one launch); miniserve, "Engine"
+ * (query_start_loc / block_table metadata, bottom-right causal mask).
+ *
+ *  out, q [total_q, n_q_heads, head_dim]; chunk c owns rows
+ *         [query_start_loc[c], query_start_loc[c+1])
+ *  query_start_loc [num_chunks+1] int32, seq_lens [num_chunks] int32 (kv length
+ *         = cached context + the chunk's own tokens, whose K/V must already be in
+ *         the cache, e.g. by pa_reshape_and_cache)
+ *  block_tables [num_chunks, max_blocks_per_seq] int32
+ *  max_q_len  host-side upper bound of the chunks' query lengths (sizes the grid)
+ *  Row j of chunk c attends to keys t <= seq_lens[c] - q_len_c + j.
+ */
+int pa_prefill_chunk(void* out, const void* q, const void* k_cache, const void* v_cache,
+                     const int32_t* block_tables, int max_blocks_per_seq, const int32_t* query_start_loc,
+                     const int32_t* seq_lens, int num_chunks, int max_q_len, int n_q_heads, int n_kv_heads,
+                     int head_dim, int block_size, int64_t num_blocks, float scale, int dtype, void* stream);
+
+/*
+ * Reads (and with clear != 0, resets) the error word of the current device.
+ * Synchronises the device first.  Returns the PA_DEVERR_* bits, or a negative
+ * status if the CUDA calls fail.
+ */
+int pa_device_errors(int clear);
+
+/* Human-readable name of a status code. */
+const char* pa_status_string(int status);
+
+/* Library version: major * 10000 + minor * 100 + patch. */
+int pa_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* PAGEDATTN_H */

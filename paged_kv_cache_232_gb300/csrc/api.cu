@@ -1,0 +1,343 @@
+// api.cu -- the C ABI of libpagedattn (include/pagedattn.h): host-side validation, tensor
+// maps for the paged caches, the decode dispatcher, the per-device error word, and the
+// KV-cache write launch.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "kv_write.cuh"
+#include "pa_launch.h"
+#include "pagedattn.h"
+
+// Error word written by the kernels (PA_DEVERR_* bits); one per device that loads the library.
+__device__ unsigned g_pa_device_errors;
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+
+struct DeviceState {
+    bool ready = false;
+    int sm_count = 0;
+    unsigned* err = nullptr;  // device address of g_pa_device_errors
+};
+
+std::mutex g_mu;
+DeviceState g_dev[kMaxDevices];
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+// Per-device set-up, done once with that device current.
+int device_state(DeviceState** out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return PA_ERR_CUDA;
+    std::lock_guard<std::mutex> lk(g_mu);
+    DeviceState& d = g_dev[dev];
+    if (!d.ready) {
+        if (cudaDeviceGetAttribute(&d.sm_count, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return PA_ERR_CUDA;
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_pa_device_errors) != cudaSuccess) return PA_ERR_CUDA;
+        d.err = static_cast<unsigned*>(p);
+        if (!g_encode) {
+            cudaDriverEntryPointQueryResult q;
+            void* fn = nullptr;
+            if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
+                    cudaSuccess ||
+                q != cudaDriverEntryPointSuccess || !fn)
+                return PA_ERR_CUDA;
+            g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+        }
+        d.ready = true;
+    }
+    *out = &d;
+    return PA_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Tensor map over a paged cache [num_blocks, block_size, n_kv_heads, head_dim]: box of
+// 64 columns x 1 head x block_size rows x 1 block, 128-byte swizzled (one TMA load moves
+// one 128-byte column slab of one head's block tile).  Out-of-range block ids read zeros.
+int encode_cache_map(CUtensorMap* m, const void* base, int dtype, int64_t num_blocks, int block_size,
+                     int n_kv_heads, int head_dim) {
+    cuuint64_t dims[4] = {(cuuint64_t)head_dim, (cuuint64_t)n_kv_heads, (cuuint64_t)block_size,
+                          (cuuint64_t)num_blocks};
+    cuuint64_t strides[3] = {(cuuint64_t)head_dim * 2, (cuuint64_t)n_kv_heads * head_dim * 2,
+                             (cuuint64_t)block_size * n_kv_heads * head_dim * 2};
+    cuuint32_t box[4] = {64, 1, (cuuint32_t)block_size, 1};
+    cuuint32_t estr[4] = {1, 1, 1, 1};
+    CUresult r = g_encode(m, dtype == PA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 4,
+                          const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? PA_OK : PA_ERR_CUDA;
+}
+
+int check_heads(int n_q_heads, int n_kv_heads, int head_dim, int block_size, int dtype) {
+    if (n_q_heads <= 0 || n_kv_heads <= 0 || n_q_heads % n_kv_heads) return PA_ERR_SHAPE;
+    const int G = n_q_heads / n_kv_heads;
+    if (G != 1 && G != 2 && G != 4 && G != 8) return PA_ERR_UNSUPPORTED;
+    if (head_dim != 64 && head_dim != 128) return PA_ERR_UNSUPPORTED;
+    if (block_size != 16) return PA_ERR_UNSUPPORTED;
+    if (dtype != PA_F16 && dtype != PA_BF16) return PA_ERR_UNSUPPORTED;
+    return PA_OK;
+}
+
+int partition_or_default(int part) { return part > 0 ? part : PA_DEFAULT_PARTITION_TOKENS; }
+
+size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+struct WsLayout {
+    size_t m_off, l_off, o_off, total;
+};
+
+WsLayout ws_layout(int num_seqs, int n_q_heads, int head_dim, int max_parts) {
+    const size_t rows = (size_t)num_seqs * n_q_heads * max_parts;
+    WsLayout w;
+    w.m_off = 0;
+    w.l_off = align256(rows * sizeof(float));
+    w.o_off = w.l_off + align256(rows * sizeof(float));
+    w.total = w.o_off + align256(rows * head_dim * sizeof(float));
+    return w;
+}
+
+// Shared argument checks of the decode entry points.
+int check_decode(const void* out, const void* q, const void* k_cache, const void* v_cache, const int32_t* bt,
+                 int max_blocks_per_seq, const int32_t* context_lens, int num_seqs, int n_q_heads, int n_kv_heads,
+                 int head_dim, int block_size, int64_t num_blocks, int dtype) {
+    if (num_seqs < 0 || max_blocks_per_seq <= 0 || num_blocks <= 0) return PA_ERR_SHAPE;
+    int st = check_heads(n_q_heads, n_kv_heads, head_dim, block_size, dtype);
+    if (st != PA_OK) return st;
+    if (num_blocks > INT32_MAX) return PA_ERR_UNSUPPORTED;
+    if ((int64_t)max_blocks_per_seq * block_size > INT32_MAX) return PA_ERR_UNSUPPORTED;
+    if (num_seqs == 0) return PA_OK;
+    if (!out || !q || !k_cache || !v_cache || !bt || !context_lens) return PA_ERR_NULL;
+    if (!aligned16(out) || !aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache)) return PA_ERR_ALIGN;
+    return PA_OK;
+}
+
+int decode_impl(void* out, const void* q, const void* k_cache, const void* v_cache, const int32_t* block_tables,
+                int max_blocks_per_seq, const int32_t* context_lens, int max_context_len, int num_seqs,
+                int n_q_heads, int n_kv_heads, int head_dim, int block_size, int64_t num_blocks, float scale,
+                int dtype, int part_tokens, void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+    int st = check_decode(out, q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens, num_seqs,
+                          n_q_heads, n_kv_heads, head_dim, block_size, num_blocks, dtype);
+    if (st != PA_OK || num_seqs == 0) return st;
+    if (!std::isfinite(scale)) return PA_ERR_SHAPE;
+    DeviceState* dev = nullptr;
+    if ((st = device_state(&dev)) != PA_OK) return st;
+
+    pa::DecodeParams p{};
+    p.out = out;
+    p.q = q;
+    p.block_tables = block_tables;
+    p.context_lens = context_lens;
+    p.err = dev->err;
+    p.num_seqs = num_seqs;
+    p.n_q_heads = n_q_heads;
+    p.n_kv_heads = n_kv_heads;
+    p.max_blocks_per_seq = max_blocks_per_seq;
+    p.num_blocks = (int)num_blocks;
+    p.qk_scale_log2 = scale * 1.4426950408889634f;
+    const int units = num_seqs * n_kv_heads;
+    int grid = units;
+    bool reduce = false;
+    if (part_tokens > 0) {
+        if (part_tokens % block_size) return PA_ERR_UNSUPPORTED;
+        if (max_context_len < 0 || (int64_t)max_context_len > (int64_t)max_blocks_per_seq * block_size)
+            return PA_ERR_BOUNDS;
+        const int max_parts = max_context_len > 0 ? (max_context_len + part_tokens - 1) / part_tokens : 1;
+        if ((int64_t)units * max_parts > INT32_MAX) return PA_ERR_UNSUPPORTED;
+        const WsLayout w = ws_layout(num_seqs, n_q_heads, head_dim, max_parts);
+        if (max_parts > 1) {
+            if (!workspace || workspace_bytes < w.total) return PA_ERR_WORKSPACE;
+            if (!aligned16(workspace)) return PA_ERR_ALIGN;
+            char* base = static_cast<char*>(workspace);
+            p.ws_m = reinterpret_cast<float*>(base + w.m_off);
+            p.ws_l = reinterpret_cast<float*>(base + w.l_off);
+            p.ws_o = reinterpret_cast<float*>(base + w.o_off);
+            reduce = true;
+        }
+        p.part_tokens = part_tokens;
+        p.max_parts = max_parts;
+        grid = units * max_parts;
+    } else {
+        p.part_tokens = 0;
+        p.max_parts = 1;
+    }
+    CUtensorMap tk, tv;
+    if ((st = encode_cache_map(&tk, k_cache, dtype, num_blocks, block_size, n_kv_heads, head_dim)) != PA_OK) return st;
+    if ((st = encode_cache_map(&tv, v_cache, dtype, num_blocks, block_size, n_kv_heads, head_dim)) != PA_OK) return st;
+    cudaError_t e = pa::launch_decode(dtype == PA_BF16, head_dim, n_q_heads / n_kv_heads, p, tk, tv, grid, reduce,
+                                      stream);
+    return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
+// Dispatcher (mini_engine, "Custom CUDA kernels": split-K when few sequences or long
+// contexts cannot fill the GPU, the one-pass kernel when there is enough parallelism).
+// The thresholds are this library's, set from GB300 measurements.
+int plan(int num_seqs, int n_kv_heads, int max_context_len, int sm_count, int* part_tokens) {
+    const int units = num_seqs * n_kv_heads;
+    if (part_tokens) *part_tokens = PA_DEFAULT_PARTITION_TOKENS;
+    if (max_context_len <= PA_DEFAULT_PARTITION_TOKENS) return 1;
+    if (units >= 4 * sm_count && max_context_len <= 4096) return 1;
+    return 2;
+}
+
+}  // namespace
+
+extern "C" {
+
+int pa_version(void) { return 100; }
+
+const char* pa_status_string(int status) {
+    switch (status) {
+        case PA_OK: return "ok";
+        case PA_ERR_NULL: return "null pointer argument";
+        case PA_ERR_SHAPE: return "inconsistent sizes";
+        case PA_ERR_UNSUPPORTED: return "unsupported shape or dtype";
+        case PA_ERR_CUDA: return "CUDA call failed";
+        case PA_ERR_BOUNDS: return "size out of range";
+        case PA_ERR_ALIGN: return "pointer not 16-byte aligned";
+        case PA_ERR_WORKSPACE: return "split-K workspace missing or too small";
+        default: return "unknown status";
+    }
+}
+
+int pa_device_errors(int clear) {
+    DeviceState* dev = nullptr;
+    int st = device_state(&dev);
+    if (st != PA_OK) return st;
+    if (cudaDeviceSynchronize() != cudaSuccess) return PA_ERR_CUDA;
+    unsigned v = 0;
+    if (cudaMemcpyFromSymbol(&v, g_pa_device_errors, sizeof(v)) != cudaSuccess) return PA_ERR_CUDA;
+    if (clear) {
+        unsigned z = 0;
+        if (cudaMemcpyToSymbol(g_pa_device_errors, &z, sizeof(z)) != cudaSuccess) return PA_ERR_CUDA;
+    }
+    return (int)v;
+}
+
+int pa_reshape_and_cache(const void* key, const void* value, void* k_cache, void* v_cache,
+                         const int64_t* slot_mapping, int64_t num_tokens, int n_kv_heads, int head_dim,
+                         int block_size, int64_t num_blocks, int dtype, void* stream) {
+    if (num_tokens < 0 || n_kv_heads <= 0 || head_dim <= 0 || block_size <= 0 || num_blocks <= 0)
+        return PA_ERR_SHAPE;
+    if (dtype != PA_F16 && dtype != PA_BF16) return PA_ERR_UNSUPPORTED;
+    const int64_t row_bytes = (int64_t)n_kv_heads * head_dim * 2;
+    if (row_bytes % 16 || row_bytes / 16 > 512) return PA_ERR_UNSUPPORTED;  // one thread per 16-byte chunk, K and V
+    if (num_tokens == 0) return PA_OK;
+    if (!key || !value || !k_cache || !v_cache || !slot_mapping) return PA_ERR_NULL;
+    if (!aligned16(key) || !aligned16(value) || !aligned16(k_cache) || !aligned16(v_cache)) return PA_ERR_ALIGN;
+    DeviceState* dev = nullptr;
+    int st = device_state(&dev);
+    if (st != PA_OK) return st;
+    const int row_vecs = (int)(row_bytes / 16);
+    const int threads = 2 * row_vecs;
+    const int64_t iters = (num_tokens + pa::kKvWriteRowsPerIter - 1) / pa::kKvWriteRowsPerIter;
+    const int64_t max_grid = (int64_t)dev->sm_count * (2048 / threads);
+    const int grid = (int)(iters < max_grid ? iters : max_grid);
+    pa::kv_write_kernel<<<grid, threads, 0, static_cast<cudaStream_t>(stream)>>>(
+        static_cast<const uint4*>(key), static_cast<const uint4*>(value), static_cast<uint4*>(k_cache),
+        static_cast<uint4*>(v_cache), slot_mapping, num_tokens, row_vecs, num_blocks * block_size, dev->err);
+    return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
+size_t pa_decode_workspace_size(int num_seqs, int n_q_heads, int head_dim, int max_context_len,
+                                int partition_tokens) {
+    if (num_seqs <= 0 || n_q_heads <= 0 || head_dim <= 0 || max_context_len < 0) return 0;
+    const int part = partition_or_default(partition_tokens);
+    const int max_parts = max_context_len > 0 ? (max_context_len + part - 1) / part : 1;
+    if (max_parts <= 1) return 0;
+    return ws_layout(num_seqs, n_q_heads, head_dim, max_parts).total;
+}
+
+int pa_decode_plan(int num_seqs, int n_kv_heads, int max_context_len, int* partition_tokens) {
+    if (num_seqs < 0 || n_kv_heads <= 0 || max_context_len < 0) return PA_ERR_SHAPE;
+    DeviceState* dev = nullptr;
+    int st = device_state(&dev);
+    if (st != PA_OK) return st;
+    return plan(num_seqs, n_kv_heads, max_context_len, dev->sm_count, partition_tokens);
+}
+
+int pa_decode_v1(void* out, const void* q, const void* k_cache, const void* v_cache, const int32_t* block_tables,
+                 int max_blocks_per_seq, const int32_t* context_lens, int num_seqs, int n_q_heads,
+                 int n_kv_heads, int head_dim, int block_size, int64_t num_blocks, float scale, int dtype,
+                 void* stream) {
+    return decode_impl(out, q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens,
+                       max_blocks_per_seq * block_size, num_seqs, n_q_heads, n_kv_heads, head_dim, block_size,
+                       num_blocks, scale, dtype, 0, nullptr, 0, static_cast<cudaStream_t>(stream));
+}
+
+int pa_decode_splitk(void* out, const void* q, const void* k_cache, const void* v_cache,
+                     const int32_t* block_tables, int max_blocks_per_seq, const int32_t* context_lens,
+                     int max_context_len, int num_seqs, int n_q_heads, int n_kv_heads, int head_dim,
+                     int block_size, int64_t num_blocks, float scale, int dtype, int partition_tokens,
+                     void* workspace, size_t workspace_bytes, void* stream) {
+    return decode_impl(out, q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens, max_context_len,
+                       num_seqs, n_q_heads, n_kv_heads, head_dim, block_size, num_blocks, scale, dtype,
+                       partition_or_default(partition_tokens), workspace, workspace_bytes,
+                       static_cast<cudaStream_t>(stream));
+}
+
+int pa_decode(void* out, const void* q, const void* k_cache, const void* v_cache, const int32_t* block_tables,
+              int max_blocks_per_seq, const int32_t* context_lens, int max_context_len, int num_seqs,
+              int n_q_heads, int n_kv_heads, int head_dim, int block_size, int64_t num_blocks, float scale,
+              int dtype, void* workspace, size_t workspace_bytes, void* stream) {
+    if (max_context_len < 0 || (int64_t)max_context_len > (int64_t)max_blocks_per_seq * block_size)
+        return PA_ERR_BOUNDS;
+    int part = 0;
+    const int which = pa_decode_plan(num_seqs, n_kv_heads > 0 ? n_kv_heads : 1, max_context_len, &part);
+    if (which < 0) return which;
+    if (which == 1)
+        return pa_decode_v1(out, q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens, num_seqs,
+                            n_q_heads, n_kv_heads, head_dim, block_size, num_blocks, scale, dtype, stream);
+    return pa_decode_splitk(out, q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens, max_context_len,
+                            num_seqs, n_q_heads, n_kv_heads, head_dim, block_size, num_blocks, scale, dtype, part,
+                            workspace, workspace_bytes, stream);
+}
+
+int pa_prefill_chunk(void* out, const void* q, const void* k_cache, const void* v_cache,
+                     const int32_t* block_tables, int max_blocks_per_seq, const int32_t* query_start_loc,
+                     const int32_t* seq_lens, int num_chunks, int max_q_len, int n_q_heads, int n_kv_heads,
+                     int head_dim, int block_size, int64_t num_blocks, float scale, int dtype, void* stream) {
+    if (num_chunks < 0 || max_q_len < 0 || max_blocks_per_seq <= 0 || num_blocks <= 0) return PA_ERR_SHAPE;
+    int st = check_heads(n_q_heads, n_kv_heads, head_dim, block_size, dtype);
+    if (st != PA_OK) return st;
+    if (head_dim != 128) return PA_ERR_UNSUPPORTED;
+    if (num_blocks > INT32_MAX) return PA_ERR_UNSUPPORTED;
+    if (num_chunks == 0 || max_q_len == 0) return PA_OK;
+    if (!out || !q || !k_cache || !v_cache || !block_tables || !query_start_loc || !seq_lens) return PA_ERR_NULL;
+    if (!aligned16(out) || !aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache)) return PA_ERR_ALIGN;
+    if (!std::isfinite(scale)) return PA_ERR_SHAPE;
+    DeviceState* dev = nullptr;
+    if ((st = device_state(&dev)) != PA_OK) return st;
+    const int G = n_q_heads / n_kv_heads;
+    pa::PrefillParams p{};
+    p.out = out;
+    p.q = q;
+    p.block_tables = block_tables;
+    p.query_start_loc = query_start_loc;
+    p.seq_lens = seq_lens;
+    p.err = dev->err;
+    p.num_chunks = num_chunks;
+    p.n_q_heads = n_q_heads;
+    p.n_kv_heads = n_kv_heads;
+    p.max_blocks_per_seq = max_blocks_per_seq;
+    p.num_blocks = (int)num_blocks;
+    p.tiles_per_chunk = (int)(((int64_t)max_q_len * G + 127) / 128);
+    p.qk_scale_log2 = scale * 1.4426950408889634f;
+    if ((int64_t)p.tiles_per_chunk * num_chunks * n_kv_heads > INT32_MAX) return PA_ERR_UNSUPPORTED;
+    CUtensorMap tk, tv;
+    if ((st = encode_cache_map(&tk, k_cache, dtype, num_blocks, block_size, n_kv_heads, head_dim)) != PA_OK) return st;
+    if ((st = encode_cache_map(&tv, v_cache, dtype, num_blocks, block_size, n_kv_heads, head_dim)) != PA_OK) return st;
+    cudaError_t e = pa::launch_prefill(dtype == PA_BF16, head_dim, G, p, tk, tv, static_cast<cudaStream_t>(stream));
+    if (e == cudaErrorNotSupported) return PA_ERR_UNSUPPORTED;
+    return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
+}  // extern "C"

@@ -1,0 +1,515 @@
+// decode.cuh -- paged decode attention for sm_103a.
+//
+// What is computed (mini_engine, "Custom CUDA kernels", paged decode attention v1/v2;
+// MiniLLM Runtime, "Core class relationships"): for sequence s, query head h and KV head
+// g = h / G, over tokens t of the work unit's range, each token translated through the
+// block table (physical block block_tables[s][t / 16], offset t % 16),
+//     out[s, h] = sum_t exp(s_t - m) V_t / sum_t exp(s_t - m),  s_t = scale * q[s, h] . K_t.
+//
+// GB300 design (not the pages' sm_80 one):
+//  * One CTA per work unit (s, g, piece).  A piece is the whole context (one-pass kernel)
+//    or a run of `part_tokens` tokens (split-K).  All G query heads of the group are
+//    handled by the CTA, so each K/V byte is fetched from HBM once.
+//  * A producer warp streams the unit's 16-token blocks with TMA: one 4-D tensor-map
+//    load per 128-byte column slab of the [16 rows x head_dim] K and V tiles, 128-byte
+//    swizzled, into an NST-stage shared-memory ring guarded by full/empty mbarriers.
+//    Block ids are read 32 at a time by the producer warp (block-table prefetch).
+//  * Four consumer warps take whole blocks round-robin.  For q.K, 8 lanes split a
+//    token's head_dim and 4 tokens run side by side; the 4*G partial dots are reduced
+//    across the 8 lanes with a transpose-reduce (each shuffle halves the values a lane
+//    keeps), so one lane ends with finished scores of a single head.  Online softmax
+//    (running max m, sum l, base-2 exponent with log2(e) folded into q) uses shuffles
+//    across the lanes of a head.  For P.V each lane owns 8 columns of head_dim for all G
+//    heads and walks its tokens; probabilities come through a small per-warp buffer.
+//  * At the end the four warps' (m, l, o) are merged in shared memory and the CTA
+//    writes either the final row (rounded to nearest even) or its piece's (m, l, o) for
+//    the reduce kernel.
+#pragma once
+
+#include "pa_device.cuh"
+
+namespace pa {
+
+struct DecodeParams {
+    void* out;                 // [S, Hq, D] T
+    const void* q;             // [S, Hq, D] T
+    const int32_t* block_tables;
+    const int32_t* context_lens;
+    float* ws_m;               // [S, Hq, P]   (split-K only)
+    float* ws_l;               // [S, Hq, P]
+    float* ws_o;               // [S, Hq, P, D]
+    unsigned* err;
+    int num_seqs, n_q_heads, n_kv_heads, max_blocks_per_seq;
+    int part_tokens;           // 0: whole context in one CTA
+    int max_parts;             // P (grid pieces per (s, g))
+    int num_blocks;
+    float qk_scale_log2;       // scale * log2(e)
+};
+
+template <int D, int G, bool BF16>
+struct DecodeCfg {
+    static constexpr int BS = 16;
+    static constexpr int HALVES = D / 64;             // 128-byte column slabs per row
+    static constexpr int SLAB_BYTES = BS * 128;       // one slab of one block tile
+    static constexpr int TILE_BYTES = HALVES * SLAB_BYTES;
+    static constexpr int STAGE_BYTES = 2 * TILE_BYTES;  // K tile + V tile
+    static constexpr int NST = (D == 128) ? 8 : 16;
+    static constexpr int NCW = 4;                     // consumer warps
+    static constexpr int THREADS = (NCW + 1) * 32;
+    static constexpr int CPL = HALVES;                // 16-byte chunks per lane for q.K
+    static constexpr int NV = 4 * G;                  // partial dots per lane before reduction
+    static constexpr int R = (NV >= 8) ? NV / 8 : 1;  // finished scores per lane
+    static constexpr int CR = D / 8;                  // 16-byte chunks per row
+    static constexpr int TGP = 32 / CR;               // token groups for P.V
+    static constexpr int TPL = BS / TGP;              // tokens per lane for P.V
+    // shared memory: ring | p buffers | alpha | barriers
+    static constexpr int RING_BYTES = NST * STAGE_BYTES;
+    static constexpr int P_BYTES = NCW * BS * G * 4;
+    static constexpr int A_BYTES = NCW * 8 * 4;
+    static constexpr int MERGE_BYTES = NCW * (G * D + 2 * G) * 4;  // aliases the ring
+    static constexpr int BAR_OFF = RING_BYTES + P_BYTES + A_BYTES;
+    static constexpr int SMEM_BYTES = BAR_OFF + 2 * NST * 8 + 1024;  // + alignment slack
+    static_assert(MERGE_BYTES <= RING_BYTES, "merge area must fit in the ring");
+    static_assert(D == 64 || D == 128, "head_dim 64 or 128");
+    static_assert(G == 1 || G == 2 || G == 4 || G == 8, "group size 1, 2, 4 or 8");
+};
+
+// One step of the transpose-reduce: the lane keeps half of its N values (the upper half if
+// `bit` is set in its lane id) and adds the partner's copy of the same half.
+template <int N>
+__device__ __forceinline__ void tr_step(float* v, int lane, int bit) {
+    const bool up = (lane & bit) != 0;
+#pragma unroll
+    for (int k = 0; k < N / 2; ++k) {
+        float send = up ? v[k] : v[k + N / 2];
+        float keep = up ? v[k + N / 2] : v[k];
+        v[k] = keep + __shfl_xor_sync(0xffffffffu, send, bit);
+    }
+}
+
+// Reduce the 4*G partial dots over the 8 lanes that share a token (lane bits 0..2).
+// Afterwards the lane holds R finished dots with flat indices base + k (index = h*4 + i).
+template <int G>
+__device__ __forceinline__ int transpose_reduce(float* v, int lane) {
+    constexpr int N0 = 4 * G;
+    int base = 0;
+    if constexpr (N0 >= 2) { tr_step<N0>(v, lane, 4); base += (lane & 4) ? N0 / 2 : 0; }
+    if constexpr (N0 / 2 >= 2) { tr_step<N0 / 2>(v, lane, 2); base += (lane & 2) ? N0 / 4 : 0; }
+    if constexpr (N0 / 4 >= 2) {
+        tr_step<N0 / 4>(v, lane, 1);
+        base += (lane & 1) ? N0 / 8 : 0;
+    } else {
+        v[0] += __shfl_xor_sync(0xffffffffu, v[0], 1);  // G == 1: both lanes end with the same sum
+    }
+    return base;
+}
+
+// xor-masks over which the lanes holding one head's scores are spread (tg bits 3,4 plus
+// the dl bits that do not encode the head).  For sums, G == 1 skips bit 0 (duplicates).
+template <int G>
+__device__ __forceinline__ float head_max(float x) {
+    if constexpr (G <= 4) x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, 1));
+    if constexpr (G <= 2) x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, 2));
+    if constexpr (G == 1) x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, 4));
+    x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, 8));
+    x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, 16));
+    return x;
+}
+
+template <int G>
+__device__ __forceinline__ float head_sum(float x) {
+    if constexpr (G == 2 || G == 4) x += __shfl_xor_sync(0xffffffffu, x, 1);
+    if constexpr (G <= 2) x += __shfl_xor_sync(0xffffffffu, x, 2);
+    if constexpr (G == 1) x += __shfl_xor_sync(0xffffffffu, x, 4);
+    x += __shfl_xor_sync(0xffffffffu, x, 8);
+    x += __shfl_xor_sync(0xffffffffu, x, 16);
+    return x;
+}
+
+template <int D, int G, bool BF16>
+__global__ void __launch_bounds__(DecodeCfg<D, G, BF16>::THREADS)
+decode_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV) {
+    using C = DecodeCfg<D, G, BF16>;
+    using F = F16x2<BF16>;
+    extern __shared__ __align__(1024) unsigned char smem_raw[];
+    // 1024-byte alignment for the 128-byte swizzle pattern of TMA
+    unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const uint32_t ring = smem_addr(smem);
+    float* p_buf = reinterpret_cast<float*>(smem + C::RING_BYTES);
+    float* a_buf = reinterpret_cast<float*>(smem + C::RING_BYTES + C::P_BYTES);
+    const uint32_t bar_full = ring + C::BAR_OFF;
+    const uint32_t bar_empty = bar_full + C::NST * 8;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int units = p.num_seqs * p.n_kv_heads;
+    const int piece = blockIdx.x / units;
+    const int sg = blockIdx.x - piece * units;
+    const int s = sg / p.n_kv_heads, g = sg - s * p.n_kv_heads;
+
+    // context length, clamped to what the table (and the split-K grid) can address
+    int L = __ldg(p.context_lens + s);
+    int cap = p.max_blocks_per_seq * C::BS;
+    if (p.part_tokens > 0 && p.max_parts * p.part_tokens < cap) cap = p.max_parts * p.part_tokens;
+    if (L < 0 || L > cap) {
+        if (piece == 0 && g == 0 && threadIdx.x == 0) flag_error(p.err, PA_DEVERR_LENGTH);
+        L = L < 0 ? 0 : cap;
+    }
+    const int t_begin = p.part_tokens > 0 ? piece * p.part_tokens : 0;
+    const int t_end = p.part_tokens > 0 ? min(L, t_begin + p.part_tokens) : L;
+    const int n_parts = p.part_tokens > 0 ? (L + p.part_tokens - 1) / p.part_tokens : 1;
+    if (t_begin >= t_end && piece > 0) return;  // split-K piece past this sequence's context
+    const int nblk = (t_end - t_begin + C::BS - 1) / C::BS;
+    const int blk0 = t_begin / C::BS;
+    const bool direct = (n_parts <= 1);
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < C::NST; ++i) {
+            mbar_init(bar_full + 8 * i, 1);
+            mbar_init(bar_empty + 8 * i, 1);
+        }
+        fence_barrier_init();
+    }
+    __syncthreads();
+
+    if (warp == C::NCW) {
+        // ------------------------------------------------------------ producer warp
+        if (lane == 0) {
+            tma_prefetch_desc(&tmK);
+            tma_prefetch_desc(&tmV);
+        }
+        const uint64_t pol = l2_policy_evict_first();
+        const int32_t* bt = p.block_tables + (size_t)s * p.max_blocks_per_seq + blk0;
+        bool ok = true;
+        for (int b0 = 0; b0 < nblk && ok; b0 += 32) {
+            int my = 0;
+            if (b0 + lane < nblk) {
+                my = __ldg(bt + b0 + lane);
+                if (my < 0 || my >= p.num_blocks) {
+                    flag_error(p.err, PA_DEVERR_BLOCK);
+                    my = p.num_blocks;  // outside the tensor map: TMA fills zeros
+                }
+            }
+            const int nb = min(32, nblk - b0);
+            for (int j = 0; j < nb; ++j) {
+                const int blk = __shfl_sync(0xffffffffu, my, j);
+                const int b = b0 + j;
+                const int st = b % C::NST;
+                const uint32_t ph = (b / C::NST) & 1;
+                if (lane == 0) {
+                    if (b >= C::NST && !mbar_wait(bar_empty + 8 * st, ph ^ 1, p.err)) ok = false;
+                    if (ok) {
+                        const uint32_t dst = ring + st * C::STAGE_BYTES;
+                        mbar_arrive_expect_tx(bar_full + 8 * st, C::STAGE_BYTES);
+#pragma unroll
+                        for (int hf = 0; hf < C::HALVES; ++hf)
+                            tma_load_4d(dst + hf * C::SLAB_BYTES, &tmK, hf * 64, g, 0, blk, bar_full + 8 * st, pol);
+#pragma unroll
+                        for (int hf = 0; hf < C::HALVES; ++hf)
+                            tma_load_4d(dst + C::TILE_BYTES + hf * C::SLAB_BYTES, &tmV, hf * 64, g, 0, blk,
+                                        bar_full + 8 * st, pol);
+                    }
+                }
+                ok = __shfl_sync(0xffffffffu, ok, 0);
+                if (!ok) break;
+            }
+        }
+        return;
+    }
+
+    // ---------------------------------------------------------------- consumer warps
+    const int tg = lane >> 3, dl = lane & 7;  // q.K layout: token group, lane within token
+    // q for the G heads of this group, this lane's CPL chunks, pre-scaled by scale*log2(e)
+    float qf[G][C::CPL][8];
+    int chunk_col[C::CPL];  // first column (element index) of each of this lane's chunks
+#pragma unroll
+    for (int j = 0; j < C::CPL; ++j) {
+        const int half = (C::HALVES == 2) ? (dl >> 2) : 0;
+        const int c = (C::HALVES == 2) ? ((2 * (dl & 3) + half + j) & 7) : dl;
+        chunk_col[j] = half * 64 + c * 8;
+    }
+    {
+        const uint16_t* qrow = static_cast<const uint16_t*>(p.q) + ((size_t)s * p.n_q_heads + (size_t)g * G) * D;
+#pragma unroll
+        for (int h = 0; h < G; ++h)
+#pragma unroll
+            for (int j = 0; j < C::CPL; ++j) {
+                uint4 raw = ldg_nc_128(qrow + h * D + chunk_col[j]);
+                unpack8<BF16>(raw, qf[h][j]);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) qf[h][j][e] *= p.qk_scale_log2;
+            }
+    }
+
+    // this lane's head in the reduced-score layout, and whether it reports that head
+    const int n0 = 4 * G;
+    int my_h;
+    {
+        int base = ((lane & 4) ? n0 / 2 : 0) + ((lane & 2) ? n0 / 4 : 0) + ((n0 >= 8 && (lane & 1)) ? n0 / 8 : 0);
+        my_h = base / 4;
+    }
+    const int hmask = (G == 1) ? 0 : (G == 2) ? 4 : (G == 4) ? 6 : 7;
+    const bool rep = (tg == 0) && ((dl & ~hmask) == 0);
+
+    float m_run = -INFINITY, l_run = 0.f;
+    float o[G][8];
+#pragma unroll
+    for (int h = 0; h < G; ++h)
+#pragma unroll
+        for (int e = 0; e < 8; ++e) o[h][e] = 0.f;
+
+    const int dg = lane % C::CR, tgp = lane / C::CR;  // P.V layout
+    float* pw = p_buf + warp * C::BS * G;
+    float* aw = a_buf + warp * 8;
+
+    bool ok = true;
+    for (int b = warp; b < nblk; b += C::NCW) {
+        const int st = b % C::NST;
+        const uint32_t ph = (b / C::NST) & 1;
+        const bool arrived = mbar_wait(bar_full + 8 * st, ph, p.err);
+        if (!__all_sync(0xffffffffu, arrived)) { ok = false; break; }  // leave the loop warp-uniformly
+        const uint32_t kt = ring + st * C::STAGE_BYTES;
+        const uint32_t vt = kt + C::TILE_BYTES;
+        const int nvalid = min(C::BS, t_end - (t_begin + b * C::BS));
+
+        // ---- q.K: 4 tokens x G heads of partial dots per lane
+        float acc[4 * G];
+#pragma unroll
+        for (int k = 0; k < 4 * G; ++k) acc[k] = 0.f;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int t = tg + 4 * i;
+#pragma unroll
+            for (int j = 0; j < C::CPL; ++j) {
+                const int half = chunk_col[j] >> 6, c = (chunk_col[j] >> 3) & 7;
+                uint4 raw = lds128(kt + half * C::SLAB_BYTES + swz128(t, c));
+                float kf[8];
+                unpack8<BF16>(raw, kf);
+#pragma unroll
+                for (int h = 0; h < G; ++h)
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) acc[h * 4 + i] = fmaf(qf[h][j][e], kf[e], acc[h * 4 + i]);
+            }
+        }
+        const int base = transpose_reduce<G>(acc, lane);
+
+        // ---- online softmax for this lane's head over the block's 16 tokens
+        float sc[C::R];
+        float bmax = -INFINITY;
+#pragma unroll
+        for (int r = 0; r < C::R; ++r) {
+            const int i = (base + r) & 3;
+            const int t = tg + 4 * i;
+            sc[r] = (t < nvalid) ? acc[r] : -INFINITY;
+            bmax = fmaxf(bmax, sc[r]);
+        }
+        bmax = head_max<G>(bmax);
+        const float m_new = fmaxf(m_run, bmax);
+        const float alpha = (m_new == -INFINITY) ? 1.f : exp2f(m_run - m_new);
+        float psum = 0.f;
+#pragma unroll
+        for (int r = 0; r < C::R; ++r) {
+            const int i = (base + r) & 3;
+            const int t = tg + 4 * i;
+            const float pr = (m_new == -INFINITY) ? 0.f : exp2f(sc[r] - m_new);
+            psum += pr;
+            if (G > 1 || (lane & 1) == 0) pw[t * G + my_h] = pr;
+        }
+        psum = head_sum<G>(psum);
+        l_run = l_run * alpha + psum;
+        m_run = m_new;
+        if (rep) aw[my_h] = alpha;
+        __syncwarp();
+
+        // ---- P.V: this lane's 8 columns for all G heads, its TPL tokens
+        bool rescale = false;
+        float al[G];
+#pragma unroll
+        for (int h = 0; h < G; ++h) {
+            al[h] = aw[h];
+            rescale |= (al[h] != 1.f);
+        }
+        if (__any_sync(0xffffffffu, rescale)) {
+#pragma unroll
+            for (int h = 0; h < G; ++h)
+#pragma unroll
+                for (int e = 0; e < 8; ++e) o[h][e] *= al[h];
+        }
+        const int half = dg >> 3, c = dg & 7;
+#pragma unroll
+        for (int i = 0; i < C::TPL; ++i) {
+            const int t = tgp + C::TGP * i;
+            if (t < nvalid) {
+                uint4 raw = lds128(vt + half * C::SLAB_BYTES + swz128(t, c));
+                float vf[8];
+                unpack8<BF16>(raw, vf);
+#pragma unroll
+                for (int h = 0; h < G; ++h) {
+                    const float pr = pw[t * G + h];
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) o[h][e] = fmaf(pr, vf[e], o[h][e]);
+                }
+            }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar_empty + 8 * st);
+    }
+
+    // fold the token groups of the P.V layout
+#pragma unroll
+    for (int h = 0; h < G; ++h)
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+            float x = o[h][e];
+            if constexpr (C::TGP >= 2) x += __shfl_xor_sync(0xffffffffu, x, C::CR);
+            if constexpr (C::TGP >= 4) x += __shfl_xor_sync(0xffffffffu, x, 2 * C::CR);
+            o[h][e] = x;
+        }
+
+    // ---------------------------------------------------------------- merge the 4 warps
+    // all consumer warps have drained the ring; reuse it as the merge area
+    asm volatile("bar.sync 1, %0;" ::"n"(C::NCW * 32) : "memory");
+    float* mo = reinterpret_cast<float*>(smem);            // [NCW][G][D]
+    float* mm = mo + C::NCW * G * D;                        // [NCW][G]
+    float* ml = mm + C::NCW * G;                            // [NCW][G]
+    if (!ok) { m_run = -INFINITY; l_run = 0.f; }
+    if (tgp == 0) {
+#pragma unroll
+        for (int h = 0; h < G; ++h) {
+            float4* dst = reinterpret_cast<float4*>(mo + (warp * G + h) * D + dg * 8);
+            dst[0] = make_float4(o[h][0], o[h][1], o[h][2], o[h][3]);
+            dst[1] = make_float4(o[h][4], o[h][5], o[h][6], o[h][7]);
+        }
+    }
+    if (rep) {
+        mm[warp * G + my_h] = m_run;
+        ml[warp * G + my_h] = l_run;
+    }
+    asm volatile("bar.sync 1, %0;" ::"n"(C::NCW * 32) : "memory");
+
+    const int tid = threadIdx.x;  // 0 .. 127
+    const int hq0 = g * G;
+    for (int idx = 2 * tid; idx < G * D; idx += 2 * C::NCW * 32) {
+        const int h = idx / D, d = idx - h * D;
+        float M = -INFINITY;
+#pragma unroll
+        for (int w = 0; w < C::NCW; ++w) M = fmaxf(M, mm[w * G + h]);
+        float Lsum = 0.f, o0 = 0.f, o1 = 0.f;
+        if (M != -INFINITY) {
+#pragma unroll
+            for (int w = 0; w < C::NCW; ++w) {
+                const float wt = exp2f(mm[w * G + h] - M);
+                Lsum = fmaf(ml[w * G + h], wt, Lsum);
+                o0 = fmaf(mo[(w * G + h) * D + d], wt, o0);
+                o1 = fmaf(mo[(w * G + h) * D + d + 1], wt, o1);
+            }
+        }
+        const float inv = (Lsum > 0.f) ? 1.f / Lsum : 0.f;
+        const size_t row = (size_t)s * p.n_q_heads + hq0 + h;
+        if (direct) {
+            uint32_t packed = F::pack_rn(o0 * inv, o1 * inv);
+            *reinterpret_cast<uint32_t*>(static_cast<uint16_t*>(p.out) + row * D + d) = packed;
+        } else {
+            const size_t pr = row * p.max_parts + piece;
+            *reinterpret_cast<float2*>(p.ws_o + pr * D + d) = make_float2(o0 * inv, o1 * inv);
+            if (d == 0) {
+                p.ws_m[pr] = M * 0.69314718055994531f;  // back to natural-log units
+                p.ws_l[pr] = Lsum;
+            }
+        }
+    }
+}
+
+// Split-K merge (mini_engine, "Custom CUDA kernels", v2 reduce): for each (s, h) with more
+// than one piece, M = max_p m_p, w_p = l_p exp(m_p - M), out = sum_p w_p o_p / sum_p w_p.
+// One CTA of 256 threads per (s, h): 8 warps take pieces round-robin, each lane 4 columns.
+template <int D, bool BF16>
+__global__ void __launch_bounds__(256) splitk_reduce_kernel(const DecodeParams p) {
+    using F = F16x2<BF16>;
+    extern __shared__ float4 red_smem4[];  // w[max_parts rounded up to 4] | acc[8][D]
+    float* red_smem = reinterpret_cast<float*>(red_smem4);
+    const int row = blockIdx.x;          // s * Hq + h
+    const int s = row / p.n_q_heads;
+    int L = __ldg(p.context_lens + s);
+    const int cap = min(p.max_blocks_per_seq * 16, p.max_parts * p.part_tokens);
+    L = L < 0 ? 0 : (L > cap ? cap : L);
+    const int n_parts = (L + p.part_tokens - 1) / p.part_tokens;
+    if (n_parts <= 1) return;  // written directly by the piece kernel
+    float* wsh = red_smem;
+    float* acc = red_smem + ((p.max_parts + 3) & ~3);  // 16-byte aligned for the float4 stores
+    const float* m = p.ws_m + (size_t)row * p.max_parts;
+    const float* l = p.ws_l + (size_t)row * p.max_parts;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    __shared__ float red[8];
+    __shared__ float Msh, Wsh;
+
+    float mx = -INFINITY;
+    for (int i = tid; i < n_parts; i += 256) mx = fmaxf(mx, m[i]);
+#pragma unroll
+    for (int o = 16; o; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    if (lane == 0) red[warp] = mx;
+    __syncthreads();
+    if (tid == 0) {
+        float M = red[0];
+        for (int w = 1; w < 8; ++w) M = fmaxf(M, red[w]);
+        Msh = M;
+    }
+    __syncthreads();
+    const float M = Msh;
+    float wsum = 0.f;
+    for (int i = tid; i < n_parts; i += 256) {
+        const float w = (l[i] > 0.f) ? l[i] * __expf(m[i] - M) : 0.f;
+        wsh[i] = w;
+        wsum += w;
+    }
+#pragma unroll
+    for (int o = 16; o; o >>= 1) wsum += __shfl_xor_sync(0xffffffffu, wsum, o);
+    __syncthreads();
+    if (lane == 0) red[warp] = wsum;
+    __syncthreads();
+    if (tid == 0) {
+        float W = 0.f;
+        for (int w = 0; w < 8; ++w) W += red[w];
+        Wsh = W;
+    }
+    __syncthreads();
+
+    constexpr int LPR = D / 4;  // lanes per row (float4 each)
+    float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (lane < LPR) {
+        const float* ob = p.ws_o + (size_t)row * p.max_parts * D + lane * 4;
+        int i = warp;
+        for (; i + 24 < n_parts; i += 32) {
+            float4 x0 = *reinterpret_cast<const float4*>(ob + (size_t)i * D);
+            float4 x1 = *reinterpret_cast<const float4*>(ob + (size_t)(i + 8) * D);
+            float4 x2 = *reinterpret_cast<const float4*>(ob + (size_t)(i + 16) * D);
+            float4 x3 = *reinterpret_cast<const float4*>(ob + (size_t)(i + 24) * D);
+            const float w0 = wsh[i], w1 = wsh[i + 8], w2 = wsh[i + 16], w3 = wsh[i + 24];
+            a.x += w0 * x0.x + w1 * x1.x + w2 * x2.x + w3 * x3.x;
+            a.y += w0 * x0.y + w1 * x1.y + w2 * x2.y + w3 * x3.y;
+            a.z += w0 * x0.z + w1 * x1.z + w2 * x2.z + w3 * x3.z;
+            a.w += w0 * x0.w + w1 * x1.w + w2 * x2.w + w3 * x3.w;
+        }
+        for (; i < n_parts; i += 8) {
+            const float w = wsh[i];
+            if (w > 0.f) {
+                float4 x = *reinterpret_cast<const float4*>(ob + (size_t)i * D);
+                a.x += w * x.x; a.y += w * x.y; a.z += w * x.z; a.w += w * x.w;
+            }
+        }
+        *reinterpret_cast<float4*>(acc + warp * D + lane * 4) = a;
+    }
+    __syncthreads();
+    if (tid < D / 2) {
+        const int d = 2 * tid;
+        float s0 = 0.f, s1 = 0.f;
+#pragma unroll
+        for (int w = 0; w < 8; ++w) {
+            s0 += acc[w * D + d];
+            s1 += acc[w * D + d + 1];
+        }
+        const float inv = (Wsh > 0.f) ? 1.f / Wsh : 0.f;
+        *reinterpret_cast<uint32_t*>(static_cast<uint16_t*>(p.out) + (size_t)row * D + d) = F::pack_rn(s0 * inv, s1 * inv);
+    }
+}
+
+}  // namespace pa

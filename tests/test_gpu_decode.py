@@ -1,0 +1,216 @@
+"""GPU parity of pa_decode (dispatcher), pa_decode_v1 and pa_decode_splitk against the
+fp64 oracle: the four decode workloads at full size, edge sweeps over lengths, group
+sizes, head dims and dtypes, NaN canaries in every slot no sequence owns, exact special
+cases, relabelling invariance, split-K intermediates and device error flags."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import paged_kv_cache_232_gb300 as pa
+import workloads as wl
+from pa_testutil import abs_bits, bits_of, check_attention, to_dev, to_dev_i, ulp_distance
+
+pytestmark = pytest.mark.gpu
+
+
+class Dev:
+    """A workload's pool and decode batch on the GPU."""
+
+    def __init__(self, w, k_cache=None, v_cache=None):
+        p, b = w.pool, w.decode
+        self.w, self.dt = w, p.dtype
+        self.kc = to_dev(p.k_cache if k_cache is None else k_cache, p.dtype)
+        self.vc = to_dev(p.v_cache if v_cache is None else v_cache, p.dtype)
+        self.q = to_dev(b.q, p.dtype)
+        self.bt = to_dev_i(b.block_tables, torch.int32)
+        self.cl = to_dev_i(b.context_lens, torch.int32)
+        self.maxL = int(b.context_lens.max())
+        self.scale = b.scale
+
+    def run(self, mode="auto", part=0, cl=None):
+        out = torch.empty_like(self.q)
+        cl = self.cl if cl is None else cl
+        S, hq, d = self.q.shape
+        if mode == "v1":
+            pa.pa_decode_v1(out, self.q, self.kc, self.vc, self.bt, cl, self.scale)
+        else:
+            ws_bytes = pa.pa_decode_workspace_size(S, hq, d, self.maxL, part)
+            ws = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=out.device)
+            self.ws = ws
+            if mode == "splitk":
+                pa.pa_decode_splitk(out, self.q, self.kc, self.vc, self.bt, cl, self.maxL, self.scale, ws, part)
+            else:
+                pa.pa_decode(out, self.q, self.kc, self.vc, self.bt, cl, self.maxL, self.scale, ws)
+        torch.cuda.synchronize()
+        return bits_of(out)
+
+
+def oracle_decode(w, k_cache=None, v_cache=None):
+    """(exact, cond): the fp64 outputs and each output's condition scale sum_t w_t |V_t|."""
+    p, b = w.pool, w.decode
+    k = p.k_cache if k_cache is None else k_cache
+    v = p.v_cache if v_cache is None else v_cache
+    exact = oracle.decode(b.q, k, v, b.block_tables, b.context_lens, b.scale, p.dtype)
+    cond = oracle.decode(b.q, k, abs_bits(v), b.block_tables, b.context_lens, b.scale, p.dtype)
+    return exact, cond
+
+
+def check(got, ref, dt, what):
+    return check_attention(got, ref[0], dt, what, cond=ref[1])
+
+
+# ------------------------------------------------------------------ the decode workloads
+
+
+@pytest.mark.parametrize("k", [1, 2, 3])
+@pytest.mark.parametrize("mode", ["auto", "v1", "splitk"])
+def test_decode_workloads_full_size(k, mode):
+    w = wl.make_workload(k)
+    pa.pa_device_errors(clear=True)
+    got = Dev(w).run(mode)
+    err = check(got, oracle_decode(w), w.pool.dtype, f"config{k}/{mode}")
+    assert err <= 2e-3
+    assert pa.pa_device_errors(clear=True) == 0
+
+
+def test_full_decode_step_batch_256_write_then_decode():
+    """Config 4: the write lands, then every sequence decodes over its context including
+    the row just written (padded rows keep the slot's previous content)."""
+    w = wl.make_workload(4)
+    p, b, wr = w.pool, w.decode, w.write
+    d = Dev(w)
+    pa.pa_reshape_and_cache(to_dev(wr.key, p.dtype), to_dev(wr.value, p.dtype), d.kc, d.vc,
+                            to_dev_i(wr.slot_mapping, torch.int64))
+    got = d.run("auto")
+    k2, v2, _ = oracle.kv_write(p.k_cache, p.v_cache, wr.key, wr.value, wr.slot_mapping, 16)
+    assert np.array_equal(bits_of(d.kc), k2) and np.array_equal(bits_of(d.vc), v2)
+    ref = oracle_decode(w, k2, v2)
+    check(got, ref, p.dtype, "config4")
+    for mode in ("v1", "splitk"):
+        check(d.run(mode), ref, p.dtype, f"config4/{mode}")
+
+
+def test_mixed_batch_decode_rows_with_shared_prefix():
+    w = wl.make_workload(5)
+    got = Dev(w).run("auto")
+    check(got, oracle_decode(w), w.pool.dtype, "config5 decode rows")
+
+
+# ------------------------------------------------------------------ edge sweeps
+
+
+EDGE_LENS = [1, 15, 16, 17, 255, 256, 257, 513, 4097]
+
+
+@pytest.mark.parametrize("dt,hq,hkv,d", [(wl.BF16, 16, 8, 128), (wl.F16, 2, 2, 64), (wl.BF16, 32, 8, 128),
+                                         (wl.F16, 8, 1, 128), (wl.BF16, 8, 2, 64), (wl.F16, 16, 4, 128)])
+@pytest.mark.parametrize("mode,part", [("v1", 0), ("splitk", 0), ("splitk", 64), ("splitk", 512)])
+def test_decode_edge_lengths(dt, hq, hkv, d, mode, part):
+    w = wl.build_workload("edge", 77 + hq + d, dtype=dt, n_q_heads=hq, n_kv_heads=hkv, head_dim=d,
+                          decode_lens=EDGE_LENS, max_blocks_per_seq=300, extra_blocks=5)
+    got = Dev(w).run(mode, part)
+    check(got, oracle_decode(w), dt, f"edge {mode}/{part}")
+
+
+def test_single_token_context_returns_v_bitwise():
+    w = wl.build_workload("one", 5, dtype=wl.BF16, n_q_heads=16, n_kv_heads=8, head_dim=128, decode_lens=[1] * 9)
+    p, b = w.pool, w.decode
+    for mode in ("v1", "splitk"):
+        got = Dev(w).run(mode).reshape(9, 16, 128)
+        for s in range(9):
+            v0 = p.v_cache[b.block_tables[s, 0], 0]          # [Hkv, D]
+            assert np.array_equal(got[s], np.repeat(v0, 2, axis=0))
+
+
+def test_uniform_v_within_one_ulp():
+    w = wl.build_workload("u", 6, dtype=wl.F16, n_q_heads=4, n_kv_heads=2, head_dim=64, decode_lens=[700, 33, 2])
+    p = w.pool
+    vrow = wl.normal_bits(8, 2 * 64, wl.F16).reshape(2, 64)
+    v = p.v_cache.copy()
+    v[p.valid] = vrow
+    for mode in ("v1", "splitk"):
+        got = Dev(w, v_cache=v).run(mode).reshape(3, 4, 64)
+        want = np.broadcast_to(np.repeat(vrow, 2, axis=0), (3, 4, 64))
+        assert ulp_distance(got, want).max() <= 1
+
+
+def test_block_relabelling_is_bitwise_invariant():
+    w = wl.make_workload(2)
+    p, b = w.pool, w.decode
+    pi = wl.permutation(4242, p.num_blocks)
+    k2, v2 = np.empty_like(p.k_cache), np.empty_like(p.v_cache)
+    k2[pi], v2[pi] = p.k_cache, p.v_cache
+    d1 = Dev(w)
+    d2 = Dev(w, k2, v2)
+    d2.bt = to_dev_i(pi[b.block_tables], torch.int32)
+    for mode in ("v1", "splitk"):
+        assert np.array_equal(d1.run(mode), d2.run(mode))
+
+
+def test_splitk_intermediates_match_oracle_pieces():
+    """fp32 per-piece max, exp-sum and normalised output, read back from the workspace
+    (layout of pa_decode_workspace_size), against the oracle's fp64 pieces at 1e-5."""
+    w = wl.build_workload("ws", 9, dtype=wl.BF16, n_q_heads=8, n_kv_heads=2, head_dim=128,
+                          decode_lens=[1000, 256, 1300, 3], max_blocks_per_seq=96)
+    p, b = w.pool, w.decode
+    d = Dev(w)
+    d.run("splitk", 256)
+    S, hq, D, P = 4, 8, 128, -(-1300 // 256)
+    rows = S * hq * P
+    al = lambda x: (x + 255) // 256 * 256
+    raw = d.ws.cpu().numpy()
+    gm = raw[: rows * 4].view(np.float32).reshape(S, hq, P)
+    gl = raw[al(rows * 4): al(rows * 4) + rows * 4].view(np.float32).reshape(S, hq, P)
+    go = raw[2 * al(rows * 4): 2 * al(rows * 4) + rows * D * 4].view(np.float32).reshape(S, hq, P, D)
+    m, l, o = oracle.decode_partitions(b.q, p.k_cache, p.v_cache, b.block_tables, b.context_lens, b.scale,
+                                       p.dtype, 256, P)
+    # the same pieces over |V| give each output's condition scale sum_t w_t |V_t|
+    absv = p.v_cache & np.uint16(0x7FFF)
+    _, _, oabs = oracle.decode_partitions(b.q, p.k_cache, absv, b.block_tables, b.context_lens, b.scale,
+                                          p.dtype, 256, P)
+    for s in range(S):
+        n = -(-int(b.context_lens[s]) // 256)
+        if n <= 1:
+            continue    # single-piece sequences are written directly, not through the workspace
+        sl = np.s_[s, :, :n]
+        np.testing.assert_allclose(gm[sl], m[sl], rtol=1e-5, atol=1e-5)
+        np.testing.assert_allclose(gl[sl], l[sl], rtol=1e-5, atol=0)
+        assert np.all(np.abs(go[sl] - o[sl]) <= 1e-5 * oabs[sl] + 1e-7)
+
+
+# ------------------------------------------------------------------ canaries and error flags
+
+
+def test_out_of_pool_block_id_is_flagged_not_faulted():
+    w = wl.build_workload("bad", 10, dtype=wl.BF16, n_q_heads=4, n_kv_heads=2, head_dim=128, decode_lens=[64, 40])
+    d = Dev(w)
+    bt = w.decode.block_tables.copy()
+    bt[0, 1] = w.pool.num_blocks + 3        # outside the pool: the kernel reads zeros, records the error
+    d.bt = to_dev_i(bt, torch.int32)
+    pa.pa_device_errors(clear=True)
+    for mode in ("v1", "splitk"):
+        got = d.run(mode)
+        assert pa.pa_device_errors(clear=True) & pa.PA_DEVERR_BLOCK
+        # the other sequence is untouched by the bad entry
+        ex, cd = oracle_decode(w)
+        check_attention(got.reshape(2, 4, 128)[1:], ex[1:], wl.BF16, "good row", cond=cd[1:])
+
+
+def test_context_longer_than_table_is_clamped_and_flagged():
+    w = wl.build_workload("len", 11, dtype=wl.BF16, n_q_heads=4, n_kv_heads=2, head_dim=128, decode_lens=[32, 20])
+    d = Dev(w)
+    cl = to_dev_i(np.array([32 + 1000, 20], np.int32), torch.int32)
+    pa.pa_device_errors(clear=True)
+    got = d.run("v1", cl=cl)
+    assert pa.pa_device_errors(clear=True) & pa.PA_DEVERR_LENGTH
+    check(got.reshape(2, 4, 128), oracle_decode(w), wl.BF16, "clamped")
+
+
+def test_zero_length_context_gives_zeros():
+    w = wl.build_workload("z", 12, dtype=wl.BF16, n_q_heads=4, n_kv_heads=2, head_dim=128, decode_lens=[5, 300])
+    d = Dev(w)
+    cl = to_dev_i(np.array([0, 300], np.int32), torch.int32)
+    for mode in ("v1", "splitk"):
+        got = d.run(mode, cl=cl).reshape(2, 4, 128)
+        assert np.all(got[0] == 0)

@@ -1,0 +1,69 @@
+"""GPU parity of pa_reshape_and_cache against the oracle: the whole cache must be
+bit-identical after the write (written slots hold the rows, -1 rows and every other
+slot unchanged)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import paged_kv_cache_232_gb300 as pa
+import workloads as wl
+from pa_testutil import bits_of, to_dev, to_dev_i
+
+pytestmark = pytest.mark.gpu
+
+
+def run_write(w, slot_mapping=None):
+    p, wr = w.pool, w.write
+    dt = p.dtype
+    sm = wr.slot_mapping if slot_mapping is None else slot_mapping
+    kc, vc = to_dev(p.k_cache, dt), to_dev(p.v_cache, dt)
+    pa.pa_reshape_and_cache(to_dev(wr.key, dt), to_dev(wr.value, dt), kc, vc, to_dev_i(sm, torch.int64))
+    torch.cuda.synchronize()
+    return bits_of(kc), bits_of(vc)
+
+
+def assert_write_matches_oracle(w, slot_mapping=None, expect_status=oracle.OK):
+    p, wr = w.pool, w.write
+    sm = wr.slot_mapping if slot_mapping is None else slot_mapping
+    pa.pa_device_errors(clear=True)
+    gk, gv = run_write(w, sm)
+    ok, ov, st = oracle.kv_write(p.k_cache, p.v_cache, wr.key, wr.value, sm, p.block_size, check=False)
+    assert st == expect_status
+    assert np.array_equal(gk, ok), "k_cache differs from the oracle"
+    assert np.array_equal(gv, ov), "v_cache differs from the oracle"
+    return pa.pa_device_errors(clear=True)
+
+
+def test_write_full_step_batch_256():
+    w = wl.make_workload(4)
+    assert assert_write_matches_oracle(w) == 0
+
+
+def test_write_bandwidth_scale_64k_rows():
+    w = wl.write_rows_case(232_104, 65536)
+    assert assert_write_matches_oracle(w) == 0
+
+
+@pytest.mark.parametrize("n,hkv,d,dt", [(1, 8, 128, wl.BF16), (3, 2, 64, wl.F16), (37, 1, 64, wl.BF16),
+                                        (1023, 4, 128, wl.F16), (4099, 8, 64, wl.BF16)])
+def test_write_shapes_and_ragged_counts(n, hkv, d, dt):
+    w = wl.write_rows_case(1000 + n, n, n_kv_heads=hkv, head_dim=d, dtype=dt, pad_frac=0.25, nan_canaries=True)
+    assert assert_write_matches_oracle(w) == 0
+
+
+def test_write_all_padded_changes_nothing():
+    w = wl.write_rows_case(5, 64)
+    sm = np.full(64, -1, dtype=np.int64)
+    assert assert_write_matches_oracle(w, sm) == 0
+    gk, gv = run_write(w, sm)
+    assert np.array_equal(gk, w.pool.k_cache) and np.array_equal(gv, w.pool.v_cache)
+
+
+def test_write_out_of_pool_slot_is_flagged_and_dropped():
+    w = wl.write_rows_case(6, 40, pad_frac=0.0)
+    sm = w.write.slot_mapping.copy()
+    sm[3] = w.pool.num_blocks * 16 + 7      # past the pool
+    sm[9] = -5                               # negative, not the padding marker
+    errs = assert_write_matches_oracle(w, sm, expect_status=oracle.EBOUNDS)
+    assert errs & pa.PA_DEVERR_SLOT
