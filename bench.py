@@ -156,10 +156,38 @@ WORKLOADS = {
     "single": 1,
     "decode64": 2,
     "long4": 3,
+    "mixed": 5,
 }
 
 
 # ----------------------------------------------------------------------------- our arm
+
+
+def prefill_flops(pre, n_q_heads, head_dim):
+    """4 * D flops (QK^T and PV) per visible (query row, key) pair and head: causal pairs only."""
+    ql = np.diff(pre.query_start_loc).astype(np.int64)
+    ctx = pre.seq_lens.astype(np.int64) - ql
+    pairs = int(np.sum(ql * ctx + ql * (ql + 1) // 2))
+    return 4 * head_dim * n_q_heads * pairs
+
+
+def prefill_bytes(pre, pool):
+    kv = int(pre.seq_lens.astype(np.int64).sum()) * 2 * pool.n_kv_heads * pool.head_dim * 2
+    return kv + 2 * nbytes(pre.q) + int(np.ceil(pre.seq_lens / pool.block_size).sum()) * 4
+
+
+def unique_decode_bytes(b, pool):
+    """Decode bytes counting each physical block's tokens once (a shared prefix is read from
+    HBM once, the rest of its reads hit L2); equals decode_bytes when no block is shared."""
+    L = b.context_lens.astype(np.int64)
+    bs = pool.block_size
+    tokens = {}
+    for s in range(b.num_seqs):
+        n = -(-int(L[s]) // bs)
+        for j, blk in enumerate(b.block_tables[s, :n].tolist()):
+            tokens[blk] = max(tokens.get(blk, 0), min(bs, int(L[s]) - j * bs))
+    kv = sum(tokens.values()) * 2 * pool.n_kv_heads * pool.head_dim * 2
+    return kv + 2 * nbytes(b.q) + int(np.ceil(L / bs).sum()) * 4 + nbytes(b.context_lens)
 
 
 def run_ours(args, rank, world, local_rank):
@@ -171,46 +199,57 @@ def run_ours(args, rank, world, local_rank):
     torch.cuda.set_device(dev)
     k = WORKLOADS[args.workload]
     w = wl.make_workload(k)     # every rank gets its own copy of the same batch (weak scaling)
-    p, b, wr = w.pool, w.decode, w.write
+    p, b, wr, pre = w.pool, w.decode, w.write, w.prefill
     dt = torch.bfloat16 if p.dtype == wl.BF16 else torch.float16
 
     def dev_bits(a):
         return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(dt).to(dev)
 
+    def dev_int(a):
+        return torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+
     kc, vc = dev_bits(p.k_cache), dev_bits(p.v_cache)
-    q = dev_bits(b.q)
-    bt = torch.from_numpy(b.block_tables).to(dev)
-    cl = torch.from_numpy(b.context_lens).to(dev)
-    out = torch.empty_like(q)
     S, hq, D = b.q.shape
+    n_pre = pre.q.shape[0] if pre is not None else 0
+    q_host = np.concatenate([b.q, pre.q]) if pre is not None else b.q
+    q = dev_bits(q_host)                       # decode rows first, then prefill rows
+    out = torch.empty_like(q)
+    bt, cl = dev_int(b.block_tables), dev_int(b.context_lens)
     maxL = int(b.context_lens.max())
-    ws_bytes = pa.pa_decode_workspace_size(S, hq, D, maxL, 0)
-    ws = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=dev)
+    ws = torch.empty(max(pa.pa_decode_workspace_size(S, hq, D, maxL, 0), 16), dtype=torch.uint8, device=dev)
     which, part = pa.pa_decode_plan(S, p.n_kv_heads, maxL)
+    stages = []   # name, launch, algorithmic amount, kind
     if wr is not None:
-        key, val = dev_bits(wr.key), dev_bits(wr.value)
-        sm = torch.from_numpy(wr.slot_mapping).to(dev)
+        key, val, sm = dev_bits(wr.key), dev_bits(wr.value), dev_int(wr.slot_mapping)
+        stages.append(("write", lambda: pa.pa_reshape_and_cache(key, val, kc, vc, sm), write_bytes(wr, p), "hbm"))
+    dec_logical = decode_bytes(b, p)
+    dec_unique = unique_decode_bytes(b, p)
+    stages.append(("decode", lambda: pa.pa_decode(out[:S], q[:S], kc, vc, bt, cl, maxL, b.scale, ws), dec_unique,
+                   "hbm"))
+    if pre is not None:
+        pbt, qsl, sl = dev_int(pre.block_tables), dev_int(pre.query_start_loc), dev_int(pre.seq_lens)
+        stages.append(("prefill", lambda: pa.pa_prefill_chunk(out[S:], q[S:], kc, vc, pbt, qsl, sl, pre.max_q_len,
+                                                              pre.scale),
+                       prefill_flops(pre, hq, D), "tensor"))
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
+    ns = len(stages)
 
     def step(ev=None):
-        if wr is not None:
+        for i, st in enumerate(stages):
             if ev:
-                ev[0].record(stream)
-            pa.pa_reshape_and_cache(key, val, kc, vc, sm)
+                ev[i].record(stream)
+            st[1]()
         if ev:
-            ev[1].record(stream)
-        pa.pa_decode(out, q, kc, vc, bt, cl, maxL, b.scale, ws)
-        if ev:
-            ev[2].record(stream)
+            ev[ns].record(stream)
 
-    launches_per_step = (1 if wr is not None else 0) + (1 if which == 1 else 2)
+    launches_per_step = (1 if wr is not None else 0) + (1 if which == 1 else 2) + (1 if pre is not None else 0)
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize()
     assert pa.pa_device_errors(clear=True) == 0
 
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(ns + 1)] for _ in range(args.steps)]
     barrier(world)
     torch.cuda.synchronize()
     t_wall0 = time.perf_counter()
@@ -221,39 +260,55 @@ def run_ours(args, rank, world, local_rank):
         torch.cuda.synchronize()
     barrier(world)
     t_wall = time.perf_counter() - t_wall0
-    w_ms = [e[0].elapsed_time(e[1]) if wr is not None else 0.0 for e in evs]
-    d_ms = [e[1].elapsed_time(e[2]) for e in evs]
-    step_ms = float(np.sum(w_ms) + np.sum(d_ms)) / args.steps
-    step_ms = max_over_ranks(step_ms, world)
+    st_ms = np.array([[e[i].elapsed_time(e[i + 1]) for i in range(ns)] for e in evs])   # [steps, stages]
+    step_ms = max_over_ranks(float(st_ms.sum(axis=1).mean()), world)
+    mean_ms = st_ms.mean(axis=0)
 
-    dbytes = decode_bytes(b, p)
-    wbytes = write_bytes(wr, p) if wr is not None else 0
-    step_bytes = dbytes + wbytes
+    step_bytes = (write_bytes(wr, p) if wr is not None else 0) + dec_logical + (
+        prefill_bytes(pre, p) if pre is not None else 0)
     value = world * step_bytes / (step_ms * 1e-3) / 1e9
     peaks = measured_peaks()
-    dec_ms = float(np.mean(d_ms))
-    achieved = dbytes / (dec_ms * 1e-3) / 1e9
+    breakdown = {}
+    for (name, _, amount, kind), ms in zip(stages, mean_ms):
+        if kind == "hbm":
+            breakdown[name] = {"us": round(float(ms) * 1e3, 2), "gbs": round(amount / (ms * 1e-3) / 1e9, 1),
+                               "frac_hbm": round(amount / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"], 4)}
+        else:
+            breakdown[name] = {"us": round(float(ms) * 1e3, 2), "tflops": round(amount / (ms * 1e-3) / 1e12, 1),
+                               "frac_bf16": round(amount / (ms * 1e-3) / 1e12 / peaks["bf16_tflops"], 4),
+                               "flop": amount}
+    if pre is not None:
+        breakdown["decode"]["logical_gbs"] = round(dec_logical / (mean_ms[0] * 1e-3) / 1e9, 1)
+    dom = int(np.argmax(mean_ms))
+    dname, _, damount, dkind = stages[dom]
+    dms = float(mean_ms[dom])
+    if dkind == "hbm":
+        ach = damount / (dms * 1e-3) / 1e9
+        roof = {"bound": "hbm", "kernel": f"{dname}", "achieved": round(ach, 1), "peak": peaks["hbm_gbs"],
+                "peak_source": peaks["source"], "unit": "GB/s", "frac": round(ach / peaks["hbm_gbs"], 4),
+                "traffic": args.traffic, "algorithmic_bytes": damount}
+    else:
+        ach = damount / (dms * 1e-3) / 1e12
+        roof = {"bound": "tensor", "kernel": f"{dname}", "achieved": round(ach, 1), "peak": peaks["bf16_tflops"],
+                "peak_source": peaks["source"], "unit": "TFLOP/s", "frac": round(ach / peaks["bf16_tflops"], 4),
+                "traffic": args.traffic, "algorithmic_flops": damount}
 
     # end to end through the C ABI with host buffers: inputs up, result down, every step
     pin = lambda t: t.cpu().pin_memory()
-    h_q, h_bt, h_cl = pin(q), pin(bt), pin(cl)
-    h_out = torch.empty_like(out, device="cpu").pin_memory()
-    h2d = nbytes(b.q) + nbytes(b.block_tables) + nbytes(b.context_lens)
+    h_in = [(q, pin(q)), (bt, pin(bt)), (cl, pin(cl))]
     if wr is not None:
-        h_key, h_val, h_sm = pin(key), pin(val), pin(sm)
-        h2d += nbytes(wr.key) + nbytes(wr.value) + nbytes(wr.slot_mapping)
-    d2h = nbytes(b.q)
+        h_in += [(key, pin(key)), (val, pin(val)), (sm, pin(sm))]
+    if pre is not None:
+        h_in += [(pbt, pin(pbt)), (qsl, pin(qsl)), (sl, pin(sl))]
+    h_out = torch.empty_like(out, device="cpu").pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t, _ in h_in)
+    d2h = out.numel() * out.element_size()
 
     def e2e_step():
-        q.copy_(h_q, non_blocking=True)
-        bt.copy_(h_bt, non_blocking=True)
-        cl.copy_(h_cl, non_blocking=True)
-        if wr is not None:
-            key.copy_(h_key, non_blocking=True)
-            val.copy_(h_val, non_blocking=True)
-            sm.copy_(h_sm, non_blocking=True)
-            pa.pa_reshape_and_cache(key, val, kc, vc, sm)
-        pa.pa_decode(out, q, kc, vc, bt, cl, maxL, b.scale, ws)
+        for d_, h_ in h_in:
+            d_.copy_(h_, non_blocking=True)
+        for st in stages:
+            st[1]()
         h_out.copy_(out, non_blocking=True)
 
     for _ in range(3):
@@ -268,6 +323,19 @@ def run_ours(args, rank, world, local_rank):
     torch.cuda.synchronize()
     e2e_ms = max_over_ranks(float(np.mean([a.elapsed_time(c) for a, c in e2e_ev])), world)
 
+    cfg = {
+        "workload": wl.WORKLOAD_NAMES[k],
+        "num_seqs": int(S), "n_q_heads": int(hq), "n_kv_heads": p.n_kv_heads, "head_dim": p.head_dim,
+        "block_size": p.block_size, "total_context_tokens": int(b.context_lens.sum()),
+        "decode_path": "one-pass" if which == 1 else f"split-K/{part}",
+        "l2": "512 MiB memset between timed steps (outside the events)",
+        "parallelism": f"replicas x{world} (independent batches, no collective)",
+    }
+    if wr is not None:
+        cfg.update(write_rows=int(wr.slot_mapping.size), padded_rows=int((wr.slot_mapping < 0).sum()))
+    if pre is not None:
+        cfg.update(prefill_chunks=pre.num_chunks, prefill_rows=int(n_pre),
+                   prefill_kv_lens=[int(x) for x in pre.seq_lens])
     res = {
         "metric": "paged decode attn us/step & achieved HBM GB/s (% of GB300 peak); KV-write GB/s",
         "value": round(value, 2),
@@ -281,35 +349,11 @@ def run_ours(args, rank, world, local_rank):
         "scaling": "weak",
         "vs_baseline": None,
         "dtype": "bf16" if p.dtype == wl.BF16 else "f16",
-        "data": "synthetic (seeded SplitMix64/Box-Muller N(0,1), bf16 RNE)",
-        "config": {
-            "workload": wl.WORKLOAD_NAMES[k],
-            "num_seqs": int(S), "n_q_heads": int(hq), "n_kv_heads": p.n_kv_heads, "head_dim": p.head_dim,
-            "block_size": p.block_size, "total_context_tokens": int(b.context_lens.sum()),
-            "write_rows": int(wr.slot_mapping.size) if wr is not None else 0,
-            "padded_rows": int((wr.slot_mapping < 0).sum()) if wr is not None else 0,
-            "decode_path": "one-pass" if which == 1 else f"split-K/{part}",
-            "l2": "512 MiB memset between timed steps (outside the events); working set > L2",
-            "parallelism": f"replicas x{world} (independent batches, no collective)",
-        },
-        "breakdown": {
-            "write_us": round(float(np.mean(w_ms)) * 1e3, 2),
-            "write_gbs": round(wbytes / (np.mean(w_ms) * 1e-3) / 1e9, 1) if wr is not None else None,
-            "decode_us": round(dec_ms * 1e3, 2),
-            "decode_gbs": round(achieved, 1),
-            "step_bytes": step_bytes,
-        },
-        "roofline": {
-            "bound": "hbm",
-            "kernel": "decode_kernel (pa_decode)",
-            "achieved": round(achieved, 1),
-            "peak": peaks["hbm_gbs"],
-            "peak_source": peaks["source"],
-            "unit": "GB/s",
-            "frac": round(achieved / peaks["hbm_gbs"], 4),
-            "traffic": args.traffic,
-            "algorithmic_bytes": dbytes,
-        },
+        "data": "synthetic (seeded SplitMix64/Box-Muller N(0,1), RNE to the 16-bit format)",
+        "config": cfg,
+        "breakdown": breakdown,
+        "step_bytes": step_bytes,
+        "roofline": roof,
         "e2e": {
             "value": round(world * step_bytes / (e2e_ms * 1e-3) / 1e9, 2),
             "unit": "GB/s",

@@ -59,8 +59,10 @@ def half_ulp(x: np.ndarray, dtype_code: int) -> np.ndarray:
     return 0.5 * 2.0 ** (e - mant)
 
 
-def check_attention(gpu_bits: np.ndarray, exact: np.ndarray, dtype_code: int, what: str = "", cond=None):
-    """Assert rules 1 and 2 above (rule 2 only when cond is given); returns max |err|."""
+def check_attention(gpu_bits: np.ndarray, exact: np.ndarray, dtype_code: int, what: str = "", cond=None,
+                    rel: float = 1e-4):
+    """Assert rules 1 and 2 above (rule 2 only when cond is given; `rel` replaces the 1e-4
+    factor where a path adds a known rounding of its own); returns max |err|."""
     assert np.isfinite(exact).all(), f"{what}: oracle produced non-finite values"
     got = oracle.to_double(gpu_bits, dtype_code).reshape(exact.shape)
     assert np.isfinite(got).all(), f"{what}: GPU output has NaN/inf (a canary was read?)"
@@ -68,7 +70,7 @@ def check_attention(gpu_bits: np.ndarray, exact: np.ndarray, dtype_code: int, wh
     hu = half_ulp(exact, dtype_code)
     r1 = (hu < ATOL) & (err > ATOL)
     if cond is not None:
-        allow2 = hu + 1e-4 * cond + 1e-6
+        allow2 = hu + rel * cond + 1e-6
         r2 = err > allow2
     else:
         allow2 = np.maximum(ATOL, hu)

@@ -1,0 +1,134 @@
+"""GPU parity of pa_prefill_chunk (tcgen05 tensor cores) against the fp64 oracle, and of
+the mixed batch (decode rows through pa_decode, prefill rows through pa_prefill_chunk,
+one output tensor).
+
+The kernel carries the softmax weights into the PV product as two 16-bit terms
+(P_hi + P_lo), whose sum is within 2^-17 (bf16) / 2^-23 (fp16) of each fp32 weight, so the
+fp32-level rule gets an extra allowance of 2^-16 * cond (bf16) or 2^-22 * cond (fp16) on
+top of its 1e-4 * cond; the 2e-3 absolute bound applies unchanged."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import paged_kv_cache_232_gb300 as pa
+import workloads as wl
+from pa_testutil import abs_bits, bits_of, check_attention, to_dev, to_dev_i
+
+pytestmark = pytest.mark.gpu
+
+P_ROUND = {wl.BF16: 2.0 ** -16, wl.F16: 2.0 ** -22}
+
+
+def run_prefill(w, out=None, q=None, kc=None, vc=None):
+    p, pre = w.pool, w.prefill
+    kc = to_dev(p.k_cache, p.dtype) if kc is None else kc
+    vc = to_dev(p.v_cache, p.dtype) if vc is None else vc
+    q = to_dev(pre.q, p.dtype) if q is None else q
+    out = torch.empty_like(q) if out is None else out
+    pa.pa_prefill_chunk(out, q, kc, vc, to_dev_i(pre.block_tables, torch.int32),
+                        to_dev_i(pre.query_start_loc, torch.int32), to_dev_i(pre.seq_lens, torch.int32),
+                        pre.max_q_len, pre.scale)
+    torch.cuda.synchronize()
+    return out
+
+
+def oracle_rows(w, rows=None):
+    """fp64 oracle for the given global query rows (all rows if None), with cond scales.
+    Sampled rows are run as one-row chunks whose kv length is ctx + j + 1, which is what
+    the bottom-right mask gives row j."""
+    p, pre = w.pool, w.prefill
+    if rows is None:
+        ex = oracle.prefill_chunk(pre.q, p.k_cache, p.v_cache, pre.block_tables, pre.query_start_loc, pre.seq_lens,
+                                  pre.scale, p.dtype)
+        cd = oracle.prefill_chunk(pre.q, p.k_cache, abs_bits(p.v_cache), pre.block_tables, pre.query_start_loc,
+                                  pre.seq_lens, pre.scale, p.dtype)
+        return ex, cd
+    rows = np.asarray(rows)
+    qsl = pre.query_start_loc
+    chunk = np.searchsorted(qsl, rows, side="right") - 1
+    j = rows - qsl[chunk]
+    ctx = pre.seq_lens[chunk] - np.diff(qsl)[chunk]
+    q = np.ascontiguousarray(pre.q[rows])
+    bt = np.ascontiguousarray(pre.block_tables[chunk])
+    one = np.arange(len(rows) + 1, dtype=np.int32)
+    kv = (ctx + j + 1).astype(np.int32)
+    ex = oracle.prefill_chunk(q, p.k_cache, p.v_cache, bt, one, kv, pre.scale, p.dtype)
+    cd = oracle.prefill_chunk(q, p.k_cache, abs_bits(p.v_cache), bt, one, kv, pre.scale, p.dtype)
+    return ex, cd
+
+
+def check(got_bits, ref, dt, what):
+    ex, cd = ref
+    return check_attention(got_bits, ex, dt, what, cond=cd, rel=1e-4 + P_ROUND[dt])
+
+
+SHAPES = [(wl.BF16, 16, 8), (wl.F16, 16, 8), (wl.BF16, 8, 8), (wl.BF16, 32, 8), (wl.F16, 16, 2)]
+
+
+@pytest.mark.parametrize("dt,hq,hkv", SHAPES)
+def test_prefill_ragged_chunks_full_parity(dt, hq, hkv):
+    w = wl.build_workload("pf", 300 + hq + hkv, dtype=dt, n_q_heads=hq, n_kv_heads=hkv, head_dim=128,
+                          prefill_q_lens=[1, 7, 64, 65, 128, 200, 17],
+                          prefill_ctx_lens=[0, 20, 5, 127, 300, 1000, 16], extra_blocks=3)
+    got = bits_of(run_prefill(w))
+    check(got, oracle_rows(w), dt, f"prefill {dt} {hq}/{hkv}")
+    assert pa.pa_device_errors(clear=True) == 0
+
+
+def test_prefill_single_row_no_context_returns_v0():
+    w = wl.build_workload("pf1", 7, dtype=wl.BF16, n_q_heads=16, n_kv_heads=8, head_dim=128,
+                          prefill_q_lens=[1, 1], prefill_ctx_lens=[0, 0])
+    got = bits_of(run_prefill(w)).reshape(2, 16, 128)
+    for c in range(2):
+        v0 = w.pool.v_cache[w.prefill.block_tables[c, 0], 0]
+        assert np.array_equal(got[c], np.repeat(v0, 2, axis=0))
+
+
+def test_prefill_mixed_batch_workload_sampled_rows():
+    """Config 5's eight 512-token chunks over 0..4096 cached tokens, full size; every
+    chunk's first 16 and last 16 rows plus 24 seeded random rows are checked."""
+    w = wl.make_workload(5)
+    got = bits_of(run_prefill(w)).reshape(w.prefill.q.shape)
+    qsl = w.prefill.query_start_loc
+    pick = wl.uniform_ints(wl.derive_seed(5, 99), 8 * 24, 0, 511).reshape(8, 24)
+    rows = []
+    for c in range(8):
+        rows += list(range(qsl[c], qsl[c] + 16)) + list(range(qsl[c + 1] - 16, qsl[c + 1])) + list(qsl[c] + pick[c])
+    rows = np.unique(np.asarray(rows))
+    check(got[rows], oracle_rows(w, rows), wl.BF16, "config5 prefill rows")
+
+
+def test_mixed_batch_one_output_tensor():
+    """Decode rows and prefill rows of one batch write disjoint rows of one output."""
+    w = wl.make_workload(5)
+    p, b, pre = w.pool, w.decode, w.prefill
+    kc, vc = to_dev(p.k_cache, p.dtype), to_dev(p.v_cache, p.dtype)
+    q_all = to_dev(np.concatenate([b.q, pre.q]), p.dtype)
+    out = torch.full_like(q_all, float("nan"))
+    S = b.num_seqs
+    maxL = int(b.context_lens.max())
+    ws = torch.empty(max(16, pa.pa_decode_workspace_size(S, 16, 128, maxL, 0)), dtype=torch.uint8, device="cuda")
+    pa.pa_decode(out[:S], q_all[:S], kc, vc, to_dev_i(b.block_tables, torch.int32),
+                 to_dev_i(b.context_lens, torch.int32), maxL, b.scale, ws)
+    run_prefill(w, out=out[S:], q=q_all[S:], kc=kc, vc=vc)
+    got = bits_of(out)
+    ex = oracle.decode(b.q, p.k_cache, p.v_cache, b.block_tables, b.context_lens, b.scale, p.dtype)
+    cd = oracle.decode(b.q, p.k_cache, abs_bits(p.v_cache), b.block_tables, b.context_lens, b.scale, p.dtype)
+    check_attention(got[:S], ex, p.dtype, "mixed: decode rows", cond=cd)
+    rows = np.arange(0, pre.q.shape[0], 61)
+    check(got[S:][rows], oracle_rows(w, rows), p.dtype, "mixed: prefill rows")
+
+
+def test_prefill_out_of_pool_block_is_flagged_not_faulted():
+    w = wl.build_workload("pfb", 8, dtype=wl.BF16, n_q_heads=16, n_kv_heads=8, head_dim=128,
+                          prefill_q_lens=[40, 30], prefill_ctx_lens=[100, 10])
+    bt = w.prefill.block_tables.copy()
+    bt[0, 2] = w.pool.num_blocks + 11
+    w.prefill.block_tables = bt
+    pa.pa_device_errors(clear=True)
+    out = run_prefill(w)
+    assert pa.pa_device_errors(clear=True) & pa.PA_DEVERR_BLOCK
+    got = bits_of(out).reshape(w.prefill.q.shape)
+    rows = np.arange(40, 70)                      # the second chunk does not touch the bad entry
+    check(got[rows], oracle_rows(w, rows), wl.BF16, "good chunk")
