@@ -50,6 +50,12 @@ def build(force: bool = False) -> str:
         subprocess.run(["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-fopenmp", "-ffp-contract=off",
                         _SRC, "-o", tmp, "-lm"], check=True)
         os.replace(tmp, so)
+        for old in os.listdir(_BUILD):          # older builds of other sources
+            if old.endswith(".so") and os.path.join(_BUILD, old) != so:
+                try:
+                    os.remove(os.path.join(_BUILD, old))
+                except OSError:
+                    pass
     return so
 
 

@@ -80,6 +80,12 @@ def build(force: bool = False, verbose: bool = False) -> str:
     os.replace(tmp, out)
     for o in objs:
         os.remove(o)
+    for old in glob.glob(os.path.join(BUILD, "libpagedattn_*.so")):   # older builds of other sources
+        if old != out:
+            try:
+                os.remove(old)
+            except OSError:
+                pass
     return out
 
 

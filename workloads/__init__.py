@@ -54,6 +54,12 @@ def build(force: bool = False) -> str:
                _SRC, "-o", tmp, "-lm"]
         subprocess.run(cmd, check=True)
         os.replace(tmp, so)
+        for old in os.listdir(_BUILD):          # older builds of other sources
+            if old.endswith(".so") and os.path.join(_BUILD, old) != so:
+                try:
+                    os.remove(os.path.join(_BUILD, old))
+                except OSError:
+                    pass
     return so
 
 
