@@ -304,13 +304,13 @@ decode_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmK, con
         }
         bmax = head_max<G>(bmax);
         const float m_new = fmaxf(m_run, bmax);
-        const float alpha = (m_new == -INFINITY) ? 1.f : exp2f(m_run - m_new);
+        const float alpha = (m_new == -INFINITY) ? 1.f : ex2(m_run - m_new);
         float psum = 0.f;
 #pragma unroll
         for (int r = 0; r < C::R; ++r) {
             const int i = (base + r) & 3;
             const int t = tg + 4 * i;
-            const float pr = (m_new == -INFINITY) ? 0.f : exp2f(sc[r] - m_new);
+            const float pr = (m_new == -INFINITY) ? 0.f : ex2(sc[r] - m_new);
             psum += pr;
             if (G > 1 || (lane & 1) == 0) pw[t * G + my_h] = pr;
         }
@@ -397,7 +397,7 @@ decode_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmK, con
         if (M != -INFINITY) {
 #pragma unroll
             for (int w = 0; w < C::NCW; ++w) {
-                const float wt = exp2f(mm[w * G + h] - M);
+                const float wt = ex2(mm[w * G + h] - M);
                 Lsum = fmaf(ml[w * G + h], wt, Lsum);
                 o0 = fmaf(mo[(w * G + h) * D + d], wt, o0);
                 o1 = fmaf(mo[(w * G + h) * D + d + 1], wt, o1);

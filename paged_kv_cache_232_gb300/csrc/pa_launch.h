@@ -22,7 +22,8 @@ struct PrefillParams {
     const int32_t* seq_lens;
     unsigned* err;
     int num_chunks, n_q_heads, n_kv_heads, max_blocks_per_seq, num_blocks;
-    int tiles_per_chunk;        // 128-row query tiles per (chunk, kv head)
+    int tiles_per_chunk;        // query tiles (or CTA units) per (chunk, kv head)
+    int lpt;                    // 1: CTAs take units longest-first (schedule fits in shared memory)
     float qk_scale_log2;
 };
 

@@ -50,18 +50,210 @@ constexpr int BAR_OFF = V_OFF + 2 * TILE;
 enum Bar { Q_FULL = 0, K_FULL = 1, K_EMPTY = 3, V_FULL = 5, V_EMPTY = 7, S_FULL = 9, P_FULL = 11, PV_DONE = 13,
            DRAIN = 15, NUM_BARS = 16 };
 constexpr int TMEM_SLOT_OFF = BAR_OFF + 16 * 8;
-constexpr int SMEM_BYTES = TMEM_SLOT_OFF + 16 + 1024;  // + alignment slack
-constexpr int THREADS = (4 * NQT + 2) * 32;
+constexpr int SCHED_OFF = TMEM_SLOT_OFF + 16;    // CTA-order scratch: query_start_loc, seq_lens, cost histogram
+constexpr int SCHED_BYTES = 24 * 1024;
+constexpr int SMEM_BYTES = SCHED_OFF + SCHED_BYTES + 1024;  // + alignment slack
+// warpgroups 0..NQT-1: softmax (one per query tile); warpgroup NQT: TMA warp, MMA warp, two idle
+constexpr int THREADS = (4 * NQT + 4) * 32;
 constexpr int TMA_WARP = 4 * NQT, MMA_WARP = 4 * NQT + 1;
+// Register split: the launch gives every thread 168 (65536 / 384, rounded down to 8); the
+// producer warpgroup drops to 88 and each softmax warpgroup rises to 208, so the totals match
+// (128 x 88 + 256 x 208 = 384 x 168 = 64512) and every SMSP keeps 208 + 208 + 88 per lane.
+constexpr int REGS_SOFTMAX = 208, REGS_PRODUCER = 88;
+static_assert(NQT * 128 * REGS_SOFTMAX + 128 * REGS_PRODUCER <= THREADS * 168, "register split exceeds the launch");
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t O_COL = 256;         // S_t at columns 128 t, O_t at 256 + 128 t
-constexpr float RESCALE_LOG2 = 8.f;
 
 }  // namespace pf
 
 __device__ __forceinline__ void sts128(uint32_t addr, uint4 v) {
     asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
                  : "memory");
+}
+
+// Key tiles a unit (a pair of query tiles: tokens [j0, j0 + span) of chunk c) streams.
+__device__ __forceinline__ int unit_cost(const int* qsl, const int* kvl, int c, int pair, int span, int cap) {
+    const int q_len = qsl[c + 1] - qsl[c], kv_len = kvl[c];
+    const int j0 = pair * span;
+    if (q_len < 0 || kv_len < q_len || kv_len > cap || j0 >= q_len) return 0;
+    return (kv_len - q_len + min(j0 + span, q_len) + pf::BN - 1) / pf::BN;
+}
+
+// The unit this CTA runs under longest-first order: every CTA computes the same counting sort
+// of all units by cost (descending, ties by unit index) and takes the entry at its blockIdx.
+// Uses the CTA-order scratch in shared memory; all threads of the CTA must call it.
+template <int SPAN>
+__device__ __forceinline__ int lpt_unit(const PrefillParams& p, unsigned char* scratch) {
+    const int C = p.num_chunks, per_unit = C * p.n_kv_heads;
+    const int U = p.tiles_per_chunk * per_unit;
+    const int cap = p.max_blocks_per_seq * 16;
+    const int ncost = cap / pf::BN + 2;
+    int* qsl = reinterpret_cast<int*>(scratch);
+    int* kvl = qsl + C + 1;
+    int* hist = kvl + C;
+    int* sel = hist + ncost;  // [0] bucket, [1] rank within the bucket, [2] chosen unit, [3..] warp counts
+    const int tid = threadIdx.x, nt = blockDim.x;
+    for (int i = tid; i <= C; i += nt) qsl[i] = __ldg(p.query_start_loc + i);
+    for (int i = tid; i < C; i += nt) kvl[i] = __ldg(p.seq_lens + i);
+    for (int i = tid; i < ncost; i += nt) hist[i] = 0;
+    __syncthreads();
+    for (int u = tid; u < U; u += nt) {
+        const int cst = min(unit_cost(qsl, kvl, (u / p.n_kv_heads) % C, u / per_unit, SPAN, cap), ncost - 1);
+        atomicAdd(&hist[cst], 1);
+    }
+    __syncthreads();
+    const int b = blockIdx.x;
+    if (tid < 32) {
+        // descending scan of the histogram; find the bucket holding position b
+        int before = 0;
+        for (int top = ncost - 1; top >= 0; top -= 32) {
+            const int k = top - tid;
+            const int v = (k >= 0) ? hist[k] : 0;
+            int incl = v;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int y = __shfl_up_sync(0xffffffffu, incl, o);
+                if (tid >= o) incl += y;
+            }
+            const int start = before + incl - v;
+            if (v > 0 && b >= start && b < start + v) {
+                sel[0] = k;
+                sel[1] = b - start;
+            }
+            before += __shfl_sync(0xffffffffu, incl, 31);
+        }
+    }
+    __syncthreads();
+    const int want = sel[0], rank = sel[1];
+    // the rank-th unit (ascending index) whose cost is `want`
+    int seen = 0;
+    for (int base = 0; base < U; base += nt) {
+        const int u = base + tid;
+        const bool hit = u < U && min(unit_cost(qsl, kvl, (u / p.n_kv_heads) % C, u / per_unit, SPAN, cap),
+                                      ncost - 1) == want;
+        const unsigned bal = __ballot_sync(0xffffffffu, hit);
+        if ((tid & 31) == 0) sel[3 + (tid >> 5)] = __popc(bal);
+        __syncthreads();
+        int off = seen;
+        for (int w = 0; w < (tid >> 5); ++w) off += sel[3 + w];
+        const int mine = off + __popc(bal & ((1u << (tid & 31)) - 1u));
+        if (hit && mine == rank) sel[2] = u;
+        int tot = 0;
+        for (int w = 0; w < (nt + 31) / 32; ++w) tot += sel[3 + w];
+        __syncthreads();
+        seen += tot;
+        if (seen > rank) break;
+    }
+    __syncthreads();
+    const int chosen = sel[2];
+    __syncthreads();
+    return chosen;
+}
+
+// Words src[from], src[from + 2], ..., src[from + 30] into 16 TMEM columns at taddr.
+__device__ __forceinline__ void tmem_store16_stride2(uint32_t taddr, const uint32_t (&src)[64], int from) {
+    uint32_t v[16];
+#pragma unroll
+    for (int e = 0; e < 16; ++e) v[e] = src[from + 2 * e];
+    tc::st16(taddr, v);
+}
+
+// Online softmax for 64 keys (half h of a 128-key tile) of this thread's row.  On entry r holds
+// the S values; on exit the weights are in TMEM over those S columns -- for each 32-key piece,
+// P_hi (16 columns) then P_lo (16 columns) -- and l / tile_l / m_ref are updated.  m_ref is an
+// integer (log2 units), so every rescale is an exact power of two.  Weights are allowed up to
+// 2^8 above the reference; a row whose keys outgrow that redoes the half with a raised
+// reference (reloading S, which is still intact), rescaling O, l and the first half's weights.
+template <bool BF16, int h>
+__device__ __forceinline__ void softmax_half(uint32_t (&r)[64], const uint32_t tS, const uint32_t tO,
+                                             const bool masked, const int kbase, const int lim, const float sc,
+                                             float& m_ref, float& l, float& tile_l) {
+    using F = F16x2<BF16>;
+    constexpr uint32_t kBits256 = BF16 ? 0x4380u : 0x5C00u;  // 2^8 as a packed 16-bit value
+    const uint32_t tcol = tS + 64 * h;
+    // decided per warp: the branch holds warp-collective TMEM loads and stores
+    bool redo = __any_sync(0xffffffffu, m_ref == -INFINITY);
+#pragma unroll 1
+    for (int attempt = 0; attempt < 2; ++attempt) {
+        if (attempt == 1) {
+            tc::ld64(tcol, r);  // the weights pass overwrote r
+            tc::wait_ld();
+        }
+        if (masked) {
+#pragma unroll
+            for (int e = 0; e < 64; ++e)
+                if (kbase + 64 * h + e > lim) r[e] = __float_as_uint(-INFINITY);
+        }
+        if (redo) {
+            float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+            for (int e = 0; e < 64; ++e) mx[e & 3] = fmaxf(mx[e & 3], __uint_as_float(r[e]));
+            const float mt = ceilf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * sc);
+            float alpha = 1.f;
+            if (m_ref == -INFINITY) {
+                m_ref = mt;
+            } else if (mt > m_ref) {
+                alpha = ex2(m_ref - mt);
+                m_ref = mt;
+            }
+            l *= alpha;
+            tile_l *= alpha;
+            if (__any_sync(0xffffffffu, alpha != 1.f)) {
+                // O is settled: this tile's S was issued after the previous PV and the S commit
+                // covers every earlier MMA of the issuing thread
+#pragma unroll 1
+                for (int q = 0; q < 8; ++q) {
+                    uint32_t o[16];
+                    tc::ld16(tO + 16 * q, o);
+                    tc::wait_ld();
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+                    tc::st16(tO + 16 * q, o);
+                }
+                if (h == 1) {  // the weights already written for keys 0..63 of this tile
+#pragma unroll 1
+                    for (int q = 0; q < 4; ++q) {
+                        uint32_t w[16];
+                        tc::ld16(tS + 16 * q, w);
+                        tc::wait_ld();
+#pragma unroll
+                        for (int e = 0; e < 16; ++e) {
+                            const float2 u = F::unpack(w[e]);
+                            w[e] = F::pack_rn(u.x * alpha, u.y * alpha);
+                        }
+                        tc::st16(tS + 16 * q, w);
+                    }
+                }
+            }
+        }
+        const float mu = (m_ref == -INFINITY) ? 0.f : m_ref;
+        const float2 sc2 = make_float2(sc, sc), nmu2 = make_float2(-mu, -mu);
+        float2 ls = make_float2(0.f, 0.f);
+        uint32_t pmax = 0;
+        // in place: keys (2e, 2e+1) -> r[2e] = P_hi pair, r[2e+1] = P_lo pair
+#pragma unroll
+        for (int e = 0; e < 32; ++e) {
+            const float2 x = ffma2(make_float2(__uint_as_float(r[2 * e]), __uint_as_float(r[2 * e + 1])), sc2, nmu2);
+            const float2 w = make_float2(ex2(x.x), ex2(x.y));
+            const uint32_t hi = F::pack_rn(w.x, w.y);
+            const float2 d = fsub2(w, F::unpack(hi));
+            r[2 * e] = hi;
+            r[2 * e + 1] = F::pack_rn(d.x, d.y);
+            ls = fadd2(ls, w);
+            pmax = umax16x2(pmax, hi);
+        }
+        const uint32_t pm = (pmax & 0xFFFFu) > (pmax >> 16) ? (pmax & 0xFFFFu) : (pmax >> 16);
+        if (attempt == 0 && __any_sync(0xffffffffu, pm > kBits256)) {
+            redo = true;
+            continue;
+        }
+        tmem_store16_stride2(tcol + 0, r, 0);    // piece 2h:   P_hi
+        tmem_store16_stride2(tcol + 16, r, 1);   //             P_lo
+        tmem_store16_stride2(tcol + 32, r, 32);  // piece 2h+1: P_hi
+        tmem_store16_stride2(tcol + 48, r, 33);  //             P_lo
+        tile_l += ls.x + ls.y;
+        break;
+    }
 }
 
 template <int G, bool BF16>
@@ -78,10 +270,13 @@ prefill_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmK, c
     volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(smem + TMEM_SLOT_OFF);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    // CTAs with the most keys (largest query offset) are scheduled first
+    // Work unit u = (pair * C + chunk) * Hkv + head.  CTAs are dispatched in blockIdx order,
+    // so handing out units longest-first gives longest-processing-time list scheduling.
     const int per_unit = p.num_chunks * p.n_kv_heads;
-    const int unit = p.tiles_per_chunk - 1 - (int)(blockIdx.x / per_unit);
-    const int rem = blockIdx.x % per_unit;
+    int u_sel = (p.tiles_per_chunk - 1 - (int)(blockIdx.x / per_unit)) * per_unit + (int)(blockIdx.x % per_unit);
+    if (p.lpt) u_sel = lpt_unit<TQ * NQT>(p, smem + SCHED_OFF);
+    const int unit = u_sel / per_unit;
+    const int rem = u_sel % per_unit;
     const int c = rem / p.n_kv_heads, g = rem % p.n_kv_heads;
 
     const int q0 = __ldg(p.query_start_loc + c);
@@ -125,6 +320,10 @@ prefill_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmK, c
     __syncthreads();
     tc::fence_after();
     const uint32_t tmem = *tmem_slot;
+    if (warp < 4 * NQT)
+        asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(REGS_SOFTMAX));
+    else
+        asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(REGS_PRODUCER));
 
     if (warp < 4 * NQT) {
         // ------------------------------------------------------------ softmax warpgroups
@@ -159,70 +358,14 @@ prefill_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmK, c
             tc::fence_after();
             const int kbase = i * BN;
             const bool masked = kbase + BN - 1 > lim_min;
-            // pass 1: row max of this key tile (masked keys excluded)
-            float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-#pragma unroll 1
-            for (int q = 0; q < 4; ++q) {
-                uint32_t raw[32];
-                tc::ld32(tS + 32 * q, raw);
-                tc::wait_ld();
-#pragma unroll
-                for (int e = 0; e < 32; ++e) {
-                    float v = __uint_as_float(raw[e]);
-                    if (masked && kbase + 32 * q + e > lim) v = -INFINITY;
-                    mx[e & 3] = fmaxf(mx[e & 3], v);
-                }
-            }
-            const float mt = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * sc;
-            float alpha = 1.f;
-            bool rescale = false;
-            if (m_ref == -INFINITY) {
-                m_ref = mt;
-            } else if (mt > m_ref + RESCALE_LOG2) {
-                alpha = exp2f(m_ref - mt);
-                m_ref = mt;
-                rescale = true;
-            }
-            // O is settled here: this tile's S was issued after the previous PV, and the S
-            // commit covers every earlier MMA of the issuing thread
-            if (__any_sync(0xffffffffu, rescale)) {
-#pragma unroll 1
-                for (int q = 0; q < 4; ++q) {
-                    uint32_t o[32];
-                    tc::ld32(tO + 32 * q, o);
-                    tc::wait_ld();
-#pragma unroll
-                    for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
-                    tc::st32(tO + 32 * q, o);
-                }
-            }
-            const float mu = (m_ref == -INFINITY) ? 0.f : m_ref;
-            // pass 2: weights, written over the S piece just read as P_hi (16 columns) + P_lo (16)
-            float ls[2] = {0.f, 0.f};
-#pragma unroll 1
-            for (int q = 0; q < 4; ++q) {
-                uint32_t raw[32];
-                tc::ld32(tS + 32 * q, raw);
-                tc::wait_ld();
-                uint32_t hi[16], lo[16];
-#pragma unroll
-                for (int e = 0; e < 16; ++e) {
-                    float s0 = __uint_as_float(raw[2 * e]), s1 = __uint_as_float(raw[2 * e + 1]);
-                    if (masked) {
-                        if (kbase + 32 * q + 2 * e > lim) s0 = -INFINITY;
-                        if (kbase + 32 * q + 2 * e + 1 > lim) s1 = -INFINITY;
-                    }
-                    const float a = exp2f(fmaf(s0, sc, -mu));
-                    const float b = exp2f(fmaf(s1, sc, -mu));
-                    hi[e] = F::pack_rn(a, b);
-                    const float2 u = F::unpack(hi[e]);
-                    lo[e] = F::pack_rn(a - u.x, b - u.y);
-                    ls[e & 1] += a + b;
-                }
-                tc::st16(tS + 32 * q, hi);
-                tc::st16(tS + 32 * q + 16, lo);
-            }
-            l = l * alpha + (ls[0] + ls[1]);
+            float tile_l = 0.f;
+            uint32_t ra[64], rb[64];
+            tc::ld64(tS, ra);
+            tc::ld64(tS + 64, rb);
+            tc::wait_ld();
+            softmax_half<BF16, 0>(ra, tS, tO, masked, kbase, lim, sc, m_ref, l, tile_l);
+            softmax_half<BF16, 1>(rb, tS, tO, masked, kbase, lim, sc, m_ref, l, tile_l);
+            l += tile_l;
             tc::wait_st();
             tc::fence_before();
             mbar_arrive(bars + 8 * (P_FULL + t));
@@ -291,61 +434,63 @@ prefill_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmK, c
                 }
             }
         }
-    } else {
-        // ------------------------------------------------------------ MMA warp
+    } else if (warp == MMA_WARP && lane == 0) {
+        // ------------------------------------------------------------ MMA issue (one thread)
         constexpr uint32_t ID_QK = tc::idesc_f16(BF16, false, BM, BN);
         constexpr uint32_t ID_PV = tc::idesc_f16(BF16, true, BM, D);
-        bool ok = __all_sync(0xffffffffu, mbar_wait(bars + 8 * Q_FULL, 0, p.err));
+        // descriptors of the tile bases as (low, high) words; a K-step adds its byte offset >> 4
+        // to the start-address field in the low word (addresses stay below 256 KB: no carry)
+        const uint64_t dq = tc::sdesc_sw128(sQ, 16, 1024), dk = tc::sdesc_sw128(sK, 16, 1024);
+        const uint64_t dv = tc::sdesc_sw128(sV, SLAB, 1024);
+        const uint32_t q_lo = (uint32_t)dq, q_hi = (uint32_t)(dq >> 32);
+        const uint32_t k_lo = (uint32_t)dk, k_hi = (uint32_t)(dk >> 32);
+        const uint32_t v_lo = (uint32_t)dv, v_hi = (uint32_t)(dv >> 32);
+        bool ok = mbar_wait(bars + 8 * Q_FULL, 0, p.err);
         int k_ready = -1, v_ready = -1, issued = 0;
         auto wait_k = [&](int jt) -> bool {
             if (jt <= k_ready) return true;
-            if (!__all_sync(0xffffffffu, mbar_wait(bars + 8 * (K_FULL + (jt & 1)), (jt >> 1) & 1, p.err))) return false;
+            if (!mbar_wait(bars + 8 * (K_FULL + (jt & 1)), (jt >> 1) & 1, p.err)) return false;
             k_ready = jt;
             return true;
         };
         auto wait_v = [&](int jt) -> bool {
             if (jt <= v_ready) return true;
-            if (!__all_sync(0xffffffffu, mbar_wait(bars + 8 * (V_FULL + (jt & 1)), (jt >> 1) & 1, p.err))) return false;
+            if (!mbar_wait(bars + 8 * (V_FULL + (jt & 1)), (jt >> 1) & 1, p.err)) return false;
             v_ready = jt;
             return true;
         };
         auto issue_s = [&](int t, int jt) {
-            if (lane == 0) {
-                const uint32_t q = sQ + t * TILE, k = sK + (jt & 1) * TILE;
+            const uint32_t qa = q_lo + (uint32_t)((t * TILE) >> 4), ka = k_lo + (uint32_t)(((jt & 1) * TILE) >> 4);
+            const uint32_t dS = tmem + (uint32_t)(t * BN);
 #pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint32_t off = (kk >> 2) * SLAB + (kk & 3) * 32;
-                    tc::mma_f16_ss(tmem + (uint32_t)(t * BN), tc::sdesc_sw128(q + off, 16, 1024),
-                                   tc::sdesc_sw128(k + off, 16, 1024), ID_QK, kk > 0);
-                }
-                tc::commit(bars + 8 * (S_FULL + t));
+            for (int kk = 0; kk < D / 16; ++kk) {
+                const uint32_t off = (uint32_t)((((kk >> 2) * SLAB) + (kk & 3) * 32) >> 4);
+                tc::mma_f16_ss_w(dS, qa + off, q_hi, ka + off, k_hi, ID_QK, kk > 0);
             }
+            tc::commit(bars + 8 * (S_FULL + t));
             ++issued;
         };
         auto issue_pv = [&](int t, int jt) {
-            if (lane == 0) {
-                const uint32_t v = sV + (jt & 1) * TILE;
-                const uint32_t pS = tmem + (uint32_t)(t * BN);
+            const uint32_t va = v_lo + (uint32_t)(((jt & 1) * TILE) >> 4);
+            const uint32_t pS = tmem + (uint32_t)(t * BN);
+            const uint32_t dO = tmem + O_COL + (uint32_t)(t * D);
 #pragma unroll
-                for (int kk = 0; kk < BN / 16; ++kk) {
-                    // keys 16kk..16kk+15: P_hi at column 32(kk/2) + 8(kk%2) of S_t, P_lo 16 further
-                    const uint32_t pc = (uint32_t)(32 * (kk >> 1) + 8 * (kk & 1));
-                    const uint64_t vd = tc::sdesc_sw128(v + kk * 2048, SLAB, 1024);
-                    tc::mma_f16_ts(tmem + O_COL + (uint32_t)(t * D), pS + pc, vd, ID_PV, (jt > 0 || kk > 0));
-                    tc::mma_f16_ts(tmem + O_COL + (uint32_t)(t * D), pS + pc + 16, vd, ID_PV, 1u);
-                }
-                tc::commit(bars + 8 * (PV_DONE + t));
+            for (int kk = 0; kk < BN / 16; ++kk) {
+                // keys 16kk..16kk+15: P_hi at column 32(kk/2) + 8(kk%2) of S_t, P_lo 16 further
+                const uint32_t pc = (uint32_t)(32 * (kk >> 1) + 8 * (kk & 1));
+                const uint32_t vb = va + (uint32_t)((kk * 2048) >> 4);
+                tc::mma_f16_ts_w(dO, pS + pc, vb, v_hi, ID_PV, (jt > 0 || kk > 0));
+                tc::mma_f16_ts_w(dO, pS + pc + 16, vb, v_hi, ID_PV, 1u);
             }
+            tc::commit(bars + 8 * (PV_DONE + t));
             ++issued;
         };
         if (ok) ok = wait_k(0);
         if (ok) {
             tc::fence_after();
-#pragma unroll
-            for (int t = 0; t < NQT; ++t)
-                if (n_kt[t] > 0) issue_s(t, 0);
-            if (lane == 0) tc::commit(bars + 8 * K_EMPTY);
-            __syncwarp();
+            if (n_kt[0] > 0) issue_s(0, 0);
+            if (n_kt[NQT - 1] > 0) issue_s(NQT - 1, 0);
+            tc::commit(bars + 8 * K_EMPTY);
         }
         for (int i = 0; i < n_max && ok; ++i) {
             bool next_k = false;
@@ -355,42 +500,36 @@ prefill_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmK, c
                 ok = wait_v(i);
                 if (!ok) break;
                 const int z0 = max(kv_len, i * BN), z1 = min(((kv_len + 15) / 16) * 16, (i + 1) * BN);
-                const int nz = z1 - z0;
-                for (int e = lane; e < 16 * max(nz, 0); e += 32) {
+                for (int e = 0; e < 16 * max(z1 - z0, 0); ++e) {
                     const int row = z0 - i * BN + e / 16;
                     sts128(sV + (i & 1) * TILE + ((e / 8) & 1) * SLAB + row * 128 + (e & 7) * 16,
                            make_uint4(0u, 0u, 0u, 0u));
                 }
                 tc::fence_async_smem();
-                __syncwarp();
             }
 #pragma unroll
             for (int t = 0; t < NQT && ok; ++t) {
-                if (i >= n_kt[t]) continue;
-                ok = __all_sync(0xffffffffu, mbar_wait(bars + 8 * (P_FULL + t), i & 1, p.err)) && wait_v(i);
+                const int nkt_t = (t == 0) ? n_kt[0] : n_kt[NQT - 1];
+                if (i >= nkt_t) continue;
+                ok = mbar_wait(bars + 8 * (P_FULL + t), i & 1, p.err) && wait_v(i);
                 if (!ok) break;
                 tc::fence_after();
                 issue_pv(t, i);
-                if (i + 1 < n_kt[t]) {
+                if (i + 1 < nkt_t) {
                     ok = wait_k(i + 1);
                     if (!ok) break;
                     tc::fence_after();
                     issue_s(t, i + 1);
                     next_k = true;
                 }
-                __syncwarp();
             }
             if (!ok) break;
-            if (lane == 0) {
-                tc::commit(bars + 8 * (V_EMPTY + (i & 1)));
-                if (next_k) tc::commit(bars + 8 * (K_EMPTY + ((i + 1) & 1)));
-            }
-            __syncwarp();
+            tc::commit(bars + 8 * (V_EMPTY + (i & 1)));
+            if (next_k) tc::commit(bars + 8 * (K_EMPTY + ((i + 1) & 1)));
         }
-        // every MMA this warp issued must be complete before TMEM is released
+        // every MMA issued must be complete before TMEM is released
         if (issued > 0) {
-            if (lane == 0) tc::commit(bars + 8 * DRAIN);
-            __syncwarp();
+            tc::commit(bars + 8 * DRAIN);
             (void)mbar_wait(bars + 8 * DRAIN, 0, p.err);
         }
     }
@@ -413,6 +552,9 @@ static cudaError_t launch_prefill_t(const PrefillParams& p, const CUtensorMap& t
     const int units = (p.tiles_per_chunk + pf::NQT - 1) / pf::NQT;
     PrefillParams q = p;
     q.tiles_per_chunk = units;
+    const int ncost = p.max_blocks_per_seq * 16 / pf::BN + 2;
+    const long sched_words = 2L * p.num_chunks + 1 + ncost + 3 + pf::THREADS / 32;
+    q.lpt = (sched_words * 4 <= pf::SCHED_BYTES) ? 1 : 0;
     const int grid = units * p.num_chunks * p.n_kv_heads;
     kern<<<grid, pf::THREADS, pf::SMEM_BYTES, st>>>(q, tmK, tmV);
     return cudaGetLastError();
