@@ -151,6 +151,35 @@ int pa_decode_splitk(void* out, const void* q, const void* k_cache, const void* 
                      void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * pa_decode_splitk_static -- pa_decode_splitk without a caller-provided workspace.
+ * The pages have no counterpart to this entry point; it exists for callers that cannot
+ * allocate device memory themselves: code running inside a framework that owns every
+ * device allocation (a stray cudaMalloc would bypass its pool and its accounting), code on
+ * a latency-critical path that cannot afford an allocation's implicit synchronisation, and
+ * code running under a stream-capture mode in which cudaMalloc is not permitted.
+ *
+ *  The split-K partials go to a fixed scratch array of PA_STATIC_SCRATCH_BYTES inside the
+ *  library's device image; every GPU that loads the library keeps that memory until the
+ *  process exits.  Arguments and results are those of pa_decode_splitk, minus the workspace.
+ *  Returns PA_ERR_WORKSPACE, launching nothing, when these sizes need more partials than the
+ *  array holds (pa_decode_workspace_size(num_seqs, n_q_heads, head_dim, max_context_len,
+ *  partition_tokens) > PA_STATIC_SCRATCH_BYTES).
+ *  The first call on a device looks up the array's device address (cudaGetSymbolAddress)
+ *  with that device current; make that first call before any stream capture.
+ *  All calls share the one array and it keeps whatever the last call wrote (nothing in it
+ *  needs to start at zero): calls that can run at the same time on the GPU -- on different
+ *  streams, or from different threads -- race on it and must be serialised by the caller.
+ *  No cudaMalloc, cudaFree or other allocating call is made.
+ */
+#define PA_STATIC_SCRATCH_BYTES (16u << 20)
+
+int pa_decode_splitk_static(void* out, const void* q, const void* k_cache, const void* v_cache,
+                            const int32_t* block_tables, int max_blocks_per_seq, const int32_t* context_lens,
+                            int max_context_len, int num_seqs, int n_q_heads, int n_kv_heads, int head_dim,
+                            int block_size, int64_t num_blocks, float scale, int dtype, int partition_tokens,
+                            void* stream);
+
+/*
  * pa_prefill_chunk -- attention for ragged prefill chunks that attend to their
  * earlier cached context, on the tcgen05 tensor cores (head_dim 128 only).
  * Source: mini_engine, "Custom CUDA kernels" (paged prefill attention: tiled,

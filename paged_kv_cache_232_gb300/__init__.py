@@ -23,7 +23,9 @@ DEFAULT_PARTITION_TOKENS = 256
 EXPORTED = (
     "pa_reshape_and_cache", "pa_decode_workspace_size", "pa_decode", "pa_decode_plan", "pa_decode_v1",
     "pa_decode_splitk", "pa_prefill_chunk", "pa_device_errors", "pa_status_string", "pa_version",
+    "pa_decode_splitk_static",
 )
+STATIC_SCRATCH_BYTES = 16 << 20
 
 
 class PagedAttnError(RuntimeError):
@@ -64,6 +66,9 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
     L.pa_decode_splitk.argtypes = [vp, vp, vp, vp, vp, i32, vp, i32, i32, i32, i32, i32, i32, i64, f32, i32, i32, vp,
                                    sz, vp]
     L.pa_decode_splitk.restype = i32
+    L.pa_decode_splitk_static.argtypes = [vp, vp, vp, vp, vp, i32, vp, i32, i32, i32, i32, i32, i32, i64, f32, i32,
+                                          i32, vp]
+    L.pa_decode_splitk_static.restype = i32
     L.pa_prefill_chunk.argtypes = [vp, vp, vp, vp, vp, i32, vp, vp, i32, i32, i32, i32, i32, i32, i64, f32, i32, vp]
     L.pa_prefill_chunk.restype = i32
     L.pa_device_errors.argtypes = [i32]
@@ -194,6 +199,19 @@ def pa_decode_splitk(out, q, k_cache, v_cache, block_tables, context_lens, max_c
     st = load().pa_decode_splitk(po, pq, pk, pv, pbt, mb, pcl, int(max_context_len), S, hq, hkv, d, bs, nb,
                                  float(scale), dt, int(partition_tokens), wp, wb, _stream(stream, q.device))
     _check(st, "pa_decode_splitk")
+
+
+def pa_decode_splitk_static(out, q, k_cache, v_cache, block_tables, context_lens, max_context_len: int,
+                            scale: float, partition_tokens: int = 0, stream=None) -> None:
+    """Split-K decode for callers that cannot allocate device memory: the partials live in a
+    fixed STATIC_SCRATCH_BYTES array inside the library (shared by all calls, so calls that
+    overlap on the GPU race).  Raises PagedAttnError(PA_ERR_WORKSPACE) when the sizes need
+    more than that."""
+    dt, nb, bs, hkv, d, S, hq, mb, (po, pq, pk, pv, pbt, pcl) = _decode_common(out, q, k_cache, v_cache, block_tables,
+                                                                             context_lens)
+    st = load().pa_decode_splitk_static(po, pq, pk, pv, pbt, mb, pcl, int(max_context_len), S, hq, hkv, d, bs, nb,
+                                        float(scale), dt, int(partition_tokens), _stream(stream, q.device))
+    _check(st, "pa_decode_splitk_static")
 
 
 def pa_prefill_chunk(out, q, k_cache, v_cache, block_tables, query_start_loc, seq_lens, max_q_len: int, scale: float,
