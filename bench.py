@@ -218,14 +218,24 @@ def run_ours(args, rank, world, local_rank):
     maxL = int(b.context_lens.max())
     ws = torch.empty(max(pa.pa_decode_workspace_size(S, hq, D, maxL, 0), 16), dtype=torch.uint8, device=dev)
     which, part = pa.pa_decode_plan(S, p.n_kv_heads, maxL)
+    if args.decode_path == "v1":
+        which = 1
+    elif args.decode_path == "splitk":
+        which, part = 2, (args.partition or part)
     stages = []   # name, launch, algorithmic amount, kind
     if wr is not None:
         key, val, sm = dev_bits(wr.key), dev_bits(wr.value), dev_int(wr.slot_mapping)
         stages.append(("write", lambda: pa.pa_reshape_and_cache(key, val, kc, vc, sm), write_bytes(wr, p), "hbm"))
     dec_logical = decode_bytes(b, p)
     dec_unique = unique_decode_bytes(b, p)
-    stages.append(("decode", lambda: pa.pa_decode(out[:S], q[:S], kc, vc, bt, cl, maxL, b.scale, ws), dec_unique,
-                   "hbm"))
+    if args.decode_path == "auto":
+        dec_fn = lambda: pa.pa_decode(out[:S], q[:S], kc, vc, bt, cl, maxL, b.scale, ws)
+    elif which == 1:
+        dec_fn = lambda: pa.pa_decode_v1(out[:S], q[:S], kc, vc, bt, cl, b.scale)
+    else:
+        ws = torch.empty(max(pa.pa_decode_workspace_size(S, hq, D, maxL, part), 16), dtype=torch.uint8, device=dev)
+        dec_fn = lambda: pa.pa_decode_splitk(out[:S], q[:S], kc, vc, bt, cl, maxL, b.scale, ws, part)
+    stages.append(("decode", dec_fn, dec_unique, "hbm"))
     if pre is not None:
         pbt, qsl, sl = dev_int(pre.block_tables), dev_int(pre.query_start_loc), dev_int(pre.seq_lens)
         stages.append(("prefill", lambda: pa.pa_prefill_chunk(out[S:], q[S:], kc, vc, pbt, qsl, sl, pre.max_q_len,
@@ -327,7 +337,7 @@ def run_ours(args, rank, world, local_rank):
         "workload": wl.WORKLOAD_NAMES[k],
         "num_seqs": int(S), "n_q_heads": int(hq), "n_kv_heads": p.n_kv_heads, "head_dim": p.head_dim,
         "block_size": p.block_size, "total_context_tokens": int(b.context_lens.sum()),
-        "decode_path": "one-pass" if which == 1 else f"split-K/{part}",
+        "decode_path": ("one-pass" if which == 1 else f"split-K/{part}") + ("" if args.decode_path == "auto" else " (forced)"),
         "l2": "512 MiB memset between timed steps (outside the events)",
         "parallelism": f"replicas x{world} (independent batches, no collective)",
     }
@@ -484,6 +494,9 @@ def main(argv=None):
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default="step256")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--decode-path", choices=["auto", "v1", "splitk"], default="auto",
+                    help="force the one-pass or split-K decode kernel instead of the library's dispatcher")
+    ap.add_argument("--partition", type=int, default=0, help="split-K piece length in tokens (with --decode-path splitk)")
     ap.add_argument("--traffic", type=float, default=None,
                     help="dram bytes per decode launch from an ncu capture of this workload (reported as-is)")
     args = ap.parse_args(argv)

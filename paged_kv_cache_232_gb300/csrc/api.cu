@@ -179,12 +179,18 @@ int decode_impl(void* out, const void* q, const void* k_cache, const void* v_cac
 
 // Dispatcher (mini_engine, "Custom CUDA kernels": split-K when few sequences or long
 // contexts cannot fill the GPU, the one-pass kernel when there is enough parallelism).
-// The thresholds are this library's, set from GB300 measurements.
+// The thresholds are this library's, set from GB300 measurements: the one-pass kernel wins
+// as soon as there is a (sequence, KV head) unit per SM and contexts are short; otherwise
+// split-K, with the piece doubled from 256 tokens while the grid still holds four pieces per
+// SM (longer pieces amortise each CTA's pipeline start and shrink the merge).
 int plan(int num_seqs, int n_kv_heads, int max_context_len, int sm_count, int* part_tokens) {
-    const int units = num_seqs * n_kv_heads;
-    if (part_tokens) *part_tokens = PA_DEFAULT_PARTITION_TOKENS;
+    const int64_t units = (int64_t)num_seqs * n_kv_heads;
+    int part = PA_DEFAULT_PARTITION_TOKENS;
+    if (part_tokens) *part_tokens = part;
     if (max_context_len <= PA_DEFAULT_PARTITION_TOKENS) return 1;
-    if (units >= 4 * sm_count && max_context_len <= 4096) return 1;
+    if (units >= sm_count && max_context_len <= 8192) return 1;
+    while (part < 4096 && units * ((max_context_len + 2 * part - 1) / (2 * part)) >= 4 * (int64_t)sm_count) part *= 2;
+    if (part_tokens) *part_tokens = part;
     return 2;
 }
 

@@ -10,25 +10,30 @@
 //  * A query tile is 128 rows = 128 / G query tokens x the G heads of one KV head, so every
 //    K/V tile feeds all G heads (GQA sharing) and the MMA M dimension is a full 128.  One CTA
 //    owns two consecutive query tiles of one (chunk, KV head): both read the same K/V tiles.
-//  * Warp 8 gathers K and V tiles of 128 keys (8 paged blocks) with one 4-D TMA load per
-//    block and 64-column slab, 128-byte swizzled, into two-stage rings.  Block ids come from
-//    the chunk's block-table row; blocks past the sequence load zeros (out-of-range block
-//    coordinate).
-//  * Warp 9 owns all 512 TMEM columns -- S_0 | S_1 | O_0 | O_1, 128 each -- and issues the
-//    MMAs from one lane:  S_t = Q_t K^T (both operands from shared memory, K-major) and
-//    O_t += P_t V (P from TMEM, V from shared memory, MN-major).  Issue order per key tile
-//    j is PV_0(j), S_0(j+1), PV_1(j), S_1(j+1): while one softmax warpgroup works on its S,
-//    the tensor cores run the other tile's PV and next QK (ping-pong).
-//  * Warpgroup t (warps 4t..4t+3; thread = query row = TMEM lane) reads its S row in
-//    32-column pieces twice (max, then probabilities), applies the causal mask only on key
-//    tiles that reach past the tile's smallest row limit, and keeps an online softmax in
-//    base 2 with a lazily updated reference max: O and l are rescaled only when the row max
-//    grows by more than 2^8; otherwise weights up to 2^8 are kept (exact in fp32, and the
-//    final O / l uses the same reference).  The PV operand is 16-bit, and one 16-bit weight
-//    costs up to 2^-9 relative -- too much next to the bf16 output rounding for a 2e-3
-//    bound -- so each weight goes in as P_hi = round(p) plus P_lo = round(p - P_hi) (about
-//    16 significant bits together), both written over the S columns just read, and the PV
-//    step issues one MMA for each half into the same fp32 accumulator.
+//  * Two producer warps (one for K, one for V) gather tiles of 128 keys (8 paged blocks) with
+//    one 4-D TMA load per block and 64-column slab, 128-byte swizzled, into two-stage rings.
+//    Block ids come from the chunk's block-table row; blocks past the sequence load zeros
+//    (out-of-range block coordinate); the V producer zeroes the stray rows of the sequence's
+//    last, partial block before it hands the last stage over.
+//  * TMEM (512 columns): for each query tile t two 64-column S buffers at 128 t and the O
+//    accumulator at 256 + 128 t.  Keys are processed in 64-key sub-tiles u: S_t(u) = Q_t K^T
+//    (both operands from shared memory, K-major) lands in buffer u % 2, so the next
+//    sub-tile's S is computed while the softmax works on this one; O_t += P_t(u) V reads the
+//    weights from TMEM (the A operand) and V from shared memory (MN-major).
+//  * One thread per query tile issues that tile's MMAs (warps 9 and 11): a wait on an mbarrier
+//    costs the issuing thread a few hundred cycles even when the phase is complete (shared
+//    memory is saturated by the operand reads), and with two issuers one tile's MMAs keep the
+//    tensor pipe busy while the other issuer waits.
+//  * Warpgroup t (warps 4t..4t+3; thread = query row = TMEM lane) reads its 64 S values,
+//    applies the causal mask only on sub-tiles that reach past the tile's smallest row limit,
+//    and keeps an online softmax in base 2 with a lazily updated integer reference max: O and l
+//    are rescaled only when the row max grows by more than 2^8; otherwise weights up to 2^8 are
+//    kept (exact in fp32, and the final O / l uses the same reference).  The PV operand is
+//    16-bit, and one 16-bit weight costs up to 2^-9 relative -- too much next to the bf16
+//    output rounding for a 2e-3 bound -- so each weight goes in as P_hi = round(p) plus
+//    P_lo = round(p - P_hi) (about 16 significant bits together), both written over the S
+//    columns just read, and the PV step issues one MMA for each half into the same fp32
+//    accumulator.
 //  * Every mbarrier wait has a time limit; on expiry the kernel flags PA_DEVERR_TIMEOUT, all
 //    roles leave their loops, and the TMEM columns are released before exit.
 #include "pa_launch.h"
@@ -47,22 +52,28 @@ constexpr int Q_OFF = 0;                // NQT tiles
 constexpr int K_OFF = NQT * TILE;       // two stages
 constexpr int V_OFF = K_OFF + 2 * TILE; // two stages
 constexpr int BAR_OFF = V_OFF + 2 * TILE;
-enum Bar { Q_FULL = 0, K_FULL = 1, K_EMPTY = 3, V_FULL = 5, V_EMPTY = 7, S_FULL = 9, P_FULL = 11, PV_DONE = 13,
-           DRAIN = 15, NUM_BARS = 16 };
-constexpr int TMEM_SLOT_OFF = BAR_OFF + 16 * 8;
+constexpr int BS = 64;                  // keys per S sub-tile (two per K/V stage)
+// barriers: K_FULL / V_FULL per ring stage; K_EMPTY / V_EMPTY, S_FULL and P_FULL per (query tile,
+// buffer) at index 2 t + b; PV_DONE and DRAIN per query tile; V_ZERO once (last V stage cleaned)
+enum Bar { Q_FULL = 0, K_FULL = 1, V_FULL = 3, K_EMPTY = 5, V_EMPTY = 9, S_FULL = 13, P_FULL = 17, PV_DONE = 21,
+           DRAIN = 23, V_ZERO = 25, NUM_BARS = 26 };
+constexpr int TMEM_SLOT_OFF = BAR_OFF + 32 * 8;
+static_assert(NUM_BARS <= 32, "barrier area");
 constexpr int SCHED_OFF = TMEM_SLOT_OFF + 16;    // CTA-order scratch: query_start_loc, seq_lens, cost histogram
 constexpr int SCHED_BYTES = 24 * 1024;
 constexpr int SMEM_BYTES = SCHED_OFF + SCHED_BYTES + 1024;  // + alignment slack
-// warpgroups 0..NQT-1: softmax (one per query tile); warpgroup NQT: TMA warp, MMA warp, two idle
+// warpgroups 0..NQT-1: softmax (one per query tile); warpgroup NQT: K loads, MMA issue for tile 0,
+// V loads, MMA issue for tile 1
+static_assert(NQT == 2, "one MMA-issuing warp per query tile, two tiles");
 constexpr int THREADS = (4 * NQT + 4) * 32;
-constexpr int TMA_WARP = 4 * NQT, MMA_WARP = 4 * NQT + 1;
+constexpr int TMA_WARP = 4 * NQT, MMA_WARP = 4 * NQT + 1, TMA_V_WARP = 4 * NQT + 2, MMA_WARP_1 = 4 * NQT + 3;
 // Register split: the launch gives every thread 168 (65536 / 384, rounded down to 8); the
 // producer warpgroup drops to 88 and each softmax warpgroup rises to 208, so the totals match
 // (128 x 88 + 256 x 208 = 384 x 168 = 64512) and every SMSP keeps 208 + 208 + 88 per lane.
 constexpr int REGS_SOFTMAX = 208, REGS_PRODUCER = 88;
 static_assert(NQT * 128 * REGS_SOFTMAX + 128 * REGS_PRODUCER <= THREADS * 168, "register split exceeds the launch");
 constexpr uint32_t TMEM_COLS = 512;
-constexpr uint32_t O_COL = 256;         // S_t at columns 128 t, O_t at 256 + 128 t
+constexpr uint32_t O_COL = 256;         // S_t buffers at columns 128 t + 64 b, O_t at 256 + 128 t
 
 }  // namespace pf
 
@@ -158,31 +169,29 @@ __device__ __forceinline__ void tmem_store16_stride2(uint32_t taddr, const uint3
     tc::st16(taddr, v);
 }
 
-// Online softmax for 64 keys (half h of a 128-key tile) of this thread's row.  On entry r holds
-// the S values; on exit the weights are in TMEM over those S columns -- for each 32-key piece,
-// P_hi (16 columns) then P_lo (16 columns) -- and l / tile_l / m_ref are updated.  m_ref is an
-// integer (log2 units), so every rescale is an exact power of two.  Weights are allowed up to
-// 2^8 above the reference; a row whose keys outgrow that redoes the half with a raised
-// reference (reloading S, which is still intact), rescaling O, l and the first half's weights.
-template <bool BF16, int h>
-__device__ __forceinline__ void softmax_half(uint32_t (&r)[64], const uint32_t tS, const uint32_t tO,
-                                             const bool masked, const int kbase, const int lim, const float sc,
-                                             float& m_ref, float& l, float& tile_l) {
+// Online softmax for one 64-key S sub-tile (keys kbase .. kbase + 63) of this thread's row,
+// read from TMEM at tSb; the weights go back over the same columns -- for each 32-key piece,
+// P_hi (16 columns) then P_lo (16 columns) -- and l / m_ref are updated.  m_ref is an integer
+// (log2 units), so every rescale is an exact power of two.  Weights may reach 2^8 above the
+// reference; a sub-tile whose weights outgrow that is redone with a raised reference (S is
+// still intact), after O -- complete through the previous sub-tile's PV -- is rescaled.
+template <bool BF16>
+__device__ __forceinline__ void softmax_sub64(const uint32_t tSb, const uint32_t tO, const bool masked, const int kbase,
+                                              const int lim, const float sc, float& m_ref, float& l,
+                                              const uint32_t pv_done, const int u, unsigned* err) {
     using F = F16x2<BF16>;
     constexpr uint32_t kBits256 = BF16 ? 0x4380u : 0x5C00u;  // 2^8 as a packed 16-bit value
-    const uint32_t tcol = tS + 64 * h;
     // decided per warp: the branch holds warp-collective TMEM loads and stores
     bool redo = __any_sync(0xffffffffu, m_ref == -INFINITY);
 #pragma unroll 1
     for (int attempt = 0; attempt < 2; ++attempt) {
-        if (attempt == 1) {
-            tc::ld64(tcol, r);  // the weights pass overwrote r
-            tc::wait_ld();
-        }
+        uint32_t r[64];
+        tc::ld64(tSb, r);
+        tc::wait_ld();
         if (masked) {
 #pragma unroll
             for (int e = 0; e < 64; ++e)
-                if (kbase + 64 * h + e > lim) r[e] = __float_as_uint(-INFINITY);
+                if (kbase + e > lim) r[e] = __float_as_uint(-INFINITY);
         }
         if (redo) {
             float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
@@ -197,10 +206,11 @@ __device__ __forceinline__ void softmax_half(uint32_t (&r)[64], const uint32_t t
                 m_ref = mt;
             }
             l *= alpha;
-            tile_l *= alpha;
             if (__any_sync(0xffffffffu, alpha != 1.f)) {
-                // O is settled: this tile's S was issued after the previous PV and the S commit
-                // covers every earlier MMA of the issuing thread
+                // O must hold every PV before this sub-tile (and none after: its PV waits for
+                // these weights)
+                if (u > 0) (void)__all_sync(0xffffffffu, mbar_wait(pv_done, (u - 1) & 1, err));
+                tc::fence_after();
 #pragma unroll 1
                 for (int q = 0; q < 8; ++q) {
                     uint32_t o[16];
@@ -209,20 +219,6 @@ __device__ __forceinline__ void softmax_half(uint32_t (&r)[64], const uint32_t t
 #pragma unroll
                     for (int e = 0; e < 16; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
                     tc::st16(tO + 16 * q, o);
-                }
-                if (h == 1) {  // the weights already written for keys 0..63 of this tile
-#pragma unroll 1
-                    for (int q = 0; q < 4; ++q) {
-                        uint32_t w[16];
-                        tc::ld16(tS + 16 * q, w);
-                        tc::wait_ld();
-#pragma unroll
-                        for (int e = 0; e < 16; ++e) {
-                            const float2 u = F::unpack(w[e]);
-                            w[e] = F::pack_rn(u.x * alpha, u.y * alpha);
-                        }
-                        tc::st16(tS + 16 * q, w);
-                    }
                 }
             }
         }
@@ -244,14 +240,14 @@ __device__ __forceinline__ void softmax_half(uint32_t (&r)[64], const uint32_t t
         }
         const uint32_t pm = (pmax & 0xFFFFu) > (pmax >> 16) ? (pmax & 0xFFFFu) : (pmax >> 16);
         if (attempt == 0 && __any_sync(0xffffffffu, pm > kBits256)) {
-            redo = true;
+            redo = true;  // a row of this warp outgrew its reference by more than 2^8
             continue;
         }
-        tmem_store16_stride2(tcol + 0, r, 0);    // piece 2h:   P_hi
-        tmem_store16_stride2(tcol + 16, r, 1);   //             P_lo
-        tmem_store16_stride2(tcol + 32, r, 32);  // piece 2h+1: P_hi
-        tmem_store16_stride2(tcol + 48, r, 33);  //             P_lo
-        tile_l += ls.x + ls.y;
+        tmem_store16_stride2(tSb + 0, r, 0);    // keys  0..31: P_hi
+        tmem_store16_stride2(tSb + 16, r, 1);   //              P_lo
+        tmem_store16_stride2(tSb + 32, r, 32);  // keys 32..63: P_hi
+        tmem_store16_stride2(tSb + 48, r, 33);  //              P_lo
+        l += ls.x + ls.y;
         break;
     }
 }
@@ -289,27 +285,31 @@ prefill_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmK, c
     const int j0 = unit * NQT * TQ;
     if (j0 >= q_len) return;  // whole CTA: past the chunk
     const int ctx = kv_len - q_len;
-    int n_kt[NQT];            // key tiles each query tile needs (0: tile past the chunk)
+    int n_sub[NQT];           // 64-key S sub-tiles each query tile needs (0: tile past the chunk)
 #pragma unroll
     for (int t = 0; t < NQT; ++t) {
         const int jt = j0 + t * TQ;
-        n_kt[t] = (jt < q_len) ? (ctx + min(jt + TQ, q_len) + BN - 1) / BN : 0;
+        n_sub[t] = (jt < q_len) ? (ctx + min(jt + TQ, q_len) + BS - 1) / BS : 0;
     }
-    const int n_max = n_kt[NQT - 1] > n_kt[0] ? n_kt[NQT - 1] : n_kt[0];
+    const int nsub_max = n_sub[NQT - 1] > n_sub[0] ? n_sub[NQT - 1] : n_sub[0];
+    const int n_max = (nsub_max + 1) / 2;  // 128-key K/V stages to stream
     const int nblk_seq = (kv_len + 15) / 16;
 
     if (threadIdx.x == 0) {
         mbar_init(bars + 8 * Q_FULL, NQT * BM);
         for (int s = 0; s < 2; ++s) {
             mbar_init(bars + 8 * (K_FULL + s), 1);
-            mbar_init(bars + 8 * (K_EMPTY + s), 1);
             mbar_init(bars + 8 * (V_FULL + s), 1);
+            mbar_init(bars + 8 * (PV_DONE + s), 1);
+            mbar_init(bars + 8 * (DRAIN + s), 1);
+        }
+        for (int s = 0; s < 4; ++s) {  // index 2 t + b
+            mbar_init(bars + 8 * (K_EMPTY + s), 1);
             mbar_init(bars + 8 * (V_EMPTY + s), 1);
             mbar_init(bars + 8 * (S_FULL + s), 1);
             mbar_init(bars + 8 * (P_FULL + s), BM);
-            mbar_init(bars + 8 * (PV_DONE + s), 1);
         }
-        mbar_init(bars + 8 * DRAIN, 1);
+        mbar_init(bars + 8 * V_ZERO, 1);
         fence_barrier_init();
     }
     if (warp == MMA_WARP) {
@@ -335,7 +335,7 @@ prefill_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmK, c
         const bool row_valid = jr < q_len;
         const int lim = row_valid ? ctx + jr : -1;  // keys <= lim are visible
         const int lim_min = ctx + jt0;              // smallest limit among the tile's rows
-        const int nkt = (t == 0) ? n_kt[0] : n_kt[NQT - 1];
+        const int nsub = (t == 0) ? n_sub[0] : n_sub[NQT - 1];
         {
             const uint16_t* src = static_cast<const uint16_t*>(p.q) + ((size_t)(q0 + jr) * p.n_q_heads + hr) * D;
             const uint32_t qt = sQ + t * TILE;
@@ -348,30 +348,32 @@ prefill_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmK, c
             mbar_arrive(bars + 8 * Q_FULL);
         }
         const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
-        const uint32_t tS = tmem + lane_base + (uint32_t)(t * BN);
+        const uint32_t tS = tmem + lane_base + (uint32_t)(t * 128);
         const uint32_t tO = tmem + lane_base + O_COL + (uint32_t)(t * D);
         const float sc = p.qk_scale_log2;
         float m_ref = -INFINITY, l = 0.f;
         bool ok = true;
-        for (int i = 0; i < nkt; ++i) {
-            if (!__all_sync(0xffffffffu, mbar_wait(bars + 8 * (S_FULL + t), i & 1, p.err))) { ok = false; break; }
+        for (int u = 0; u < nsub; ++u) {
+            const int b = u & 1;
+            if (!__all_sync(0xffffffffu, mbar_wait(bars + 8 * (S_FULL + 2 * t + b), (u >> 1) & 1, p.err))) {
+                ok = false;
+                break;
+            }
             tc::fence_after();
-            const int kbase = i * BN;
-            const bool masked = kbase + BN - 1 > lim_min;
-            float tile_l = 0.f;
-            uint32_t ra[64], rb[64];
-            tc::ld64(tS, ra);
-            tc::ld64(tS + 64, rb);
-            tc::wait_ld();
-            softmax_half<BF16, 0>(ra, tS, tO, masked, kbase, lim, sc, m_ref, l, tile_l);
-            softmax_half<BF16, 1>(rb, tS, tO, masked, kbase, lim, sc, m_ref, l, tile_l);
-            l += tile_l;
+            const int kbase = u * BS;
+            softmax_sub64<BF16>(tS + (uint32_t)(b * BS), tO, kbase + BS - 1 > lim_min, kbase, lim, sc, m_ref, l,
+                                bars + 8 * (PV_DONE + t), u, p.err);
             tc::wait_st();
             tc::fence_before();
-            mbar_arrive(bars + 8 * (P_FULL + t));
+            mbar_arrive(bars + 8 * (P_FULL + 2 * t + b));
         }
-        // epilogue: O / l -> out
-        if (ok && nkt > 0 && __all_sync(0xffffffffu, mbar_wait(bars + 8 * (PV_DONE + t), (nkt - 1) & 1, p.err))) {
+        // epilogue: O / l -> out.  PV_DONE completes one phase per sub-tile, and with two S
+        // buffers the PVs of the last two sub-tiles may both be outstanding here (S of the last
+        // one only implies the PV two before it): wait for phase nsub - 2, then nsub - 1, so
+        // that no wait can be satisfied by a phase of the same parity two back.
+        if (ok && nsub > 1)
+            ok = __all_sync(0xffffffffu, mbar_wait(bars + 8 * (PV_DONE + t), (nsub - 2) & 1, p.err));
+        if (ok && nsub > 0 && __all_sync(0xffffffffu, mbar_wait(bars + 8 * (PV_DONE + t), (nsub - 1) & 1, p.err))) {
             tc::fence_after();
             const float inv = (l > 0.f) ? 1.f / l : 0.f;
             uint16_t* dst = static_cast<uint16_t*>(p.out) + ((size_t)(q0 + jr) * p.n_q_heads + hr) * D;
@@ -393,14 +395,19 @@ prefill_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmK, c
                 }
             }
         }
-    } else if (warp == TMA_WARP) {
-        // ------------------------------------------------------------ TMA producer warp
-        if (lane == 0) {
-            tma_prefetch_desc(&tmK);
-            tma_prefetch_desc(&tmV);
-        }
+    } else if (warp == TMA_WARP || warp == TMA_V_WARP) {
+        // ------------------------------------------------------------ TMA producers: K (warp
+        // TMA_WARP) and V (warp TMA_V_WARP) rings, issued by separate warps so that the two
+        // tiles' box loads are in flight together.  Stage i reuses the buffer of stage i - 2
+        // once every query tile that read stage i - 2 has released it (tile t reads stages
+        // 0 .. (n_sub[t] + 1) / 2 - 1).
+        const int kv = (warp == TMA_V_WARP) ? 1 : 0;
+        const CUtensorMap* map = kv ? &tmV : &tmK;
+        if (lane == 0) tma_prefetch_desc(map);
         const uint64_t pol = l2_policy_evict_last();
         const int32_t* bt = p.block_tables + (size_t)c * p.max_blocks_per_seq;
+        const uint32_t full0 = bars + 8 * (kv ? V_FULL : K_FULL), empty0 = bars + 8 * (kv ? V_EMPTY : K_EMPTY);
+        const uint32_t dst_base = kv ? sV : sK;
         bool ok = true;
         for (int i = 0; i < n_max && ok; ++i) {
             const int st = i & 1;
@@ -410,127 +417,128 @@ prefill_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmK, c
             if (lane < 8 && b < nblk_seq) {
                 my = __ldg(bt + b);
                 if (my < 0 || my >= p.num_blocks) {
-                    flag_error(p.err, PA_DEVERR_BLOCK);
+                    if (kv == 0) flag_error(p.err, PA_DEVERR_BLOCK);
                     my = p.num_blocks;
                 }
             }
+            if (lane == 0 && i >= 2) {
 #pragma unroll
-            for (int kv = 0; kv < 2; ++kv) {
-                const uint32_t full = bars + 8 * ((kv ? V_FULL : K_FULL) + st);
-                const uint32_t empty = bars + 8 * ((kv ? V_EMPTY : K_EMPTY) + st);
-                const uint32_t dst0 = (kv ? sV : sK) + st * TILE;
-                const CUtensorMap* map = kv ? &tmV : &tmK;
-                if (lane == 0 && i >= 2 && !mbar_wait(empty, ph ^ 1, p.err)) ok = false;
-                ok = __shfl_sync(0xffffffffu, ok, 0);
-                if (!ok) break;
-                if (lane == 0) mbar_arrive_expect_tx(full, TILE);
+                for (int t = 0; t < NQT; ++t)
+                    if (ok && 2 * (i - 2) < n_sub[t]) ok = mbar_wait(empty0 + 8 * (2 * t + st), ph ^ 1, p.err);
+            }
+            if (!__shfl_sync(0xffffffffu, ok, 0)) break;
+            const uint32_t full = full0 + 8 * st;
+            const uint32_t dst0 = dst_base + st * TILE;
+            if (lane == 0) mbar_arrive_expect_tx(full, TILE);
 #pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                    const int blk = __shfl_sync(0xffffffffu, my, j);
-                    if (lane == 0) {
-                        tma_load_4d(dst0 + j * 2048, map, 0, g, 0, blk, full, pol);
-                        tma_load_4d(dst0 + SLAB + j * 2048, map, 64, g, 0, blk, full, pol);
-                    }
+            for (int j = 0; j < 8; ++j) {
+                const int blk = __shfl_sync(0xffffffffu, my, j);
+                if (lane == 0) {
+                    tma_load_4d(dst0 + j * 2048, map, 0, g, 0, blk, full, pol);
+                    tma_load_4d(dst0 + SLAB + j * 2048, map, 64, g, 0, blk, full, pol);
                 }
             }
+            if (kv == 1 && i == n_max - 1) {
+                // Rows of the sequence's last, partial block past kv_len may hold anything (P
+                // is 0 there, but 0 * NaN is NaN): once the last V stage has landed, zero them,
+                // then release the stage to the MMA issuers through V_ZERO.
+                if (lane == 0) ok = mbar_wait(full, ph, p.err);
+                if (!__shfl_sync(0xffffffffu, ok, 0)) break;
+                const int z0 = max(kv_len, i * BN), z1 = min(((kv_len + 15) / 16) * 16, (i + 1) * BN);
+                for (int e = lane; e < 16 * max(z1 - z0, 0); e += 32) {
+                    const int row = z0 - i * BN + e / 16;
+                    sts128(dst0 + ((e / 8) & 1) * SLAB + row * 128 + (e & 7) * 16, make_uint4(0u, 0u, 0u, 0u));
+                }
+                tc::fence_async_smem();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bars + 8 * V_ZERO);
+            }
         }
-    } else if (warp == MMA_WARP && lane == 0) {
-        // ------------------------------------------------------------ MMA issue (one thread)
-        constexpr uint32_t ID_QK = tc::idesc_f16(BF16, false, BM, BN);
+    } else if ((warp == MMA_WARP || warp == MMA_WARP_1) && lane == 0 && (warp == MMA_WARP ? n_sub[0] : n_sub[1]) > 0) {
+        // ------------------------------------------------------------ MMA issue, one thread per
+        // query tile.  A wait on an mbarrier costs the issuing thread a few hundred cycles even
+        // when the phase is already complete, and the tensor pipe starves meanwhile; with one
+        // issuer per tile, one tile's MMAs go out while the other issuer waits.
+        const int t = (warp == MMA_WARP) ? 0 : 1;
+        const int nst = (t == 0) ? n_sub[0] : n_sub[1];
+        constexpr uint32_t ID_QK = tc::idesc_f16(BF16, false, BM, BS);
         constexpr uint32_t ID_PV = tc::idesc_f16(BF16, true, BM, D);
         // descriptors of the tile bases as (low, high) words; a K-step adds its byte offset >> 4
         // to the start-address field in the low word (addresses stay below 256 KB: no carry)
-        const uint64_t dq = tc::sdesc_sw128(sQ, 16, 1024), dk = tc::sdesc_sw128(sK, 16, 1024);
+        const uint64_t dq = tc::sdesc_sw128(sQ + t * TILE, 16, 1024), dk = tc::sdesc_sw128(sK, 16, 1024);
         const uint64_t dv = tc::sdesc_sw128(sV, SLAB, 1024);
         const uint32_t q_lo = (uint32_t)dq, q_hi = (uint32_t)(dq >> 32);
         const uint32_t k_lo = (uint32_t)dk, k_hi = (uint32_t)(dk >> 32);
         const uint32_t v_lo = (uint32_t)dv, v_hi = (uint32_t)(dv >> 32);
+        const uint32_t dS0 = tmem + (uint32_t)(t * 128), dO = tmem + O_COL + (uint32_t)(t * D);
         bool ok = mbar_wait(bars + 8 * Q_FULL, 0, p.err);
-        int k_ready = -1, v_ready = -1, issued = 0;
-        auto wait_k = [&](int jt) -> bool {
-            if (jt <= k_ready) return true;
-            if (!mbar_wait(bars + 8 * (K_FULL + (jt & 1)), (jt >> 1) & 1, p.err)) return false;
-            k_ready = jt;
+        int k_ready = -1, v_ready = -1;
+        bool issued = false;
+        auto wait_k = [&](int j) -> bool {
+            if (j <= k_ready) return true;
+            if (!mbar_wait(bars + 8 * (K_FULL + (j & 1)), (j >> 1) & 1, p.err)) return false;
+            k_ready = j;
             return true;
         };
-        auto wait_v = [&](int jt) -> bool {
-            if (jt <= v_ready) return true;
-            if (!mbar_wait(bars + 8 * (V_FULL + (jt & 1)), (jt >> 1) & 1, p.err)) return false;
-            v_ready = jt;
+        auto wait_v = [&](int j) -> bool {
+            if (j <= v_ready) return true;
+            // the last stage is handed over through V_ZERO once its stray rows are cleaned
+            const bool w = (j == n_max - 1) ? mbar_wait(bars + 8 * V_ZERO, 0, p.err)
+                                            : mbar_wait(bars + 8 * (V_FULL + (j & 1)), (j >> 1) & 1, p.err);
+            if (!w) return false;
+            v_ready = j;
             return true;
         };
-        auto issue_s = [&](int t, int jt) {
-            const uint32_t qa = q_lo + (uint32_t)((t * TILE) >> 4), ka = k_lo + (uint32_t)(((jt & 1) * TILE) >> 4);
-            const uint32_t dS = tmem + (uint32_t)(t * BN);
+        // S_t(v) = Q_t K^T for keys 64v .. 64v+63 (rows (v & 1) * 64 of stage v / 2), into buffer v & 1
+        auto issue_s = [&](int v) -> bool {
+            if (!wait_k(v >> 1)) return false;
+            tc::fence_after();
+            const uint32_t ka = k_lo + (uint32_t)((((v >> 1) & 1) * TILE + (v & 1) * (BS * 128)) >> 4);
+            const uint32_t dS = dS0 + (uint32_t)((v & 1) * BS);
 #pragma unroll
             for (int kk = 0; kk < D / 16; ++kk) {
                 const uint32_t off = (uint32_t)((((kk >> 2) * SLAB) + (kk & 3) * 32) >> 4);
-                tc::mma_f16_ss_w(dS, qa + off, q_hi, ka + off, k_hi, ID_QK, kk > 0);
+                tc::mma_f16_ss_w(dS, q_lo + off, q_hi, ka + off, k_hi, ID_QK, kk > 0);
             }
-            tc::commit(bars + 8 * (S_FULL + t));
-            ++issued;
+            tc::commit(bars + 8 * (S_FULL + 2 * t + (v & 1)));
+            issued = true;
+            return true;
         };
-        auto issue_pv = [&](int t, int jt) {
-            const uint32_t va = v_lo + (uint32_t)(((jt & 1) * TILE) >> 4);
-            const uint32_t pS = tmem + (uint32_t)(t * BN);
-            const uint32_t dO = tmem + O_COL + (uint32_t)(t * D);
+        // O_t += P_t(u) V for keys 64u .. 64u+63 (P_hi and P_lo from the S buffer u & 1)
+        auto issue_pv = [&](int u) -> bool {
+            if (!wait_v(u >> 1)) return false;
+            tc::fence_after();
+            const uint32_t va = v_lo + (uint32_t)((((u >> 1) & 1) * TILE + (u & 1) * (BS * 128)) >> 4);
+            const uint32_t pS = dS0 + (uint32_t)((u & 1) * BS);
 #pragma unroll
-            for (int kk = 0; kk < BN / 16; ++kk) {
-                // keys 16kk..16kk+15: P_hi at column 32(kk/2) + 8(kk%2) of S_t, P_lo 16 further
+            for (int kk = 0; kk < BS / 16; ++kk) {
+                // keys 16kk..16kk+15: P_hi at column 32(kk/2) + 8(kk%2) of the buffer, P_lo 16 further
                 const uint32_t pc = (uint32_t)(32 * (kk >> 1) + 8 * (kk & 1));
                 const uint32_t vb = va + (uint32_t)((kk * 2048) >> 4);
-                tc::mma_f16_ts_w(dO, pS + pc, vb, v_hi, ID_PV, (jt > 0 || kk > 0));
+                tc::mma_f16_ts_w(dO, pS + pc, vb, v_hi, ID_PV, (u > 0 || kk > 0));
                 tc::mma_f16_ts_w(dO, pS + pc + 16, vb, v_hi, ID_PV, 1u);
             }
             tc::commit(bars + 8 * (PV_DONE + t));
-            ++issued;
+            issued = true;
+            return true;
         };
-        if (ok) ok = wait_k(0);
-        if (ok) {
-            tc::fence_after();
-            if (n_kt[0] > 0) issue_s(0, 0);
-            if (n_kt[NQT - 1] > 0) issue_s(NQT - 1, 0);
-            tc::commit(bars + 8 * K_EMPTY);
-        }
-        for (int i = 0; i < n_max && ok; ++i) {
-            bool next_k = false;
-            if (i == n_max - 1) {
-                // rows of the sequence's last, partial block past kv_len may hold anything
-                // (P is 0 there, but 0 * NaN is NaN): zero them in the last V tile
-                ok = wait_v(i);
-                if (!ok) break;
-                const int z0 = max(kv_len, i * BN), z1 = min(((kv_len + 15) / 16) * 16, (i + 1) * BN);
-                for (int e = 0; e < 16 * max(z1 - z0, 0); ++e) {
-                    const int row = z0 - i * BN + e / 16;
-                    sts128(sV + (i & 1) * TILE + ((e / 8) & 1) * SLAB + row * 128 + (e & 7) * 16,
-                           make_uint4(0u, 0u, 0u, 0u));
-                }
-                tc::fence_async_smem();
-            }
-#pragma unroll
-            for (int t = 0; t < NQT && ok; ++t) {
-                const int nkt_t = (t == 0) ? n_kt[0] : n_kt[NQT - 1];
-                if (i >= nkt_t) continue;
-                ok = mbar_wait(bars + 8 * (P_FULL + t), i & 1, p.err) && wait_v(i);
-                if (!ok) break;
-                tc::fence_after();
-                issue_pv(t, i);
-                if (i + 1 < nkt_t) {
-                    ok = wait_k(i + 1);
-                    if (!ok) break;
-                    tc::fence_after();
-                    issue_s(t, i + 1);
-                    next_k = true;
-                }
-            }
+        // the last of this tile's sub-tiles that reads stage j
+        auto stage_last = [&](int j) { return min(2 * j + 1, nst - 1); };
+        // prologue: both S buffers
+        for (int v = 0; v < 2 && v < nst && ok; ++v) ok = issue_s(v);
+        if (ok) tc::commit(bars + 8 * (K_EMPTY + 2 * t));
+        for (int u = 0; u < nst && ok; ++u) {
+            ok = mbar_wait(bars + 8 * (P_FULL + 2 * t + (u & 1)), (u >> 1) & 1, p.err) && issue_pv(u);
+            if (ok && u + 2 < nst) ok = issue_s(u + 2);
             if (!ok) break;
-            tc::commit(bars + 8 * (V_EMPTY + (i & 1)));
-            if (next_k) tc::commit(bars + 8 * (K_EMPTY + ((i + 1) & 1)));
+            if (u == stage_last(u >> 1)) tc::commit(bars + 8 * (V_EMPTY + 2 * t + ((u >> 1) & 1)));
+            const int v = u + 2;
+            if (v < nst && v == stage_last(v >> 1)) tc::commit(bars + 8 * (K_EMPTY + 2 * t + ((v >> 1) & 1)));
         }
-        // every MMA issued must be complete before TMEM is released
-        if (issued > 0) {
-            tc::commit(bars + 8 * DRAIN);
-            (void)mbar_wait(bars + 8 * DRAIN, 0, p.err);
+        // every MMA this thread issued must be complete before TMEM is released
+        if (issued) {
+            tc::commit(bars + 8 * (DRAIN + t));
+            (void)mbar_wait(bars + 8 * (DRAIN + t), 0, p.err);
         }
     }
 
