@@ -367,13 +367,11 @@ prefill_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmK, c
             tc::fence_before();
             mbar_arrive(bars + 8 * (P_FULL + 2 * t + b));
         }
-        // epilogue: O / l -> out.  PV_DONE completes one phase per sub-tile, and with two S
-        // buffers the PVs of the last two sub-tiles may both be outstanding here (S of the last
-        // one only implies the PV two before it): wait for phase nsub - 2, then nsub - 1, so
-        // that no wait can be satisfied by a phase of the same parity two back.
-        if (ok && nsub > 1)
-            ok = __all_sync(0xffffffffu, mbar_wait(bars + 8 * (PV_DONE + t), (nsub - 2) & 1, p.err));
-        if (ok && nsub > 0 && __all_sync(0xffffffffu, mbar_wait(bars + 8 * (PV_DONE + t), (nsub - 1) & 1, p.err))) {
+        // epilogue: O / l -> out.  With two S buffers, PV_DONE may stand at any of three
+        // phases here (S of the last sub-tile only implies the PV two before it), which one
+        // parity bit cannot tell apart; DRAIN_t, committed once after this tile's last MMA,
+        // completes exactly one phase.
+        if (ok && nsub > 0 && __all_sync(0xffffffffu, mbar_wait(bars + 8 * (DRAIN + t), 0, p.err))) {
             tc::fence_after();
             const float inv = (l > 0.f) ? 1.f / l : 0.f;
             uint16_t* dst = static_cast<uint16_t*>(p.out) + ((size_t)(q0 + jr) * p.n_q_heads + hr) * D;
@@ -430,13 +428,12 @@ prefill_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmK, c
             const uint32_t full = full0 + 8 * st;
             const uint32_t dst0 = dst_base + st * TILE;
             if (lane == 0) mbar_arrive_expect_tx(full, TILE);
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                const int blk = __shfl_sync(0xffffffffu, my, j);
-                if (lane == 0) {
-                    tma_load_4d(dst0 + j * 2048, map, 0, g, 0, blk, full, pol);
-                    tma_load_4d(dst0 + SLAB + j * 2048, map, 64, g, 0, blk, full, pol);
-                }
+            __syncwarp();
+            {
+                // lanes 0..15 each issue one box: block lane % 8, 64-column slab lane / 8
+                const int blk = __shfl_sync(0xffffffffu, my, lane & 7);
+                const int sl = (lane >> 3) & 1;
+                if (lane < 16) tma_load_4d(dst0 + sl * SLAB + (lane & 7) * 2048, map, sl * 64, g, 0, blk, full, pol);
             }
             if (kv == 1 && i == n_max - 1) {
                 // Rows of the sequence's last, partial block past kv_len may hold anything (P
