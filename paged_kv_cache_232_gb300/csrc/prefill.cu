@@ -275,9 +275,11 @@ prefill_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmK, c
     const int rem = u_sel % per_unit;
     const int c = rem / p.n_kv_heads, g = rem % p.n_kv_heads;
 
-    const int q0 = __ldg(p.query_start_loc + c);
-    const int q_len = __ldg(p.query_start_loc + c + 1) - q0;
-    const int kv_len = __ldg(p.seq_lens + c);
+    // the CTA-order step left query_start_loc and seq_lens in shared memory
+    const int* sched = reinterpret_cast<const int*>(smem + SCHED_OFF);
+    const int q0 = p.lpt ? sched[c] : __ldg(p.query_start_loc + c);
+    const int q_len = (p.lpt ? sched[c + 1] : __ldg(p.query_start_loc + c + 1)) - q0;
+    const int kv_len = p.lpt ? sched[p.num_chunks + 1 + c] : __ldg(p.seq_lens + c);
     if (q_len < 0 || kv_len < q_len || kv_len > p.max_blocks_per_seq * 16) {
         if (unit == 0 && g == 0 && threadIdx.x == 0) flag_error(p.err, PA_DEVERR_LENGTH);
         return;
@@ -337,16 +339,30 @@ prefill_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmK, c
         const int lim_min = ctx + jt0;              // smallest limit among the tile's rows
         const int nsub = (t == 0) ? n_sub[0] : n_sub[NQT - 1];
         {
-            const uint16_t* src = static_cast<const uint16_t*>(p.q) + ((size_t)(q0 + jr) * p.n_q_heads + hr) * D;
+            // Q tile t: warp w of the group copies rows 32w .. 32w+31, two rows per instruction
+            // (lanes 0..15 one row, 16..31 the next: 512 contiguous bytes when G >= 2), each lane
+            // one 16-byte chunk into its 128-byte-swizzled place
             const uint32_t qt = sQ + t * TILE;
+            const int ch = lane & 15;
+            uint4 v[16];
 #pragma unroll
-            for (int ch = 0; ch < 16; ++ch) {
-                uint4 v = row_valid ? ldg_nc_128(src + ch * 8) : make_uint4(0u, 0u, 0u, 0u);
-                sts128(qt + (ch >> 3) * SLAB + swz128(r, ch & 7), v);
+            for (int i = 0; i < 16; ++i) {
+                const int R = (warp & 3) * 32 + 2 * i + (lane >> 4);
+                const int tok = jt0 + R / G;
+                const uint16_t* src =
+                    static_cast<const uint16_t*>(p.q) + ((size_t)(q0 + tok) * p.n_q_heads + g * G + R % G) * D + ch * 8;
+                v[i] = (tok < q_len) ? ldg_nc_128(src) : make_uint4(0u, 0u, 0u, 0u);
+            }
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                const int R = (warp & 3) * 32 + 2 * i + (lane >> 4);
+                sts128(qt + (ch >> 3) * SLAB + swz128(R, ch & 7), v[i]);
             }
             tc::fence_async_smem();
             mbar_arrive(bars + 8 * Q_FULL);
         }
+        // this row's output, formed before the loop so that only the pointer stays live across it
+        uint16_t* const dst = static_cast<uint16_t*>(p.out) + ((size_t)(q0 + jr) * p.n_q_heads + hr) * D;
         const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
         const uint32_t tS = tmem + lane_base + (uint32_t)(t * 128);
         const uint32_t tO = tmem + lane_base + O_COL + (uint32_t)(t * D);
@@ -374,7 +390,6 @@ prefill_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmK, c
         if (ok && nsub > 0 && __all_sync(0xffffffffu, mbar_wait(bars + 8 * (DRAIN + t), 0, p.err))) {
             tc::fence_after();
             const float inv = (l > 0.f) ? 1.f / l : 0.f;
-            uint16_t* dst = static_cast<uint16_t*>(p.out) + ((size_t)(q0 + jr) * p.n_q_heads + hr) * D;
 #pragma unroll 1
             for (int q = 0; q < 4; ++q) {
                 uint32_t o[32];

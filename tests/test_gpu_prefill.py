@@ -132,3 +132,26 @@ def test_prefill_out_of_pool_block_is_flagged_not_faulted():
     got = bits_of(out).reshape(w.prefill.q.shape)
     rows = np.arange(40, 70)                      # the second chunk does not touch the bad entry
     check(got[rows], oracle_rows(w, rows), wl.BF16, "good chunk")
+
+
+@pytest.mark.parametrize("cfg", ["mixed", "short"])
+def test_prefill_repeated_runs_bitwise_identical_and_no_device_errors(cfg):
+    """The kernel's pipeline has no data-dependent order of accumulation, so repeated runs
+    must agree bit for bit, and no barrier wait may ever reach its time limit (a wait that
+    mistook an earlier phase for the one it wanted would either time out -- raising
+    PA_DEVERR_TIMEOUT and leaving rows unwritten -- or read O early)."""
+    if cfg == "mixed":
+        w = wl.make_workload(5)
+    else:  # many short chunks: most CTAs finish within a few sub-tiles, where phases race most
+        w = wl.build_workload("pfr", 31, dtype=wl.BF16, n_q_heads=16, n_kv_heads=8, head_dim=128,
+                              prefill_q_lens=[1, 3, 64, 65, 127, 128, 129, 200, 256, 17, 90, 40],
+                              prefill_ctx_lens=[0, 1, 0, 63, 64, 1, 130, 5, 0, 300, 47, 2000], extra_blocks=3)
+    p, pre = w.pool, w.prefill
+    kc, vc, q = to_dev(p.k_cache, p.dtype), to_dev(p.v_cache, p.dtype), to_dev(pre.q, p.dtype)
+    pa.pa_device_errors(clear=True)
+    first = bits_of(run_prefill(w, kc=kc, vc=vc, q=q))
+    for _ in range(24):
+        out = torch.full_like(q, float("nan"))
+        again = bits_of(run_prefill(w, out=out, kc=kc, vc=vc, q=q))
+        assert np.array_equal(again, first)
+    assert pa.pa_device_errors(clear=True) == 0
