@@ -157,7 +157,39 @@ WORKLOADS = {
     "decode64": 2,
     "long4": 3,
     "mixed": 5,
+    "write64k": "write64k",   # bandwidth-scale KV write: 65,536 rows (10% padded) to random slots
 }
+
+
+def make_bench_workload(k, wl):
+    if k == "write64k":
+        return wl.write_rows_case(232_104, 65536)
+    return wl.make_workload(k)
+
+
+def workload_name(k, wl):
+    if k == "write64k":
+        return "bandwidth-scale KV write: 65,536 rows x 8 KV heads x 128 (bf16, 10% padded -1) to random slots"
+    return wl.WORKLOAD_NAMES[k]
+
+
+def sample_units(w):
+    """Units the oracle samples: sequences (their write rows + decode), or write rows."""
+    return w.decode.num_seqs if w.decode is not None else int(w.write.slot_mapping.size)
+
+
+def recorded_traffic(workload, kernel):
+    """DRAM bytes per launch of `kernel` on `workload` from the committed ncu record, or None
+    when there is none or the kernels have been rebuilt from other sources since."""
+    try:
+        with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
+            rec = json.load(f).get(f"{kernel}@{workload}")
+        from paged_kv_cache_232_gb300 import _build
+        if rec and rec.get("build_digest") == _build._digest():
+            return int(rec["dram_bytes_per_launch"])
+    except (OSError, ValueError, KeyError):
+        pass
+    return None
 
 
 # ----------------------------------------------------------------------------- our arm
@@ -198,7 +230,7 @@ def run_ours(args, rank, world, local_rank):
     dev = torch.device("cuda", local_rank)
     torch.cuda.set_device(dev)
     k = WORKLOADS[args.workload]
-    w = wl.make_workload(k)     # every rank gets its own copy of the same batch (weak scaling)
+    w = make_bench_workload(k, wl)   # every rank gets its own copy of the same batch (weak scaling)
     p, b, wr, pre = w.pool, w.decode, w.write, w.prefill
     dt = torch.bfloat16 if p.dtype == wl.BF16 else torch.float16
 
@@ -209,33 +241,40 @@ def run_ours(args, rank, world, local_rank):
         return torch.from_numpy(np.ascontiguousarray(a)).to(dev)
 
     kc, vc = dev_bits(p.k_cache), dev_bits(p.v_cache)
-    S, hq, D = b.q.shape
-    n_pre = pre.q.shape[0] if pre is not None else 0
-    q_host = np.concatenate([b.q, pre.q]) if pre is not None else b.q
-    q = dev_bits(q_host)                       # decode rows first, then prefill rows
-    out = torch.empty_like(q)
-    bt, cl = dev_int(b.block_tables), dev_int(b.context_lens)
-    maxL = int(b.context_lens.max())
-    ws = torch.empty(max(pa.pa_decode_workspace_size(S, hq, D, maxL, 0), 16), dtype=torch.uint8, device=dev)
-    which, part = pa.pa_decode_plan(S, p.n_kv_heads, maxL)
-    if args.decode_path == "v1":
-        which = 1
-    elif args.decode_path == "splitk":
-        which, part = 2, (args.partition or part)
     stages = []   # name, launch, algorithmic amount, kind
     if wr is not None:
         key, val, sm = dev_bits(wr.key), dev_bits(wr.value), dev_int(wr.slot_mapping)
         stages.append(("write", lambda: pa.pa_reshape_and_cache(key, val, kc, vc, sm), write_bytes(wr, p), "hbm"))
-    dec_logical = decode_bytes(b, p)
-    dec_unique = unique_decode_bytes(b, p)
-    if args.decode_path == "auto":
-        dec_fn = lambda: pa.pa_decode(out[:S], q[:S], kc, vc, bt, cl, maxL, b.scale, ws)
-    elif which == 1:
-        dec_fn = lambda: pa.pa_decode_v1(out[:S], q[:S], kc, vc, bt, cl, b.scale)
+    S, which, dec_logical = 0, 0, 0
+    if b is not None:
+        S, hq, D = b.q.shape
+        q_host = np.concatenate([b.q, pre.q]) if pre is not None else b.q
+        q = dev_bits(q_host)                       # decode rows first, then prefill rows
+        out = torch.empty_like(q)
+        bt, cl = dev_int(b.block_tables), dev_int(b.context_lens)
+        maxL = int(b.context_lens.max())
+        ws = torch.empty(max(pa.pa_decode_workspace_size(S, hq, D, maxL, 0), 16), dtype=torch.uint8, device=dev)
+        which, part = pa.pa_decode_plan(S, p.n_kv_heads, maxL)
+        if args.decode_path == "v1":
+            which = 1
+        elif args.decode_path == "splitk":
+            which, part = 2, (args.partition or part)
+        dec_logical = decode_bytes(b, p)
+        dec_unique = unique_decode_bytes(b, p)
+        if args.decode_path == "auto":
+            dec_fn = lambda: pa.pa_decode(out[:S], q[:S], kc, vc, bt, cl, maxL, b.scale, ws)
+        elif which == 1:
+            dec_fn = lambda: pa.pa_decode_v1(out[:S], q[:S], kc, vc, bt, cl, b.scale)
+        else:
+            ws = torch.empty(max(pa.pa_decode_workspace_size(S, hq, D, maxL, part), 16), dtype=torch.uint8,
+                             device=dev)
+            dec_fn = lambda: pa.pa_decode_splitk(out[:S], q[:S], kc, vc, bt, cl, maxL, b.scale, ws, part)
+        stages.append(("decode", dec_fn, dec_unique, "hbm"))
     else:
-        ws = torch.empty(max(pa.pa_decode_workspace_size(S, hq, D, maxL, part), 16), dtype=torch.uint8, device=dev)
-        dec_fn = lambda: pa.pa_decode_splitk(out[:S], q[:S], kc, vc, bt, cl, maxL, b.scale, ws, part)
-    stages.append(("decode", dec_fn, dec_unique, "hbm"))
+        # write only: the step's result lives in the cache; the end-to-end leg reads back the
+        # first written K row as its completion check
+        slot0 = int(wr.slot_mapping[wr.slot_mapping >= 0][0])
+        out = kc[slot0 // p.block_size, slot0 % p.block_size]
     if pre is not None:
         pbt, qsl, sl = dev_int(pre.block_tables), dev_int(pre.query_start_loc), dev_int(pre.seq_lens)
         stages.append(("prefill", lambda: pa.pa_prefill_chunk(out[S:], q[S:], kc, vc, pbt, qsl, sl, pre.max_q_len,
@@ -253,7 +292,8 @@ def run_ours(args, rank, world, local_rank):
         if ev:
             ev[ns].record(stream)
 
-    launches_per_step = (1 if wr is not None else 0) + (1 if which == 1 else 2) + (1 if pre is not None else 0)
+    launches_per_step = ((1 if wr is not None else 0) + (0 if b is None else (1 if which == 1 else 2))
+                         + (1 if pre is not None else 0))
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize()
@@ -287,7 +327,7 @@ def run_ours(args, rank, world, local_rank):
             breakdown[name] = {"us": round(float(ms) * 1e3, 2), "tflops": round(amount / (ms * 1e-3) / 1e12, 1),
                                "frac_bf16": round(amount / (ms * 1e-3) / 1e12 / peaks["bf16_tflops"], 4),
                                "flop": amount}
-    if pre is not None:
+    if pre is not None and b is not None:
         breakdown["decode"]["logical_gbs"] = round(dec_logical / (mean_ms[0] * 1e-3) / 1e9, 1)
     dom = int(np.argmax(mean_ms))
     dname, _, damount, dkind = stages[dom]
@@ -296,16 +336,18 @@ def run_ours(args, rank, world, local_rank):
         ach = damount / (dms * 1e-3) / 1e9
         roof = {"bound": "hbm", "kernel": f"{dname}", "achieved": round(ach, 1), "peak": peaks["hbm_gbs"],
                 "peak_source": peaks["source"], "unit": "GB/s", "frac": round(ach / peaks["hbm_gbs"], 4),
-                "traffic": args.traffic, "algorithmic_bytes": damount}
+                "traffic": args.traffic if args.traffic is not None else recorded_traffic(args.workload, dname),
+                "algorithmic_bytes": damount}
     else:
         ach = damount / (dms * 1e-3) / 1e12
         roof = {"bound": "tensor", "kernel": f"{dname}", "achieved": round(ach, 1), "peak": peaks["bf16_tflops"],
                 "peak_source": peaks["source"], "unit": "TFLOP/s", "frac": round(ach / peaks["bf16_tflops"], 4),
-                "traffic": args.traffic, "algorithmic_flops": damount}
+                "traffic": args.traffic if args.traffic is not None else recorded_traffic(args.workload, dname),
+                "algorithmic_flops": damount}
 
     # end to end through the C ABI with host buffers: inputs up, result down, every step
     pin = lambda t: t.cpu().pin_memory()
-    h_in = [(q, pin(q)), (bt, pin(bt)), (cl, pin(cl))]
+    h_in = [(q, pin(q)), (bt, pin(bt)), (cl, pin(cl))] if b is not None else []
     if wr is not None:
         h_in += [(key, pin(key)), (val, pin(val)), (sm, pin(sm))]
     if pre is not None:
@@ -333,18 +375,18 @@ def run_ours(args, rank, world, local_rank):
     torch.cuda.synchronize()
     e2e_ms = max_over_ranks(float(np.mean([a.elapsed_time(c) for a, c in e2e_ev])), world)
 
-    cfg = {
-        "workload": wl.WORKLOAD_NAMES[k],
-        "num_seqs": int(S), "n_q_heads": int(hq), "n_kv_heads": p.n_kv_heads, "head_dim": p.head_dim,
-        "block_size": p.block_size, "total_context_tokens": int(b.context_lens.sum()),
-        "decode_path": ("one-pass" if which == 1 else f"split-K/{part}") + ("" if args.decode_path == "auto" else " (forced)"),
-        "l2": "512 MiB memset between timed steps (outside the events)",
-        "parallelism": f"replicas x{world} (independent batches, no collective)",
-    }
+    cfg = {"workload": workload_name(k, wl), "n_kv_heads": p.n_kv_heads, "head_dim": p.head_dim,
+           "block_size": p.block_size}
+    if b is not None:
+        cfg.update({"num_seqs": int(S), "n_q_heads": int(hq), "total_context_tokens": int(b.context_lens.sum()),
+                    "decode_path": ("one-pass" if which == 1 else f"split-K/{part}")
+                    + ("" if args.decode_path == "auto" else " (forced)")})
+    cfg.update({"l2": "512 MiB memset between timed steps (outside the events)",
+                "parallelism": f"replicas x{world} (independent batches, no collective)"})
     if wr is not None:
         cfg.update(write_rows=int(wr.slot_mapping.size), padded_rows=int((wr.slot_mapping < 0).sum()))
     if pre is not None:
-        cfg.update(prefill_chunks=pre.num_chunks, prefill_rows=int(n_pre),
+        cfg.update(prefill_chunks=pre.num_chunks, prefill_rows=int(pre.q.shape[0]),
                    prefill_kv_lens=[int(x) for x in pre.seq_lens])
     res = {
         "metric": "paged decode attn us/step & achieved HBM GB/s (% of GB300 peak); KV-write GB/s",
@@ -387,7 +429,8 @@ def run_ours(args, rank, world, local_rank):
 
 def oracle_sample_step(w, n_seqs):
     """One bounded step of the oracle: the write of the sample's rows, then decode of the
-    first n_seqs sequences.  Returns (bytes, seconds)."""
+    first n_seqs sequences (a write-only workload: the write of its first n_seqs rows).
+    Returns (bytes, seconds)."""
     import oracle
     p, b, wr = w.pool, w.decode, w.write
     t0 = time.perf_counter()
@@ -399,6 +442,8 @@ def oracle_sample_step(w, n_seqs):
                                               wr.slot_mapping[sl], p.block_size)
         valid = int((wr.slot_mapping[sl] >= 0).sum())
         nbytes_done += 2 * valid * p.n_kv_heads * p.head_dim * 2 * 2 + 8 * n_seqs
+    if b is None:
+        return nbytes_done, time.perf_counter() - t0
     out = oracle.decode(b.q[:n_seqs], k_cache, v_cache, b.block_tables[:n_seqs], b.context_lens[:n_seqs], b.scale,
                         p.dtype)
     dt = time.perf_counter() - t0
@@ -411,7 +456,7 @@ def oracle_sample_step(w, n_seqs):
 def _sample_size(w, budget_s):
     n = 1
     nb, dt = oracle_sample_step(w, n)
-    S = w.decode.num_seqs
+    S = sample_units(w)
     while dt < budget_s / 4 and n < S:
         n = min(S, n * 2)
         nb, dt = oracle_sample_step(w, n)
@@ -430,7 +475,8 @@ def cpu_baseline(w, k, budget_s=10.0):
         tot += b_
     el = time.perf_counter() - t0
     return {"value": round(tot / el / 1e9, 4), "unit": "GB/s", "cores": oracle.num_threads(), "kind": "oracle",
-            "sample": f"{n} of {w.decode.num_seqs} sequences (their write rows + decode), {reps} reps, {el:.1f} s"}
+            "sample": (f"{n} of {w.decode.num_seqs} sequences (their write rows + decode)" if w.decode is not None
+                       else f"{n} of {sample_units(w)} write rows") + f", {reps} reps, {el:.1f} s"}
 
 
 def run_reference(args, rank, world):
@@ -439,7 +485,7 @@ def run_reference(args, rank, world):
     if rank != 0:
         return None
     k = WORKLOADS[args.workload]
-    w = wl.make_workload(k)
+    w = make_bench_workload(k, wl)
     n, _, dt = _sample_size(w, budget_s=min(5.0, args.cpu_seconds))
     for _ in range(args.warmup):
         oracle_sample_step(w, n)
@@ -449,16 +495,17 @@ def run_reference(args, rank, world):
         tot += b_
         el += t_
     value = tot / el / 1e9
-    p, b = w.pool, w.decode
+    units = sample_units(w)
+    what = "sequences" if w.decode is not None else "write rows"
     return {
         "impl": "reference",
         "metric": "paged decode attn us/step & achieved HBM GB/s (% of GB300 peak); KV-write GB/s",
         "value": round(value, 4), "unit": "GB/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(el / args.steps * 1e3, 3), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic (same seeded workload)",
-        "config": {"workload": wl.WORKLOAD_NAMES[k], "num_seqs": int(b.num_seqs), "sampled_seqs": n},
+        "config": {"workload": workload_name(k, wl), f"num_{what.replace(' ', '_')}": units, "sampled": n},
         "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": oracle.num_threads(), "kind": "oracle",
-                         "sample": f"{n} of {b.num_seqs} sequences per step"},
+                         "sample": f"{n} of {units} {what} per step"},
         "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
 

@@ -161,6 +161,16 @@ __device__ __forceinline__ int lpt_unit(const PrefillParams& p, unsigned char* s
     return chosen;
 }
 
+// The whole warp waits for a phase through lane 0 alone (fewer shared-memory polls next to the
+// tensor core's operand reads); __syncwarp orders the other lanes after lane 0's acquire.
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, unsigned* err) {
+    bool ok = true;
+    if ((threadIdx.x & 31) == 0) ok = mbar_wait(bar, parity, err);
+    ok = __shfl_sync(0xffffffffu, ok, 0);
+    __syncwarp();
+    return ok;
+}
+
 // Words src[from], src[from + 2], ..., src[from + 30] into 16 TMEM columns at taddr.
 __device__ __forceinline__ void tmem_store16_stride2(uint32_t taddr, const uint32_t (&src)[64], int from) {
     uint32_t v[16];
@@ -209,7 +219,7 @@ __device__ __forceinline__ void softmax_sub64(const uint32_t tSb, const uint32_t
             if (__any_sync(0xffffffffu, alpha != 1.f)) {
                 // O must hold every PV before this sub-tile (and none after: its PV waits for
                 // these weights)
-                if (u > 0) (void)__all_sync(0xffffffffu, mbar_wait(pv_done, (u - 1) & 1, err));
+                if (u > 0) (void)warp_wait(pv_done, (u - 1) & 1, err);
                 tc::fence_after();
 #pragma unroll 1
                 for (int q = 0; q < 8; ++q) {
@@ -309,7 +319,7 @@ prefill_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmK, c
             mbar_init(bars + 8 * (K_EMPTY + s), 1);
             mbar_init(bars + 8 * (V_EMPTY + s), 1);
             mbar_init(bars + 8 * (S_FULL + s), 1);
-            mbar_init(bars + 8 * (P_FULL + s), BM);
+            mbar_init(bars + 8 * (P_FULL + s), 4);  // one arrival per softmax warp
         }
         mbar_init(bars + 8 * V_ZERO, 1);
         fence_barrier_init();
@@ -371,7 +381,7 @@ prefill_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmK, c
         bool ok = true;
         for (int u = 0; u < nsub; ++u) {
             const int b = u & 1;
-            if (!__all_sync(0xffffffffu, mbar_wait(bars + 8 * (S_FULL + 2 * t + b), (u >> 1) & 1, p.err))) {
+            if (!warp_wait(bars + 8 * (S_FULL + 2 * t + b), (u >> 1) & 1, p.err)) {
                 ok = false;
                 break;
             }
@@ -381,13 +391,14 @@ prefill_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmK, c
                                 bars + 8 * (PV_DONE + t), u, p.err);
             tc::wait_st();
             tc::fence_before();
-            mbar_arrive(bars + 8 * (P_FULL + 2 * t + b));
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bars + 8 * (P_FULL + 2 * t + b));
         }
         // epilogue: O / l -> out.  With two S buffers, PV_DONE may stand at any of three
         // phases here (S of the last sub-tile only implies the PV two before it), which one
         // parity bit cannot tell apart; DRAIN_t, committed once after this tile's last MMA,
         // completes exactly one phase.
-        if (ok && nsub > 0 && __all_sync(0xffffffffu, mbar_wait(bars + 8 * (DRAIN + t), 0, p.err))) {
+        if (ok && nsub > 0 && warp_wait(bars + 8 * (DRAIN + t), 0, p.err)) {
             tc::fence_after();
             const float inv = (l > 0.f) ? 1.f / l : 0.f;
 #pragma unroll 1
