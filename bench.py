@@ -375,6 +375,28 @@ def run_ours(args, rank, world, local_rank):
     torch.cuda.synchronize()
     e2e_ms = max_over_ranks(float(np.mean([a.elapsed_time(c) for a, c in e2e_ev])), world)
 
+    # the same step captured once into a CUDA graph and replayed (launch overhead removed)
+    graph_ms = None
+    try:
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            for st in stages:
+                st[1]()
+        for _ in range(3):
+            g.replay()
+        torch.cuda.synchronize()
+        g_ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
+        for i in range(args.steps):
+            flush.zero_()
+            g_ev[i][0].record(stream)
+            g.replay()
+            g_ev[i][1].record(stream)
+        torch.cuda.synchronize()
+        graph_ms = max_over_ranks(float(np.mean([a.elapsed_time(c) for a, c in g_ev])), world)
+        assert pa.pa_device_errors(clear=True) == 0
+    except RuntimeError as ex:   # capture refused: report it instead of a number
+        graph_ms = f"capture failed: {str(ex).splitlines()[0][:120]}"
+
     cfg = {"workload": workload_name(k, wl), "n_kv_heads": p.n_kv_heads, "head_dim": p.head_dim,
            "block_size": p.block_size}
     if b is not None:
@@ -413,6 +435,9 @@ def run_ours(args, rank, world, local_rank):
             "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h,
         },
+        "graph": ({"us_per_step": round(graph_ms * 1e3, 2), "value": round(world * step_bytes / (graph_ms * 1e-3) / 1e9, 2),
+                   "unit": "GB/s", "note": "the step's launches captured once into a CUDA graph, replayed per step"}
+                  if isinstance(graph_ms, float) else {"unavailable": graph_ms}),
         "gpu_launches": launches_per_step * args.steps,
         "wall_s_timed_region": round(t_wall, 4),
     }

@@ -8,15 +8,19 @@ static cudaError_t launch_decode_t(const DecodeParams& p, const CUtensorMap& tmK
                                    bool with_reduce, cudaStream_t st) {
     using C = DecodeCfg<D, G, BF16>;
     auto kern = decode_kernel<D, G, BF16>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+    static std::atomic<unsigned long long> s_done{0};
+    cudaError_t e = smem_limit_once(reinterpret_cast<const void*>(kern), C::SMEM_BYTES, s_done);
     if (e != cudaSuccess) return e;
     kern<<<grid, C::THREADS, C::SMEM_BYTES, st>>>(p, tmK, tmV);
     e = cudaGetLastError();
     if (e != cudaSuccess || !with_reduce) return e;
     const size_t red_smem = (size_t)(((p.max_parts + 3) & ~3) + 8 * D) * sizeof(float);
     auto rk = splitk_reduce_kernel<D, BF16>;
+    if (red_smem > 227 * 1024) return cudaErrorInvalidValue;
     if (red_smem > 48 * 1024) {
-        e = cudaFuncSetAttribute(rk, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)red_smem);
+        // set once to the per-CTA maximum, so that no later (larger) piece count needs it again
+        static std::atomic<unsigned long long> s_red_done{0};
+        e = smem_limit_once(reinterpret_cast<const void*>(rk), 227 * 1024, s_red_done);
         if (e != cudaSuccess) return e;
     }
     rk<<<p.num_seqs * p.n_q_heads, 256, red_smem, st>>>(p);

@@ -2,12 +2,29 @@
 // that instantiate the kernels.  Internal to libpagedattn.
 #pragma once
 
+#include <atomic>
 #include <cuda.h>
 #include <cuda_runtime.h>
 
 #include "decode.cuh"
 
 namespace pa {
+
+// Raise a kernel's dynamic shared-memory limit once per device: the attribute persists, and
+// not touching it again keeps the launch path free of host calls other than the launch itself
+// (what a CUDA-graph capture of a decode or prefill step needs).  `done` is one bit per device,
+// owned by the launcher of that kernel instantiation.
+inline cudaError_t smem_limit_once(const void* func, int bytes, std::atomic<unsigned long long>& done) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    const unsigned long long bit = 1ull << (dev & 63);
+    if (done.load(std::memory_order_acquire) & bit) return cudaSuccess;
+    e = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e == cudaSuccess) done.fetch_or(bit, std::memory_order_acq_rel);
+    return e;
+}
+
 
 // Launch the decode piece kernel for (dtype, head_dim, group) on `grid` CTAs; when
 // params.part_tokens > 0 and any sequence has more than one piece, also launch the reduce.

@@ -577,7 +577,8 @@ template <int G, bool BF16>
 static cudaError_t launch_prefill_t(const PrefillParams& p, const CUtensorMap& tmK, const CUtensorMap& tmV,
                                     cudaStream_t st) {
     auto kern = prefill_kernel<G, BF16>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, pf::SMEM_BYTES);
+    static std::atomic<unsigned long long> s_done{0};
+    cudaError_t e = smem_limit_once(reinterpret_cast<const void*>(kern), pf::SMEM_BYTES, s_done);
     if (e != cudaSuccess) return e;
     // one CTA per pair of 128-row query tiles of a (chunk, KV head)
     const int units = (p.tiles_per_chunk + pf::NQT - 1) / pf::NQT;
