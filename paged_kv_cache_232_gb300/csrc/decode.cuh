@@ -70,6 +70,10 @@ struct DecodeCfg {
     static constexpr int BAR_OFF = RING_BYTES + P_BYTES + A_BYTES;
     static constexpr int SMEM_BYTES = BAR_OFF + 2 * NST * 8 + 1024;  // + alignment slack
     static_assert(MERGE_BYTES <= RING_BYTES, "merge area must fit in the ring");
+    // Consumer warp w takes blocks b = w, w + NCW, ...; with NST a multiple of NCW every ring stage
+    // belongs to one warp, which waits on its phases in order -- a stage's full barrier is then
+    // never two phases behind the phase its warp waits for (where the parity test would pass early).
+    static_assert(NST % NCW == 0, "ring stages must be a multiple of the consumer warps");
     static_assert(D == 64 || D == 128, "head_dim 64 or 128");
     static_assert(G == 1 || G == 2 || G == 4 || G == 8, "group size 1, 2, 4 or 8");
 };
@@ -180,6 +184,7 @@ decode_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmK, con
         const uint64_t pol = l2_policy_evict_first();
         const int32_t* bt = p.block_tables + (size_t)s * p.max_blocks_per_seq + blk0;
         bool ok = true;
+        int n_issued = 0;  // blocks whose loads were issued
         for (int b0 = 0; b0 < nblk && ok; b0 += 32) {
             int my = 0;
             if (b0 + lane < nblk) {
@@ -211,8 +216,21 @@ decode_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmK, con
                 }
                 ok = __shfl_sync(0xffffffffu, ok, 0);
                 if (!ok) break;
+                n_issued = b + 1;
             }
         }
+        // No load may still be landing when the consumers reuse the ring for their merge or the
+        // CTA exits (after a time-out the consumers may not have taken every stage): wait, with
+        // the time limit, for the last phase of every stage that was filled, then release the
+        // consumers' merge barrier.  Each of those phases is the one just issued or already done.
+        if (lane == 0) {
+            for (int st = 0; st < C::NST && st < n_issued; ++st) {
+                const int b_last = st + ((n_issued - 1 - st) / C::NST) * C::NST;
+                (void)mbar_wait(bar_full + 8 * st, (b_last / C::NST) & 1, p.err);
+            }
+        }
+        __syncwarp();
+        asm volatile("bar.arrive 2, %0;" ::"n"(C::THREADS) : "memory");
         return;
     }
 
@@ -366,8 +384,9 @@ decode_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmK, con
         }
 
     // ---------------------------------------------------------------- merge the 4 warps
-    // all consumer warps have drained the ring; reuse it as the merge area
-    asm volatile("bar.sync 1, %0;" ::"n"(C::NCW * 32) : "memory");
+    // the consumer warps are done with the ring and the producer has seen every load land
+    // (barrier 2 counts the producer warp too); reuse the ring as the merge area
+    asm volatile("bar.sync 2, %0;" ::"n"(C::THREADS) : "memory");
     float* mo = reinterpret_cast<float*>(smem);            // [NCW][G][D]
     float* mm = mo + C::NCW * G * D;                        // [NCW][G]
     float* ml = mm + C::NCW * G;                            // [NCW][G]
