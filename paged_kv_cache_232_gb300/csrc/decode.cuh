@@ -146,8 +146,12 @@ decode_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmK, con
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int units = p.num_seqs * p.n_kv_heads;
-    const int piece = blockIdx.x / units;
-    const int sg = blockIdx.x - piece * units;
+    // split-K: the grid runs the highest piece index first -- only long contexts have one -- so the
+    // extra pieces of long sequences start at once and the short, whole-sequence pieces fill in
+    // behind them (longest-first without knowing the lengths on the host)
+    const int qpos = (int)(blockIdx.x / units);
+    const int piece = (p.max_parts - 1) - qpos;
+    const int sg = (int)blockIdx.x - qpos * units;
     const int s = sg / p.n_kv_heads, g = sg - s * p.n_kv_heads;
 
     // context length, clamped to what the table (and the split-K grid) can address
