@@ -74,6 +74,9 @@ def lib():
         L.pao_round_array.argtypes = [vp, i64, i32, vp]
         L.pao_widen_array.argtypes = [vp, i64, i32, vp]
         L.pao_kv_write.argtypes = [vp, vp, vp, vp, vp, i64, i32, i32, i32, i64]
+        L.pao_rope_exact.argtypes = [vp, vp, i32, dbl, dbl]
+        L.pao_rope_exact.restype = None
+        L.pao_rope_kv_write.argtypes = [vp, vp, vp, vp, vp, vp, vp, i64, i32, i32, i32, i32, i64, i64, dbl, i32]
         L.pao_kv_write.restype = i32
         dec = [vp, vp, vp, vp, vp, vp, i32, vp, i32, i32, i32, i32, i32, i64, dbl, i32]
         L.pao_decode.argtypes = dec
@@ -133,6 +136,37 @@ def kv_write(k_cache, v_cache, key, value, slot_mapping, block_size: int, check:
     if check:
         _check(st, "kv_write")
     return k, v, st
+
+
+def rope_exact(x, m: float, theta: float) -> np.ndarray:
+    """Rotary embedding of one double row x (head_dim even) at position m, unrounded."""
+    x = np.ascontiguousarray(np.asarray(x, dtype=np.float64))
+    out = np.empty_like(x)
+    lib().pao_rope_exact(x.ctypes.data, out.ctypes.data, x.size, float(m), float(theta))
+    return out
+
+
+def rope_kv_write(q, k_cache, v_cache, key, value, slot_mapping, positions, max_position: int, theta: float,
+                  dtype: int, check: bool = True):
+    """Fused rotary embedding + KV write.  Returns (q rotated or None, k_cache, v_cache, status),
+    all new arrays; the inputs are not modified."""
+    qq = None
+    qptr = None
+    if q is not None:
+        qq, qptr = _c(np.array(q, copy=True), np.uint16)
+    k, kp = _c(np.array(k_cache, copy=True), np.uint16)
+    v, vp_ = _c(np.array(v_cache, copy=True), np.uint16)
+    key, keyp = _c(key, np.uint16)
+    val, valp = _c(value, np.uint16)
+    sm, smp = _c(slot_mapping, np.int64)
+    pos, posp = _c(positions, np.int64)
+    nb, bs, hkv, d = k.shape
+    hq = qq.shape[1] if qq is not None else 0
+    st = lib().pao_rope_kv_write(qptr, kp, vp_, keyp, valp, smp, posp, sm.size, hq, hkv, d, bs, nb,
+                                 int(max_position), float(theta), int(dtype))
+    if check:
+        _check(st, "rope_kv_write")
+    return qq, k, v, st
 
 
 def decode(q, k_cache, v_cache, block_tables, context_lens, scale: float, dtype: int, want_weights=False):

@@ -28,6 +28,9 @@
  *  - Prefill chunk (mini_engine paged prefill; miniserve "Engine", bottom-right
  *    causal mask): query row j of a chunk of q_len rows whose kv length is
  *    kv_len sees keys t <= (kv_len - q_len) + j.
+ *  - Rotary position embedding fused into the KV write (mini_engine, "Roadmap":
+ *    fused RoPE folded into the KV-cache write; "Features": Qwen3 with RoPE): the
+ *    textbook rotation of each dimension pair (i, i + head_dim/2) by m * f_i.
  *  - Materialise-then-attend (MiniLLM Runtime, "Key benchmark results"): copy the
  *    sequence's K/V into contiguous arrays first, then run the same textbook
  *    attention; used only as an invariant (paged == contiguous).
@@ -154,6 +157,74 @@ int pao_kv_write(uint16_t* k_cache, uint16_t* v_cache, const uint16_t* key, cons
                 k_cache[dst] = key[src];
                 v_cache[dst] = value[src];
             }
+    }
+    return status;
+}
+
+/* ---- rotary position embedding (fused into the KV write) ------------------ */
+
+/*
+ * Rotary position embedding (mini_engine, "Features": the Qwen3 decoder uses RoPE;
+ * "Roadmap": fused RoPE folded into the KV-cache write).  The textbook rotation, in the
+ * rotate-half pairing: with half = head_dim / 2 and f_i = theta^(-2 i / head_dim), a row x of
+ * a token at position m becomes, for i < half,
+ *     x'[i]        = x[i] cos(m f_i) - x[i + half] sin(m f_i)
+ *     x'[i + half] = x[i + half] cos(m f_i) + x[i] sin(m f_i).
+ * pao_rope_exact rotates doubles (no rounding; for the invariants); pao_rope_kv_write works on
+ * 16-bit rows and rounds each result once, to nearest even.
+ */
+void pao_rope_exact(const double* x, double* out, int head_dim, double m, double theta) {
+    const int half = head_dim / 2;
+    for (int i = 0; i < half; ++i) {
+        const double f = pow(theta, -2.0 * (double)i / (double)head_dim);
+        const double c = cos(m * f), sn = sin(m * f);
+        const double x0 = x[i], x1 = x[i + half];
+        out[i] = x0 * c - x1 * sn;
+        out[i + half] = x1 * c + x0 * sn;
+    }
+}
+
+static void pao_rope_bits(const uint16_t* x, uint16_t* out, int head_dim, int64_t m, double theta, int dtype) {
+    double in[PAO_MAX_HEAD_DIM], rot[PAO_MAX_HEAD_DIM];
+    for (int e = 0; e < head_dim; ++e) in[e] = pao_to_double(x[e], dtype);
+    pao_rope_exact(in, rot, head_dim, (double)m, theta);
+    for (int e = 0; e < head_dim; ++e) out[e] = pao_from_double(rot[e], dtype);
+}
+
+/*
+ * Fused rotary embedding + KV write.  For each row i with positions[i] in [0, max_position):
+ * every head of q (when q is not NULL, [num_tokens, n_q_heads, head_dim]) is rotated in place;
+ * if slot_mapping[i] != -1 the rotated key row goes to k_cache and the value row to v_cache at
+ * that slot, exactly as pao_kv_write places rows.  A row whose position is out of range is
+ * left untouched (status PAO_EBOUNDS); a slot outside the pool drops the row's write (same).
+ */
+int pao_rope_kv_write(uint16_t* q, uint16_t* k_cache, uint16_t* v_cache, const uint16_t* key,
+                      const uint16_t* value, const int64_t* slot_mapping, const int64_t* positions,
+                      int64_t num_tokens, int n_q_heads, int n_kv_heads, int head_dim, int block_size,
+                      int64_t num_blocks, int64_t max_position, double theta, int dtype) {
+    if (head_dim <= 0 || head_dim > PAO_MAX_HEAD_DIM || head_dim % 2) return PAO_EARG;
+    int status = PAO_OK;
+    uint16_t rot[PAO_MAX_HEAD_DIM];
+    for (int64_t i = 0; i < num_tokens; ++i) {
+        const int64_t m = positions[i];
+        if (m < 0 || m >= max_position) { status = PAO_EBOUNDS; continue; }
+        if (q) {
+            for (int h = 0; h < n_q_heads; ++h) {
+                uint16_t* row = q + (i * n_q_heads + h) * head_dim;
+                pao_rope_bits(row, rot, head_dim, m, theta, dtype);
+                memcpy(row, rot, (size_t)head_dim * sizeof(uint16_t));
+            }
+        }
+        const int64_t slot = slot_mapping[i];
+        if (slot == -1) continue;
+        if (slot < 0 || slot >= num_blocks * block_size) { status = PAO_EBOUNDS; continue; }
+        const int64_t block = slot / block_size, offset = slot % block_size;
+        for (int h = 0; h < n_kv_heads; ++h) {
+            const int64_t dst = ((block * block_size + offset) * n_kv_heads + h) * head_dim;
+            const int64_t src = (i * n_kv_heads + h) * head_dim;
+            pao_rope_bits(key + src, k_cache + dst, head_dim, m, theta, dtype);
+            for (int d = 0; d < head_dim; ++d) v_cache[dst + d] = value[src + d];
+        }
     }
     return status;
 }

@@ -348,3 +348,85 @@ def test_prefill_row_is_a_decode_row_with_shorter_context():
     v0 = f64(p.v_cache[pre.block_tables[1, 0], 0], BF16)
     for h in range(4):
         assert np.array_equal(got[9, h], v0[h // 2])
+
+
+# ------------------------------------------------------------------ rotary embedding (fused RoPE + KV write)
+# Pins for the textbook rotation the oracle's fused write uses: each (i, i + D/2) pair turned
+# by m * theta^(-2i/D).  Every pin is independent of the oracle's own formula.
+
+
+def test_rope_one_pair_is_complex_multiplication():
+    """D = 2, one pair, f_0 = 1: x0 + i x1 times e^{i m} (Python's complex arithmetic)."""
+    import cmath
+    for m in [0.0, 1.0, 2.5, 100.0, 12345.0]:
+        for x0, x1 in [(1.0, 0.0), (0.3, -1.7), (-2.0, 0.5)]:
+            z = complex(x0, x1) * cmath.exp(1j * m)
+            got = oracle.rope_exact([x0, x1], m, 10000.0)
+            assert abs(got[0] - z.real) < 1e-12 and abs(got[1] - z.imag) < 1e-12
+
+
+def test_rope_pairing_frequencies_and_norm():
+    """e_i moves only within the pair (i, i + D/2), by the angle m * theta^(-2i/D) (recovered with
+    atan2), and every pair keeps its length."""
+    D, theta, m = 128, 1.0e6, 37.0
+    for i in [0, 1, 5, 31, 63]:
+        x = np.zeros(D)
+        x[i] = 1.0
+        y = oracle.rope_exact(x, m, theta)
+        nz = set(np.nonzero(np.abs(y) > 1e-15)[0].tolist())
+        assert nz <= {i, i + D // 2}
+        ang = math.atan2(y[i + D // 2], y[i])
+        want = math.remainder(m * theta ** (-2.0 * i / D), 2 * math.pi)
+        assert abs(math.remainder(ang - want, 2 * math.pi)) < 1e-9
+    rng = np.random.default_rng(3)
+    x = rng.standard_normal(D)
+    y = oracle.rope_exact(x, 1234.0, theta)
+    h = D // 2
+    assert np.allclose(x[:h] ** 2 + x[h:] ** 2, y[:h] ** 2 + y[h:] ** 2, rtol=1e-12, atol=1e-12)
+
+
+def test_rope_scores_depend_only_on_relative_position():
+    """<R_m q, R_n k> == <R_{m+s} q, R_{n+s} k>: the property RoPE exists for."""
+    D, theta = 64, 10000.0
+    rng = np.random.default_rng(4)
+    q, k = rng.standard_normal(D), rng.standard_normal(D)
+    for m, n, s in [(5, 2, 100), (0, 7, 3), (1000, 999, 12345)]:
+        a = float(np.dot(oracle.rope_exact(q, m, theta), oracle.rope_exact(k, n, theta)))
+        b = float(np.dot(oracle.rope_exact(q, m + s, theta), oracle.rope_exact(k, n + s, theta)))
+        assert abs(a - b) < 1e-9 * max(1.0, abs(a))
+
+
+@pytest.mark.parametrize("dt", [BF16, F16])
+def test_rope_kv_write_position_zero_and_row_handling(dt):
+    """Position 0 is the identity (bit for bit); V rows are copied as by the plain write; a
+    padded row rotates q but writes nothing; an out-of-range position leaves its row alone."""
+    w = wl.write_rows_case(91, 12, n_kv_heads=2, head_dim=64, dtype=dt, pad_frac=0.0)
+    p, wr = w.pool, w.write
+    n = wr.key.shape[0]
+    q = wl.normal_bits(wl.derive_seed(91, 7), n * 4 * 64, dt).reshape(n, 4, 64)
+    sm = wr.slot_mapping.copy()
+    sm[3] = -1
+    pos = np.zeros(n, np.int64)
+    pos[5:] = np.arange(5, n) * 17
+    pos[7] = 1 << 40                      # out of range
+    q2, k2, v2, st = oracle.rope_kv_write(q, p.k_cache, p.v_cache, wr.key, wr.value, sm, pos, 4096, 1.0e6, dt,
+                                          check=False)
+    assert st == oracle.EBOUNDS
+    # V exactly as the plain write of the rows that are written
+    keep = sm.copy()
+    keep[7] = -1
+    _, v_ref, _ = oracle.kv_write(p.k_cache, p.v_cache, wr.key, wr.value, keep, p.block_size)
+    assert np.array_equal(v2, v_ref)
+    flat_k = k2.reshape(-1, 2, 64)
+    for i in range(n):
+        if sm[i] < 0 or i == 7:
+            continue
+        if pos[i] == 0:
+            assert np.array_equal(flat_k[sm[i]], wr.key[i])
+        else:  # the written row is the rotation of the key row
+            want = np.stack([oracle.round_to(oracle.rope_exact(f64(wr.key[i, h], dt), pos[i], 1.0e6), dt)
+                             for h in range(2)])
+            assert np.array_equal(flat_k[sm[i]], want)
+    assert np.array_equal(q2[:5], q[:5])           # position 0: identity, padded row 3 included
+    assert np.array_equal(q2[7], q[7])             # out of range: untouched
+    assert not np.array_equal(q2[6], q[6])
