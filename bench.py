@@ -158,18 +158,45 @@ WORKLOADS = {
     "long4": 3,
     "mixed": 5,
     "write64k": "write64k",   # bandwidth-scale KV write: 65,536 rows (10% padded) to random slots
+    "rope64k": "rope64k",     # the same write with rotary embedding fused in (keys, and 16 query heads per row)
+    "rope256": "rope256",     # the batch-256 decode step with the fused RoPE write in place of the plain one
 }
+ROPE_THETA, ROPE_MAX_POS = 1.0e6, 32768   # Qwen3-shaped: rotary base 1e6
 
 
 def make_bench_workload(k, wl):
-    if k == "write64k":
-        return wl.write_rows_case(232_104, 65536)
+    if k in ("write64k", "rope64k"):
+        w = wl.write_rows_case(232_104, 65536)
+        if k == "rope64k":
+            n = w.write.key.shape[0]
+            w.rope = dict(q=wl.normal_bits(wl.derive_seed(232_104, 12), n * 16 * 128, wl.BF16).reshape(n, 16, 128),
+                          positions=wl.uniform_ints(wl.derive_seed(232_104, 11), n, 0, ROPE_MAX_POS - 1).astype(np.int64))
+        return w
+    if k == "rope256":
+        w = wl.make_workload(4)
+        w.rope = dict(q=w.decode.q, positions=w.decode.context_lens.astype(np.int64) - 1)
+        return w
     return wl.make_workload(k)
+
+
+def rope_write_bytes(w):
+    """Positions and slots, query rows read and written, and per written row: key / value read,
+    both cache rows written, one cos / sin table row read."""
+    p, wr, q = w.pool, w.write, w.rope["q"]
+    n = wr.slot_mapping.size
+    valid = int((wr.slot_mapping >= 0).sum())
+    row = p.n_kv_heads * p.head_dim * 2
+    return 16 * n + 2 * q.nbytes + valid * (4 * row + p.head_dim * 4)
 
 
 def workload_name(k, wl):
     if k == "write64k":
         return "bandwidth-scale KV write: 65,536 rows x 8 KV heads x 128 (bf16, 10% padded -1) to random slots"
+    if k == "rope64k":
+        return ("bandwidth-scale KV write with fused RoPE: 65,536 rows x 8 KV heads x 128 + 16 query heads rotated "
+                "in place (bf16, 10% padded -1, positions U[0, 32768), base 1e6)")
+    if k == "rope256":
+        return "full decode step at batch 256 with the fused RoPE write (positions = context_len - 1, base 1e6)"
     return wl.WORKLOAD_NAMES[k]
 
 
@@ -242,14 +269,29 @@ def run_ours(args, rank, world, local_rank):
 
     kc, vc = dev_bits(p.k_cache), dev_bits(p.v_cache)
     stages = []   # name, launch, algorithmic amount, kind
+    rope = getattr(w, "rope", None)
+    if rope is not None and b is not None:
+        q_host = np.concatenate([b.q, pre.q]) if pre is not None else b.q
+        q = dev_bits(q_host)                       # rotated in place by the fused write, then decoded
+        q_rope = q[:b.num_seqs]
+    elif rope is not None:
+        q_rope = dev_bits(rope["q"])
     if wr is not None:
         key, val, sm = dev_bits(wr.key), dev_bits(wr.value), dev_int(wr.slot_mapping)
-        stages.append(("write", lambda: pa.pa_reshape_and_cache(key, val, kc, vc, sm), write_bytes(wr, p), "hbm"))
+        if rope is None:
+            stages.append(("write", lambda: pa.pa_reshape_and_cache(key, val, kc, vc, sm), write_bytes(wr, p), "hbm"))
+        else:
+            pos_d = dev_int(rope["positions"])
+            cos_sin = pa.rope_cos_sin(ROPE_MAX_POS, p.head_dim, ROPE_THETA, dev)
+            stages.append(("rope_write", lambda: pa.pa_rope_reshape_and_cache(key, val, kc, vc, sm, pos_d, cos_sin,
+                                                                              q=q_rope),
+                           rope_write_bytes(w), "hbm"))
     S, which, dec_logical = 0, 0, 0
     if b is not None:
         S, hq, D = b.q.shape
-        q_host = np.concatenate([b.q, pre.q]) if pre is not None else b.q
-        q = dev_bits(q_host)                       # decode rows first, then prefill rows
+        if rope is None:
+            q_host = np.concatenate([b.q, pre.q]) if pre is not None else b.q
+            q = dev_bits(q_host)                   # decode rows first, then prefill rows
         out = torch.empty_like(q)
         bt, cl = dev_int(b.block_tables), dev_int(b.context_lens)
         maxL = int(b.context_lens.max())
@@ -275,6 +317,8 @@ def run_ours(args, rank, world, local_rank):
         # first written K row as its completion check
         slot0 = int(wr.slot_mapping[wr.slot_mapping >= 0][0])
         out = kc[slot0 // p.block_size, slot0 % p.block_size]
+        if rope is not None:
+            q = q_rope
     if pre is not None:
         pbt, qsl, sl = dev_int(pre.block_tables), dev_int(pre.query_start_loc), dev_int(pre.seq_lens)
         stages.append(("prefill", lambda: pa.pa_prefill_chunk(out[S:], q[S:], kc, vc, pbt, qsl, sl, pre.max_q_len,
@@ -314,8 +358,8 @@ def run_ours(args, rank, world, local_rank):
     step_ms = max_over_ranks(float(st_ms.sum(axis=1).mean()), world)
     mean_ms = st_ms.mean(axis=0)
 
-    step_bytes = (write_bytes(wr, p) if wr is not None else 0) + dec_logical + (
-        prefill_bytes(pre, p) if pre is not None else 0)
+    wbytes = 0 if wr is None else (rope_write_bytes(w) if rope is not None else write_bytes(wr, p))
+    step_bytes = wbytes + dec_logical + (prefill_bytes(pre, p) if pre is not None else 0)
     value = world * step_bytes / (step_ms * 1e-3) / 1e9
     peaks = measured_peaks()
     breakdown = {}
@@ -348,6 +392,8 @@ def run_ours(args, rank, world, local_rank):
     # end to end through the C ABI with host buffers: inputs up, result down, every step
     pin = lambda t: t.cpu().pin_memory()
     h_in = [(q, pin(q)), (bt, pin(bt)), (cl, pin(cl))] if b is not None else []
+    if rope is not None:
+        h_in += [(pos_d, pin(pos_d))] + ([(q_rope, pin(q_rope))] if b is None else [])
     if wr is not None:
         h_in += [(key, pin(key)), (val, pin(val)), (sm, pin(sm))]
     if pre is not None:
@@ -461,15 +507,23 @@ def oracle_sample_step(w, n_seqs):
     t0 = time.perf_counter()
     nbytes_done = 0
     k_cache, v_cache = p.k_cache, p.v_cache
+    rope = getattr(w, "rope", None)
+    qs = None
     if wr is not None:
         sl = slice(0, n_seqs)
-        k_cache, v_cache, _ = oracle.kv_write(p.k_cache, p.v_cache, wr.key[sl], wr.value[sl],
-                                              wr.slot_mapping[sl], p.block_size)
+        if rope is None:
+            k_cache, v_cache, _ = oracle.kv_write(p.k_cache, p.v_cache, wr.key[sl], wr.value[sl],
+                                                  wr.slot_mapping[sl], p.block_size)
+        else:
+            qs, k_cache, v_cache, _ = oracle.rope_kv_write(rope["q"][sl], p.k_cache, p.v_cache, wr.key[sl],
+                                                           wr.value[sl], wr.slot_mapping[sl], rope["positions"][sl],
+                                                           ROPE_MAX_POS, ROPE_THETA, p.dtype)
+            nbytes_done += 2 * rope["q"][sl].nbytes + 16 * n_seqs
         valid = int((wr.slot_mapping[sl] >= 0).sum())
         nbytes_done += 2 * valid * p.n_kv_heads * p.head_dim * 2 * 2 + 8 * n_seqs
     if b is None:
         return nbytes_done, time.perf_counter() - t0
-    out = oracle.decode(b.q[:n_seqs], k_cache, v_cache, b.block_tables[:n_seqs], b.context_lens[:n_seqs], b.scale,
+    out = oracle.decode(b.q[:n_seqs] if qs is None else qs, k_cache, v_cache, b.block_tables[:n_seqs], b.context_lens[:n_seqs], b.scale,
                         p.dtype)
     dt = time.perf_counter() - t0
     sub = type(b)(b.q[:n_seqs], b.block_tables[:n_seqs], b.context_lens[:n_seqs], b.n_q_heads, b.scale)

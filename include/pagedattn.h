@@ -56,6 +56,7 @@ extern "C" {
 #define PA_DEVERR_BLOCK 2u   /* a block-table entry outside [0, num_blocks) was needed */
 #define PA_DEVERR_LENGTH 4u  /* a context / kv length outside its allowed range */
 #define PA_DEVERR_TIMEOUT 8u /* a pipeline wait in a kernel exceeded its time limit; the kernel gave up */
+#define PA_DEVERR_POSITION 16u /* a rotary-embedding position outside [0, max_position) */
 
 /* split-K piece length the pages use (mini_engine, "Custom CUDA kernels", v2) */
 #define PA_DEFAULT_PARTITION_TOKENS 256
@@ -76,6 +77,51 @@ extern "C" {
 int pa_reshape_and_cache(const void* key, const void* value, void* k_cache, void* v_cache,
                          const int64_t* slot_mapping, int64_t num_tokens, int n_kv_heads, int head_dim,
                          int block_size, int64_t num_blocks, int dtype, void* stream);
+
+/*
+ * pa_rope_table -- the cos / sin table pa_rope_reshape_and_cache reads (HOST function, no GPU).
+ * Source: mini_engine, "Features" (the Qwen3 decoder uses rotary position embedding) and
+ * "Roadmap" (fused RoPE folded into the KV-cache write).  Dimension pair i < head_dim / 2
+ * of a token at position m turns by the angle m * f_i, f_i = theta^(-2 i / head_dim).
+ *
+ *  out   HOST buffer of max_position * head_dim floats, written: row m holds
+ *        cos(m f_i) for i < head_dim / 2, then sin(m f_i) for i < head_dim / 2; angles and
+ *        functions in double, stored rounded to float.  The caller copies it to the device
+ *        once (it depends only on max_position, head_dim and theta).
+ *  Returns PA_ERR_NULL for out == NULL; PA_ERR_SHAPE for max_position <= 0, head_dim <= 0 or
+ *  odd, or theta <= 0.
+ */
+int pa_rope_table(float* out, int64_t max_position, int head_dim, double theta);
+
+/*
+ * pa_rope_reshape_and_cache -- KV-cache write with rotary position embedding fused in: the
+ * key rows are rotated on their way into k_cache, the query rows are rotated in place.
+ * Source: mini_engine, "Roadmap" (fused RoPE folded into the KV-cache write) and "Features"
+ * (Qwen3: GQA, RoPE); miniserve, "Engine" (per forward: qkv projection, RoPE, then the KV
+ * write at slot = block_id * block_size + offset).
+ *
+ * With c_i, s_i the table row of the token's position and half = head_dim / 2, a row x
+ * becomes, for i < half (the rotate-half pairing),
+ *     x'[i] = x[i] c_i - x[i + half] s_i,     x'[i + half] = x[i + half] c_i + x[i] s_i,
+ * computed in fp32 and rounded to dtype (nearest even); values are copied unchanged.
+ *
+ *  q            [num_tokens, n_q_heads, head_dim] rotated in place (every head of every row
+ *               with a valid position), or NULL to rotate keys only
+ *  key, value   [num_tokens, n_kv_heads, head_dim] read
+ *  k_cache, v_cache [num_blocks, block_size, n_kv_heads, head_dim]: at slot_mapping[i],
+ *               k_cache gets the rotated key row and v_cache the value row
+ *  slot_mapping [num_tokens] int64 as for pa_reshape_and_cache; -1: nothing is written for
+ *               the row (its q is still rotated)
+ *  positions    [num_tokens] int64 in [0, max_position); a row outside is left untouched (q
+ *               and cache) and sets PA_DEVERR_POSITION
+ *  cos_sin      [max_position, head_dim] float32, device copy of pa_rope_table's output
+ *  head_dim 64 or 128; n_q_heads >= 0 (ignored when q is NULL).  num_tokens == 0 launches
+ *  nothing and returns PA_OK.
+ */
+int pa_rope_reshape_and_cache(void* q, const void* key, const void* value, void* k_cache, void* v_cache,
+                              const int64_t* slot_mapping, const int64_t* positions, const float* cos_sin,
+                              int64_t num_tokens, int n_q_heads, int n_kv_heads, int head_dim, int block_size,
+                              int64_t num_blocks, int64_t max_position, int dtype, void* stream);
 
 /*
  * Split-K workspace size in bytes for pa_decode / pa_decode_splitk with these

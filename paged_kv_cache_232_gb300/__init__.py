@@ -16,14 +16,14 @@ from . import _build
 
 PA_F16, PA_BF16 = 0, 1
 PA_OK = 0
-PA_DEVERR_SLOT, PA_DEVERR_BLOCK, PA_DEVERR_LENGTH, PA_DEVERR_TIMEOUT = 1, 2, 4, 8
+PA_DEVERR_SLOT, PA_DEVERR_BLOCK, PA_DEVERR_LENGTH, PA_DEVERR_TIMEOUT, PA_DEVERR_POSITION = 1, 2, 4, 8, 16
 DEFAULT_PARTITION_TOKENS = 256
 
 # names the header declares; the CPU test checks that the library exports each one
 EXPORTED = (
     "pa_reshape_and_cache", "pa_decode_workspace_size", "pa_decode", "pa_decode_plan", "pa_decode_v1",
     "pa_decode_splitk", "pa_prefill_chunk", "pa_device_errors", "pa_status_string", "pa_version",
-    "pa_decode_splitk_static",
+    "pa_decode_splitk_static", "pa_rope_table", "pa_rope_reshape_and_cache",
 )
 STATIC_SCRATCH_BYTES = 16 << 20
 
@@ -55,6 +55,10 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
     vp, i32, i64, f32, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_float, ctypes.c_size_t
     L.pa_reshape_and_cache.argtypes = [vp, vp, vp, vp, vp, i64, i32, i32, i32, i64, i32, vp]
     L.pa_reshape_and_cache.restype = i32
+    L.pa_rope_table.argtypes = [vp, i64, i32, ctypes.c_double]
+    L.pa_rope_table.restype = i32
+    L.pa_rope_reshape_and_cache.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i64, i32, i32, i32, i32, i64, i64, i32, vp]
+    L.pa_rope_reshape_and_cache.restype = i32
     L.pa_decode_workspace_size.argtypes = [i32, i32, i32, i32, i32]
     L.pa_decode_workspace_size.restype = sz
     L.pa_decode.argtypes = [vp, vp, vp, vp, vp, i32, vp, i32, i32, i32, i32, i32, i32, i64, f32, i32, vp, sz, vp]
@@ -141,6 +145,38 @@ def pa_reshape_and_cache(key, value, k_cache, v_cache, slot_mapping, stream=None
                                      _dev(slot_mapping, "slot_mapping", torch.int64), n, hkv, d, bs, nb, dt,
                                      _stream(stream, key.device))
     _check(st, "pa_reshape_and_cache")
+
+
+def pa_rope_table(max_position: int, head_dim: int, theta: float):
+    """The float32 [max_position, head_dim] cos / sin table (host numpy array) the fused RoPE
+    write reads; copy it to the device once."""
+    import numpy as np
+    out = np.empty((int(max_position), int(head_dim)), dtype=np.float32)
+    _check(load().pa_rope_table(out.ctypes.data, int(max_position), int(head_dim), float(theta)), "pa_rope_table")
+    return out
+
+
+def rope_cos_sin(max_position: int, head_dim: int, theta: float, device="cuda"):
+    """pa_rope_table's output as a device tensor."""
+    return _torch().from_numpy(pa_rope_table(max_position, head_dim, theta)).to(device)
+
+
+def pa_rope_reshape_and_cache(key, value, k_cache, v_cache, slot_mapping, positions, cos_sin, q=None,
+                              stream=None) -> None:
+    """Rotate key [N, Hkv, D] by positions [N] (int64) with the cos_sin table [max_position, D]
+    (float32) and scatter it, and value unchanged, into the caches at slot_mapping [N] (int64,
+    -1 skips); q [N, Hq, D], if given, is rotated in place."""
+    torch = _torch()
+    dt = _dtype_code(key)
+    nb, bs, hkv, d = _cache_dims(k_cache)
+    n = int(key.shape[0])
+    qp, hq = (None, 0) if q is None else (_dev(q, "q", key.dtype), int(q.shape[1]))
+    st = load().pa_rope_reshape_and_cache(
+        qp, _dev(key, "key", key.dtype), _dev(value, "value", key.dtype), _dev(k_cache, "k_cache", key.dtype),
+        _dev(v_cache, "v_cache", key.dtype), _dev(slot_mapping, "slot_mapping", torch.int64),
+        _dev(positions, "positions", torch.int64), _dev(cos_sin, "cos_sin", torch.float32), n, hq, hkv, d, bs, nb,
+        int(cos_sin.shape[0]), dt, _stream(stream, key.device))
+    _check(st, "pa_rope_reshape_and_cache")
 
 
 def pa_decode_workspace_size(num_seqs: int, n_q_heads: int, head_dim: int, max_context_len: int,

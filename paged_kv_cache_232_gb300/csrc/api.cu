@@ -11,6 +11,7 @@
 #include <mutex>
 
 #include "kv_write.cuh"
+#include "rope_write.cuh"
 #include "pa_launch.h"
 #include "pagedattn.h"
 
@@ -250,6 +251,63 @@ int pa_reshape_and_cache(const void* key, const void* value, void* k_cache, void
     pa::kv_write_kernel<<<grid, threads, 0, static_cast<cudaStream_t>(stream)>>>(
         static_cast<const uint4*>(key), static_cast<const uint4*>(value), static_cast<uint4*>(k_cache),
         static_cast<uint4*>(v_cache), slot_mapping, num_tokens, row_vecs, num_blocks * block_size, dev->err);
+    return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
+int pa_rope_table(float* out, int64_t max_position, int head_dim, double theta) {
+    if (!out) return PA_ERR_NULL;
+    if (max_position <= 0 || head_dim <= 0 || (head_dim & 1) || !(theta > 0.0)) return PA_ERR_SHAPE;
+    const int half = head_dim / 2;
+    for (int i = 0; i < half; ++i) {
+        const double f = std::pow(theta, -2.0 * (double)i / (double)head_dim);
+        for (int64_t m = 0; m < max_position; ++m) {
+            const double a = (double)m * f;
+            out[m * head_dim + i] = (float)std::cos(a);
+            out[m * head_dim + half + i] = (float)std::sin(a);
+        }
+    }
+    return PA_OK;
+}
+
+int pa_rope_reshape_and_cache(void* q, const void* key, const void* value, void* k_cache, void* v_cache,
+                              const int64_t* slot_mapping, const int64_t* positions, const float* cos_sin,
+                              int64_t num_tokens, int n_q_heads, int n_kv_heads, int head_dim, int block_size,
+                              int64_t num_blocks, int64_t max_position, int dtype, void* stream) {
+    if (num_tokens < 0 || n_kv_heads <= 0 || head_dim <= 0 || block_size <= 0 || num_blocks <= 0 ||
+        max_position <= 0 || (q && n_q_heads <= 0))
+        return PA_ERR_SHAPE;
+    if (dtype != PA_F16 && dtype != PA_BF16) return PA_ERR_UNSUPPORTED;
+    if (head_dim != 64 && head_dim != 128) return PA_ERR_UNSUPPORTED;
+    if (num_tokens == 0) return PA_OK;
+    if (!key || !value || !k_cache || !v_cache || !slot_mapping || !positions || !cos_sin) return PA_ERR_NULL;
+    if (!aligned16(key) || !aligned16(value) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(cos_sin) ||
+        (q && !aligned16(q)))
+        return PA_ERR_ALIGN;
+    DeviceState* dev = nullptr;
+    int st = device_state(&dev);
+    if (st != PA_OK) return st;
+    const int pairs = head_dim / 16;
+    const int units = (q ? n_q_heads * pairs : 0) + n_kv_heads * pairs + n_kv_heads * (head_dim / 8);
+    const int threads = units >= 512 ? 512 : ((units + 31) / 32) * 32;
+    // two rows per thread in flight once there are at least four rows per SM, else one (more CTAs)
+    const int rows = num_tokens >= 4 * (int64_t)dev->sm_count ? 2 : 1;
+    const int64_t iters = (num_tokens + rows - 1) / rows;
+    const int64_t max_grid = (int64_t)dev->sm_count * (2048 / threads);
+    const int grid = (int)(iters < max_grid ? iters : max_grid);
+    auto launch = [&](auto kern) {
+        kern<<<grid, threads, 0, static_cast<cudaStream_t>(stream)>>>(
+            static_cast<uint4*>(q), static_cast<const uint4*>(key), static_cast<const uint4*>(value),
+            static_cast<uint4*>(k_cache), static_cast<uint4*>(v_cache), slot_mapping, positions, cos_sin, num_tokens,
+            n_q_heads, n_kv_heads, num_blocks * block_size, max_position, dev->err);
+    };
+    const bool bf = dtype == PA_BF16, d128 = head_dim == 128;
+    if (rows == 2) {
+        if (bf) d128 ? launch(pa::rope_write_kernel<true, 128, 2>) : launch(pa::rope_write_kernel<true, 64, 2>);
+        else d128 ? launch(pa::rope_write_kernel<false, 128, 2>) : launch(pa::rope_write_kernel<false, 64, 2>);
+    } else {
+        if (bf) d128 ? launch(pa::rope_write_kernel<true, 128, 1>) : launch(pa::rope_write_kernel<true, 64, 1>);
+        else d128 ? launch(pa::rope_write_kernel<false, 128, 1>) : launch(pa::rope_write_kernel<false, 64, 1>);
+    }
     return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 

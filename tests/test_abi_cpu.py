@@ -67,3 +67,33 @@ def test_validation_rejects_before_any_device_work(lib):
                                 None) == 0
     # write: a row of 1 head x 3 columns (6 bytes) is not a whole number of 16-byte chunks
     assert lib.pa_reshape_and_cache(vp, vp, vp, vp, vp, 4, 1, 3, 16, 10, 1, None) == -3
+
+
+def test_rope_table_matches_the_formula_and_validates(lib):
+    """pa_rope_table is host code: row m = [cos(m f_i) ..., sin(m f_i) ...], f_i = theta^(-2i/D),
+    computed in double and stored as float; compared with numpy's float64 cos / sin."""
+    import numpy as np
+    t = pa.pa_rope_table(257, 64, 1.0e6)
+    i = np.arange(32)
+    f = 1.0e6 ** (-2.0 * i / 64)
+    m = np.arange(257)[:, None]
+    want = np.concatenate([np.cos(m * f), np.sin(m * f)], axis=1).astype(np.float32)
+    assert np.array_equal(t, want)
+    buf = (ctypes.c_float * 16)()
+    assert lib.pa_rope_table(None, 2, 8, 1e4) == -1
+    assert lib.pa_rope_table(buf, 2, 7, 1e4) == -2
+    assert lib.pa_rope_table(buf, 0, 8, 1e4) == -2
+    assert lib.pa_rope_table(buf, 2, 8, -1.0) == -2
+
+
+def test_rope_write_validation_rejects_before_any_device_work(lib):
+    vp = ctypes.c_void_p(16)
+    args = lambda q=vp, d=128, n=4, dt=1, mp=100: (q, vp, vp, vp, vp, vp, vp, vp, n, 16, 8, d, 16, 10, mp, dt, None)
+    assert lib.pa_rope_reshape_and_cache(*args(d=96)) == -3          # head_dim
+    assert lib.pa_rope_reshape_and_cache(*args(dt=7)) == -3          # dtype
+    assert lib.pa_rope_reshape_and_cache(*args(mp=0)) == -2          # empty table
+    assert lib.pa_rope_reshape_and_cache(*args(n=0)) == 0            # nothing to do
+    assert lib.pa_rope_reshape_and_cache(ctypes.c_void_p(8), vp, vp, vp, vp, vp, vp, vp, 4, 16, 8, 128, 16, 10,
+                                         100, 1, None) == -6         # q misaligned
+    assert lib.pa_rope_reshape_and_cache(vp, None, vp, vp, vp, vp, vp, vp, 4, 16, 8, 128, 16, 10, 100, 1,
+                                         None) == -1                 # key NULL
