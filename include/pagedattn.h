@@ -81,7 +81,7 @@ int pa_reshape_and_cache(const void* key, const void* value, void* k_cache, void
 /*
  * pa_rope_table -- the cos / sin table pa_rope_reshape_and_cache reads (HOST function, no GPU).
  * Source: mini_engine, "Features" (the Qwen3 decoder uses rotary position embedding) and
- * "Roadmap" (fused RoPE folded into the KV-cache write).  Dimension pair i < head_dim / 2
+ * "Roadmap" (the rotary embedding applied inside the KV-cache write).  Dimension pair i < head_dim / 2
  * of a token at position m turns by the angle m * f_i, f_i = theta^(-2 i / head_dim).
  *
  *  out   HOST buffer of max_position * head_dim floats, written: row m holds
@@ -96,7 +96,7 @@ int pa_rope_table(float* out, int64_t max_position, int head_dim, double theta);
 /*
  * pa_rope_reshape_and_cache -- KV-cache write with rotary position embedding fused in: the
  * key rows are rotated on their way into k_cache, the query rows are rotated in place.
- * Source: mini_engine, "Roadmap" (fused RoPE folded into the KV-cache write) and "Features"
+ * Source: mini_engine, "Roadmap" (the rotary embedding applied inside the KV-cache write) and "Features"
  * (Qwen3: GQA, RoPE); miniserve, "Engine" (per forward: qkv projection, RoPE, then the KV
  * write at slot = block_id * block_size + offset).
  *

@@ -29,7 +29,8 @@
  *    causal mask): query row j of a chunk of q_len rows whose kv length is
  *    kv_len sees keys t <= (kv_len - q_len) + j.
  *  - Rotary position embedding fused into the KV write (mini_engine, "Roadmap":
- *    fused RoPE folded into the KV-cache write; "Features": Qwen3 with RoPE): the
+ *    the rotary embedding is to be applied inside the KV-cache write; "Features":
+ *    Qwen3 with RoPE): the
  *    textbook rotation of each dimension pair (i, i + head_dim/2) by m * f_i.
  *  - Materialise-then-attend (MiniLLM Runtime, "Key benchmark results"): copy the
  *    sequence's K/V into contiguous arrays first, then run the same textbook
@@ -165,7 +166,7 @@ int pao_kv_write(uint16_t* k_cache, uint16_t* v_cache, const uint16_t* key, cons
 
 /*
  * Rotary position embedding (mini_engine, "Features": the Qwen3 decoder uses RoPE;
- * "Roadmap": fused RoPE folded into the KV-cache write).  The textbook rotation, in the
+ * "Roadmap": the rotary embedding applied inside the KV-cache write).  The textbook rotation, in the
  * rotate-half pairing: with half = head_dim / 2 and f_i = theta^(-2 i / head_dim), a row x of
  * a token at position m becomes, for i < half,
  *     x'[i]        = x[i] cos(m f_i) - x[i + half] sin(m f_i)

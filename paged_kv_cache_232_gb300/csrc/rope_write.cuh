@@ -1,6 +1,6 @@
 // rope_write.cuh -- KV-cache write with rotary position embedding applied on the way, and the
-// query rows rotated in place (mini_engine, "Roadmap": fused RoPE folded into the KV-cache
-// write; "Features": the Qwen3 decoder's RoPE; miniserve, "Engine": per forward, the qkv
+// query rows rotated in place (mini_engine, "Roadmap": a planned kernel that applies the rotary
+// embedding inside the KV-cache write; "Features": the Qwen3 decoder's RoPE; miniserve, "Engine": per forward, the qkv
 // projection and RoPE, then the KV write at slot = block_id * block_size + offset).
 //
 // Rotation (rotate-half pairing): dims i and i + D/2 of a row at position m turn by the angle
