@@ -63,8 +63,8 @@ extern "C" {
 
 /*
  * pa_reshape_and_cache -- KV-cache write.
- * Source: mini_engine, "Custom CUDA kernels" (KV-cache write: scatters new K/V
- * rows into their paged slots, skipping padded slots); miniserve, "Engine"
+ * Source: mini_engine, "Custom CUDA kernels" (the KV-cache write kernel: each new
+ * K/V row goes to its slot of the pool, padded rows are left out); miniserve, "Engine"
  * (slot = block_id * block_size + offset).
  *
  *  key, value      [num_tokens, n_kv_heads, head_dim]            read

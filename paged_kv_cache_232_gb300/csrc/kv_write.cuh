@@ -1,6 +1,6 @@
-// kv_write.cuh -- KV-cache write (mini_engine, "Custom CUDA kernels": scatter new K/V rows
-// into their paged slots with 16-byte vector copies, skipping padded slots; miniserve,
-// "Engine": slot = block_id * block_size + offset).
+// kv_write.cuh -- KV-cache write (mini_engine, "Custom CUDA kernels": a kernel that puts each
+// new K/V row into its slot of the paged pool with 16-byte vector copies and leaves padded rows
+// out; miniserve, "Engine": slot = block_id * block_size + offset).
 //
 // A cache row for one slot, [n_kv_heads, head_dim], is contiguous in the
 // [num_blocks, block_size, n_kv_heads, head_dim] layout, so the write is a row scatter:
