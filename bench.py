@@ -319,7 +319,15 @@ def run_ours(args, rank, world, local_rank):
         out = kc[slot0 // p.block_size, slot0 % p.block_size]
         if rope is not None:
             q = q_rope
-    if pre is not None:
+    if pre is not None and args.unified:
+        # one prefill launch over every row: decode sequences as one-row chunks, then the chunks
+        u = wl.unified_batch(w)
+        pbt, qsl, sl = dev_int(u.block_tables), dev_int(u.query_start_loc), dev_int(u.seq_lens)
+        stages = [s_ for s_ in stages if s_[0] != "decode"]
+        stages.append(("unified", lambda: pa.pa_prefill_chunk(out, q, kc, vc, pbt, qsl, sl, u.max_q_len, u.scale),
+                       prefill_flops(u, hq, D), "tensor"))
+        which, dec_logical = 0, 0
+    elif pre is not None:
         pbt, qsl, sl = dev_int(pre.block_tables), dev_int(pre.query_start_loc), dev_int(pre.seq_lens)
         stages.append(("prefill", lambda: pa.pa_prefill_chunk(out[S:], q[S:], kc, vc, pbt, qsl, sl, pre.max_q_len,
                                                               pre.scale),
@@ -336,7 +344,7 @@ def run_ours(args, rank, world, local_rank):
         if ev:
             ev[ns].record(stream)
 
-    launches_per_step = ((1 if wr is not None else 0) + (0 if b is None else (1 if which == 1 else 2))
+    launches_per_step = ((1 if wr is not None else 0) + (0 if (b is None or which == 0) else (1 if which == 1 else 2))
                          + (1 if pre is not None else 0))
     for _ in range(args.warmup):
         step()
@@ -359,7 +367,8 @@ def run_ours(args, rank, world, local_rank):
     mean_ms = st_ms.mean(axis=0)
 
     wbytes = 0 if wr is None else (rope_write_bytes(w) if rope is not None else write_bytes(wr, p))
-    step_bytes = wbytes + dec_logical + (prefill_bytes(pre, p) if pre is not None else 0)
+    step_bytes = wbytes + (decode_bytes(b, p) if (b is not None and args.unified) else dec_logical) + (
+        prefill_bytes(pre, p) if pre is not None else 0)
     value = world * step_bytes / (step_ms * 1e-3) / 1e9
     peaks = measured_peaks()
     breakdown = {}
@@ -371,7 +380,7 @@ def run_ours(args, rank, world, local_rank):
             breakdown[name] = {"us": round(float(ms) * 1e3, 2), "tflops": round(amount / (ms * 1e-3) / 1e12, 1),
                                "frac_bf16": round(amount / (ms * 1e-3) / 1e12 / peaks["bf16_tflops"], 4),
                                "flop": amount}
-    if pre is not None and b is not None:
+    if pre is not None and b is not None and "decode" in breakdown:
         breakdown["decode"]["logical_gbs"] = round(dec_logical / (mean_ms[0] * 1e-3) / 1e9, 1)
     dom = int(np.argmax(mean_ms))
     dname, _, damount, dkind = stages[dom]
@@ -447,8 +456,9 @@ def run_ours(args, rank, world, local_rank):
            "block_size": p.block_size}
     if b is not None:
         cfg.update({"num_seqs": int(S), "n_q_heads": int(hq), "total_context_tokens": int(b.context_lens.sum()),
-                    "decode_path": ("one-pass" if which == 1 else f"split-K/{part}")
-                    + ("" if args.decode_path == "auto" else " (forced)")})
+                    "decode_path": ("unified: decode rows as one-row chunks of the prefill launch" if which == 0
+                                    else ("one-pass" if which == 1 else f"split-K/{part}")
+                                    + ("" if args.decode_path == "auto" else " (forced)"))})
     cfg.update({"l2": "512 MiB memset between timed steps (outside the events)",
                 "parallelism": f"replicas x{world} (independent batches, no collective)"})
     if wr is not None:
@@ -620,6 +630,8 @@ def main(argv=None):
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default="step256")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--unified", action="store_true",
+                    help="mixed batch: decode rows through the prefill kernel in the same launch (one-row chunks)")
     ap.add_argument("--decode-path", choices=["auto", "v1", "splitk"], default="auto",
                     help="force the one-pass or split-K decode kernel instead of the library's dispatcher")
     ap.add_argument("--partition", type=int, default=0, help="split-K piece length in tokens (with --decode-path splitk)")

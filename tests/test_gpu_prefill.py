@@ -155,3 +155,26 @@ def test_prefill_repeated_runs_bitwise_identical_and_no_device_errors(cfg):
         again = bits_of(run_prefill(w, out=out, kc=kc, vc=vc, q=q))
         assert np.array_equal(again, first)
     assert pa.pa_device_errors(clear=True) == 0
+
+
+def test_unified_mixed_batch_single_launch():
+    """The mixed batch through one prefill launch: each decode sequence a chunk of one query
+    row over its whole context, then the prefill chunks (the unified variant the split
+    dispatch is compared with).  Decode rows against the oracle's decode, prefill rows sampled."""
+    w = wl.make_workload(5)
+    p, b = w.pool, w.decode
+    u = wl.unified_batch(w)
+    kc, vc, q = to_dev(p.k_cache, p.dtype), to_dev(p.v_cache, p.dtype), to_dev(u.q, p.dtype)
+    out = torch.full_like(q, float("nan"))
+    pa.pa_device_errors(clear=True)
+    pa.pa_prefill_chunk(out, q, kc, vc, to_dev_i(u.block_tables, torch.int32), to_dev_i(u.query_start_loc, torch.int32),
+                        to_dev_i(u.seq_lens, torch.int32), u.max_q_len, u.scale)
+    torch.cuda.synchronize()
+    assert pa.pa_device_errors(clear=True) == 0
+    got = bits_of(out)
+    S = b.num_seqs
+    ex = oracle.decode(b.q, p.k_cache, p.v_cache, b.block_tables, b.context_lens, b.scale, p.dtype)
+    cd = oracle.decode(b.q, p.k_cache, abs_bits(p.v_cache), b.block_tables, b.context_lens, b.scale, p.dtype)
+    check(got[:S], (ex, cd), p.dtype, "unified: decode rows")
+    rows = np.arange(0, w.prefill.q.shape[0], 97)
+    check(got[S:][rows], oracle_rows(w, rows), p.dtype, "unified: prefill rows")

@@ -379,3 +379,19 @@ def write_rows_case(seed: int, n_rows: int, *, n_kv_heads: int = 8, head_dim: in
     pool = _fill_pool(seed, dtype, nb, bs, n_kv_heads, head_dim, pool_valid, -1, nan_canaries)
     return Workload(f"write{n_rows}", seed, pool, write=WriteBatch(key, val, slots),
                     meta=dict(dtype=dtype, n_kv_heads=n_kv_heads, head_dim=head_dim, block_size=bs))
+
+
+def unified_batch(w: "Workload") -> PrefillBatch:
+    """The mixed batch as one list of chunks for a single prefill launch: each decode sequence
+    as a chunk of one query row whose kv length is its context length, then the prefill chunks.
+    Rows keep their order (decode rows first), tables are padded to the wider of the two."""
+    b, pre = w.decode, w.prefill
+    mb = max(b.block_tables.shape[1], pre.block_tables.shape[1])
+    pad = lambda t: np.pad(t, ((0, 0), (0, mb - t.shape[1])), constant_values=0).astype(np.int32)
+    S = b.num_seqs
+    qsl = np.concatenate([np.arange(S + 1, dtype=np.int64), S + pre.query_start_loc[1:].astype(np.int64)])
+    return PrefillBatch(q=np.concatenate([b.q, pre.q]), block_tables=np.concatenate([pad(b.block_tables),
+                                                                                     pad(pre.block_tables)]),
+                        query_start_loc=qsl.astype(np.int32),
+                        seq_lens=np.concatenate([b.context_lens, pre.seq_lens]).astype(np.int32),
+                        n_q_heads=pre.n_q_heads, scale=pre.scale)
