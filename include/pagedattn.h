@@ -227,9 +227,9 @@ int pa_decode_splitk_static(void* out, const void* q, const void* k_cache, const
 
 /*
  * pa_prefill_chunk -- attention for ragged prefill chunks that attend to their
- * earlier cached context, on the tcgen05 tensor cores (head_dim 128 only).
+ * earlier cached context, on the tcgen05 tensor cores (head_dim 64 or 128).
  * Source: mini_engine, "Custom CUDA kernels" (paged prefill attention: tiled,
- * online softmax, K/V straight from the paged cache, ragged batches, prefix
+ * online softmax, K/V read from the paged pool itself, ragged batches, prefix
  * hits and chunks over earlier chunks in one launch); miniserve, "Engine"
  * (query_start_loc / block_table metadata, bottom-right causal mask).
  *

@@ -16,7 +16,7 @@
 //    (out-of-range block coordinate); the V producer zeroes the stray rows of the sequence's
 //    last, partial block before it hands the last stage over.
 //  * TMEM (512 columns): for each query tile t two 64-column S buffers at 128 t and the O
-//    accumulator at 256 + 128 t.  Keys are processed in 64-key sub-tiles u: S_t(u) = Q_t K^T
+//    accumulator (head_dim columns; head_dim 64 or 128) at 256 + head_dim t.  Keys are processed in 64-key sub-tiles u: S_t(u) = Q_t K^T
 //    (both operands from shared memory, K-major) lands in buffer u % 2, so the next
 //    sub-tile's S is computed while the softmax works on this one; O_t += P_t(u) V reads the
 //    weights from TMEM (the A operand) and V from shared memory (MN-major).
@@ -44,24 +44,29 @@ namespace pf {
 
 constexpr int BM = 128;                 // query rows per tile
 constexpr int BN = 128;                 // keys per tile
-constexpr int D = 128;                  // head_dim
 constexpr int NQT = 2;                  // query tiles per CTA
 constexpr int SLAB = BN * 128;          // 128 rows x 128 bytes: one 64-column slab
-constexpr int TILE = 2 * SLAB;          // a [128 x 128] 16-bit tile
-constexpr int Q_OFF = 0;                // NQT tiles
-constexpr int K_OFF = NQT * TILE;       // two stages
-constexpr int V_OFF = K_OFF + 2 * TILE; // two stages
-constexpr int BAR_OFF = V_OFF + 2 * TILE;
 constexpr int BS = 64;                  // keys per S sub-tile (two per K/V stage)
 // barriers: K_FULL / V_FULL per ring stage; K_EMPTY / V_EMPTY, S_FULL and P_FULL per (query tile,
 // buffer) at index 2 t + b; PV_DONE and DRAIN per query tile; V_ZERO once (last V stage cleaned)
 enum Bar { Q_FULL = 0, K_FULL = 1, V_FULL = 3, K_EMPTY = 5, V_EMPTY = 9, S_FULL = 13, P_FULL = 17, PV_DONE = 21,
            DRAIN = 23, V_ZERO = 25, NUM_BARS = 26 };
-constexpr int TMEM_SLOT_OFF = BAR_OFF + 32 * 8;
 static_assert(NUM_BARS <= 32, "barrier area");
-constexpr int SCHED_OFF = TMEM_SLOT_OFF + 16;    // CTA-order scratch: query_start_loc, seq_lens, cost histogram
 constexpr int SCHED_BYTES = 24 * 1024;
-constexpr int SMEM_BYTES = SCHED_OFF + SCHED_BYTES + 1024;  // + alignment slack
+// Shared-memory layout for head_dim D (64 or 128): a [128 x D] 16-bit tile is D / 64 slabs.
+template <int D>
+struct Layout {
+    static_assert(D == 64 || D == 128, "head_dim 64 or 128");
+    static constexpr int SLABS = D / 64;
+    static constexpr int TILE = SLABS * SLAB;
+    static constexpr int Q_OFF = 0;                 // NQT tiles
+    static constexpr int K_OFF = NQT * TILE;        // two stages
+    static constexpr int V_OFF = K_OFF + 2 * TILE;  // two stages
+    static constexpr int BAR_OFF = V_OFF + 2 * TILE;
+    static constexpr int TMEM_SLOT_OFF = BAR_OFF + 32 * 8;
+    static constexpr int SCHED_OFF = TMEM_SLOT_OFF + 16;  // CTA-order scratch: query_start_loc, seq_lens, histogram
+    static constexpr int SMEM_BYTES = SCHED_OFF + SCHED_BYTES + 1024;  // + alignment slack
+};
 // warpgroups 0..NQT-1: softmax (one per query tile); warpgroup NQT: K loads, MMA issue for tile 0,
 // V loads, MMA issue for tile 1
 static_assert(NQT == 2, "one MMA-issuing warp per query tile, two tiles");
@@ -73,7 +78,7 @@ constexpr int TMA_WARP = 4 * NQT, MMA_WARP = 4 * NQT + 1, TMA_V_WARP = 4 * NQT +
 constexpr int REGS_SOFTMAX = 208, REGS_PRODUCER = 88;
 static_assert(NQT * 128 * REGS_SOFTMAX + 128 * REGS_PRODUCER <= THREADS * 168, "register split exceeds the launch");
 constexpr uint32_t TMEM_COLS = 512;
-constexpr uint32_t O_COL = 256;         // S_t buffers at columns 128 t + 64 b, O_t at 256 + 128 t
+constexpr uint32_t O_COL = 256;         // S_t buffers at columns 128 t + 64 b, O_t (D columns) at 256 + D t
 
 }  // namespace pf
 
@@ -185,7 +190,7 @@ __device__ __forceinline__ void tmem_store16_stride2(uint32_t taddr, const uint3
 // (log2 units), so every rescale is an exact power of two.  Weights may reach 2^8 above the
 // reference; a sub-tile whose weights outgrow that is redone with a raised reference (S is
 // still intact), after O -- complete through the previous sub-tile's PV -- is rescaled.
-template <bool BF16>
+template <bool BF16, int D>
 __device__ __forceinline__ void softmax_sub64(const uint32_t tSb, const uint32_t tO, const bool masked, const int kbase,
                                               const int lim, const float sc, float& m_ref, float& l,
                                               const uint32_t pv_done, const int u, unsigned* err) {
@@ -222,7 +227,7 @@ __device__ __forceinline__ void softmax_sub64(const uint32_t tSb, const uint32_t
                 if (u > 0) (void)warp_wait(pv_done, (u - 1) & 1, err);
                 tc::fence_after();
 #pragma unroll 1
-                for (int q = 0; q < 8; ++q) {
+                for (int q = 0; q < D / 16; ++q) {
                     uint32_t o[16];
                     tc::ld16(tO + 16 * q, o);
                     tc::wait_ld();
@@ -262,31 +267,33 @@ __device__ __forceinline__ void softmax_sub64(const uint32_t tSb, const uint32_t
     }
 }
 
-template <int G, bool BF16>
+template <int G, bool BF16, int D>
 __global__ void __launch_bounds__(pf::THREADS, 1)
 prefill_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV) {
     using namespace pf;
+    using L = Layout<D>;
+    constexpr int SLABS = L::SLABS, TILE = L::TILE;
     using F = F16x2<BF16>;
     constexpr int TQ = BM / G;  // query tokens per tile
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sbase = smem_addr(smem);
-    const uint32_t sQ = sbase + Q_OFF, sK = sbase + K_OFF, sV = sbase + V_OFF;
-    const uint32_t bars = sbase + BAR_OFF;
-    volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(smem + TMEM_SLOT_OFF);
+    const uint32_t sQ = sbase + L::Q_OFF, sK = sbase + L::K_OFF, sV = sbase + L::V_OFF;
+    const uint32_t bars = sbase + L::BAR_OFF;
+    volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(smem + L::TMEM_SLOT_OFF);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     // Work unit u = (pair * C + chunk) * Hkv + head.  CTAs are dispatched in blockIdx order,
     // so handing out units longest-first gives longest-processing-time list scheduling.
     const int per_unit = p.num_chunks * p.n_kv_heads;
     int u_sel = (p.tiles_per_chunk - 1 - (int)(blockIdx.x / per_unit)) * per_unit + (int)(blockIdx.x % per_unit);
-    if (p.lpt) u_sel = lpt_unit<TQ * NQT>(p, smem + SCHED_OFF);
+    if (p.lpt) u_sel = lpt_unit<TQ * NQT>(p, smem + L::SCHED_OFF);
     const int unit = u_sel / per_unit;
     const int rem = u_sel % per_unit;
     const int c = rem / p.n_kv_heads, g = rem % p.n_kv_heads;
 
     // the CTA-order step left query_start_loc and seq_lens in shared memory
-    const int* sched = reinterpret_cast<const int*>(smem + SCHED_OFF);
+    const int* sched = reinterpret_cast<const int*>(smem + L::SCHED_OFF);
     const int q0 = p.lpt ? sched[c] : __ldg(p.query_start_loc + c);
     const int q_len = (p.lpt ? sched[c + 1] : __ldg(p.query_start_loc + c + 1)) - q0;
     const int kv_len = p.lpt ? sched[p.num_chunks + 1 + c] : __ldg(p.seq_lens + c);
@@ -349,23 +356,24 @@ prefill_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmK, c
         const int lim_min = ctx + jt0;              // smallest limit among the tile's rows
         const int nsub = (t == 0) ? n_sub[0] : n_sub[NQT - 1];
         {
-            // Q tile t: warp w of the group copies rows 32w .. 32w+31, two rows per instruction
-            // (lanes 0..15 one row, 16..31 the next: 512 contiguous bytes when G >= 2), each lane
-            // one 16-byte chunk into its 128-byte-swizzled place
+            // Q tile t: warp w of the group copies rows 32w .. 32w+31, 32 / CPR rows per
+            // instruction (consecutive rows are contiguous when G >= 2), each lane one 16-byte
+            // chunk into its 128-byte-swizzled place
+            constexpr int CPR = D / 8, RPI = 32 / CPR;  // chunks per row, rows per instruction
             const uint32_t qt = sQ + t * TILE;
-            const int ch = lane & 15;
-            uint4 v[16];
+            const int ch = lane % CPR;
+            uint4 v[CPR];
 #pragma unroll
-            for (int i = 0; i < 16; ++i) {
-                const int R = (warp & 3) * 32 + 2 * i + (lane >> 4);
+            for (int i = 0; i < CPR; ++i) {
+                const int R = (warp & 3) * 32 + RPI * i + lane / CPR;
                 const int tok = jt0 + R / G;
                 const uint16_t* src =
                     static_cast<const uint16_t*>(p.q) + ((size_t)(q0 + tok) * p.n_q_heads + g * G + R % G) * D + ch * 8;
                 v[i] = (tok < q_len) ? ldg_nc_128(src) : make_uint4(0u, 0u, 0u, 0u);
             }
 #pragma unroll
-            for (int i = 0; i < 16; ++i) {
-                const int R = (warp & 3) * 32 + 2 * i + (lane >> 4);
+            for (int i = 0; i < CPR; ++i) {
+                const int R = (warp & 3) * 32 + RPI * i + lane / CPR;
                 sts128(qt + (ch >> 3) * SLAB + swz128(R, ch & 7), v[i]);
             }
             tc::fence_async_smem();
@@ -387,7 +395,7 @@ prefill_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmK, c
             }
             tc::fence_after();
             const int kbase = u * BS;
-            softmax_sub64<BF16>(tS + (uint32_t)(b * BS), tO, kbase + BS - 1 > lim_min, kbase, lim, sc, m_ref, l,
+            softmax_sub64<BF16, D>(tS + (uint32_t)(b * BS), tO, kbase + BS - 1 > lim_min, kbase, lim, sc, m_ref, l,
                                 bars + 8 * (PV_DONE + t), u, p.err);
             tc::wait_st();
             tc::fence_before();
@@ -402,7 +410,7 @@ prefill_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmK, c
             tc::fence_after();
             const float inv = (l > 0.f) ? 1.f / l : 0.f;
 #pragma unroll 1
-            for (int q = 0; q < 4; ++q) {
+            for (int q = 0; q < D / 32; ++q) {
                 uint32_t o[32];
                 tc::ld32(tO + 32 * q, o);
                 tc::wait_ld();
@@ -456,10 +464,11 @@ prefill_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmK, c
             if (lane == 0) mbar_arrive_expect_tx(full, TILE);
             __syncwarp();
             {
-                // lanes 0..15 each issue one box: block lane % 8, 64-column slab lane / 8
+                // lanes 0 .. 8 SLABS - 1 each issue one box: block lane % 8, 64-column slab lane / 8
                 const int blk = __shfl_sync(0xffffffffu, my, lane & 7);
-                const int sl = (lane >> 3) & 1;
-                if (lane < 16) tma_load_4d(dst0 + sl * SLAB + (lane & 7) * 2048, map, sl * 64, g, 0, blk, full, pol);
+                const int sl = lane >> 3;
+                if (lane < 8 * SLABS)
+                    tma_load_4d(dst0 + sl * SLAB + (lane & 7) * 2048, map, sl * 64, g, 0, blk, full, pol);
             }
             if (kv == 1 && i == n_max - 1) {
                 // Rows of the sequence's last, partial block past kv_len may hold anything (P
@@ -468,9 +477,10 @@ prefill_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmK, c
                 if (lane == 0) ok = mbar_wait(full, ph, p.err);
                 if (!__shfl_sync(0xffffffffu, ok, 0)) break;
                 const int z0 = max(kv_len, i * BN), z1 = min(((kv_len + 15) / 16) * 16, (i + 1) * BN);
-                for (int e = lane; e < 16 * max(z1 - z0, 0); e += 32) {
-                    const int row = z0 - i * BN + e / 16;
-                    sts128(dst0 + ((e / 8) & 1) * SLAB + row * 128 + (e & 7) * 16, make_uint4(0u, 0u, 0u, 0u));
+                constexpr int CPR = D / 8;  // 16-byte chunks per row
+                for (int e = lane; e < CPR * max(z1 - z0, 0); e += 32) {
+                    const int row = z0 - i * BN + e / CPR, chk = e % CPR;
+                    sts128(dst0 + (chk >> 3) * SLAB + row * 128 + (chk & 7) * 16, make_uint4(0u, 0u, 0u, 0u));
                 }
                 tc::fence_async_smem();
                 __syncwarp();
@@ -573,12 +583,12 @@ prefill_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmK, c
     }
 }
 
-template <int G, bool BF16>
+template <int G, bool BF16, int D>
 static cudaError_t launch_prefill_t(const PrefillParams& p, const CUtensorMap& tmK, const CUtensorMap& tmV,
                                     cudaStream_t st) {
-    auto kern = prefill_kernel<G, BF16>;
+    auto kern = prefill_kernel<G, BF16, D>;
     static std::atomic<unsigned long long> s_done{0};
-    cudaError_t e = smem_limit_once(reinterpret_cast<const void*>(kern), pf::SMEM_BYTES, s_done);
+    cudaError_t e = smem_limit_once(reinterpret_cast<const void*>(kern), pf::Layout<D>::SMEM_BYTES, s_done);
     if (e != cudaSuccess) return e;
     // one CTA per pair of 128-row query tiles of a (chunk, KV head)
     const int units = (p.tiles_per_chunk + pf::NQT - 1) / pf::NQT;
@@ -588,26 +598,29 @@ static cudaError_t launch_prefill_t(const PrefillParams& p, const CUtensorMap& t
     const long sched_words = 2L * p.num_chunks + 1 + ncost + 3 + pf::THREADS / 32;
     q.lpt = (sched_words * 4 <= pf::SCHED_BYTES) ? 1 : 0;
     const int grid = units * p.num_chunks * p.n_kv_heads;
-    kern<<<grid, pf::THREADS, pf::SMEM_BYTES, st>>>(q, tmK, tmV);
+    kern<<<grid, pf::THREADS, pf::Layout<D>::SMEM_BYTES, st>>>(q, tmK, tmV);
     return cudaGetLastError();
 }
 
-template <bool BF16>
+template <bool BF16, int D>
 static cudaError_t by_group(int group, const PrefillParams& p, const CUtensorMap& k, const CUtensorMap& v,
                             cudaStream_t st) {
     switch (group) {
-        case 1: return launch_prefill_t<1, BF16>(p, k, v, st);
-        case 2: return launch_prefill_t<2, BF16>(p, k, v, st);
-        case 4: return launch_prefill_t<4, BF16>(p, k, v, st);
-        case 8: return launch_prefill_t<8, BF16>(p, k, v, st);
+        case 1: return launch_prefill_t<1, BF16, D>(p, k, v, st);
+        case 2: return launch_prefill_t<2, BF16, D>(p, k, v, st);
+        case 4: return launch_prefill_t<4, BF16, D>(p, k, v, st);
+        case 8: return launch_prefill_t<8, BF16, D>(p, k, v, st);
         default: return cudaErrorInvalidValue;
     }
 }
 
 cudaError_t launch_prefill(int bf16, int head_dim, int group, const PrefillParams& p, const CUtensorMap& tmK,
                            const CUtensorMap& tmV, cudaStream_t st) {
-    if (head_dim != pf::D) return cudaErrorNotSupported;
-    return bf16 ? by_group<true>(group, p, tmK, tmV, st) : by_group<false>(group, p, tmK, tmV, st);
+    if (head_dim == 128)
+        return bf16 ? by_group<true, 128>(group, p, tmK, tmV, st) : by_group<false, 128>(group, p, tmK, tmV, st);
+    if (head_dim == 64)
+        return bf16 ? by_group<true, 64>(group, p, tmK, tmV, st) : by_group<false, 64>(group, p, tmK, tmV, st);
+    return cudaErrorNotSupported;
 }
 
 }  // namespace pa

@@ -63,16 +63,27 @@ def check(got_bits, ref, dt, what):
     return check_attention(got_bits, ex, dt, what, cond=cd, rel=1e-4 + P_ROUND[dt])
 
 
-SHAPES = [(wl.BF16, 16, 8), (wl.F16, 16, 8), (wl.BF16, 8, 8), (wl.BF16, 32, 8), (wl.F16, 16, 2)]
+SHAPES = [(wl.BF16, 16, 8, 128), (wl.F16, 16, 8, 128), (wl.BF16, 8, 8, 128), (wl.BF16, 32, 8, 128),
+          (wl.F16, 16, 2, 128), (wl.BF16, 16, 8, 64), (wl.F16, 8, 8, 64), (wl.BF16, 32, 4, 64), (wl.F16, 2, 2, 64)]
 
 
-@pytest.mark.parametrize("dt,hq,hkv", SHAPES)
-def test_prefill_ragged_chunks_full_parity(dt, hq, hkv):
-    w = wl.build_workload("pf", 300 + hq + hkv, dtype=dt, n_q_heads=hq, n_kv_heads=hkv, head_dim=128,
+@pytest.mark.parametrize("dt,hq,hkv,d", SHAPES)
+def test_prefill_ragged_chunks_full_parity(dt, hq, hkv, d):
+    w = wl.build_workload("pf", 300 + hq + hkv + d, dtype=dt, n_q_heads=hq, n_kv_heads=hkv, head_dim=d,
                           prefill_q_lens=[1, 7, 64, 65, 128, 200, 17],
                           prefill_ctx_lens=[0, 20, 5, 127, 300, 1000, 16], extra_blocks=3)
     got = bits_of(run_prefill(w))
-    check(got, oracle_rows(w), dt, f"prefill {dt} {hq}/{hkv}")
+    check(got, oracle_rows(w), dt, f"prefill {dt} {hq}/{hkv} hd {d}")
+    assert pa.pa_device_errors(clear=True) == 0
+
+
+def test_prefill_head_dim_64_long_context_sampled_rows():
+    """hd 64 at a mixed-workload-like size: 4 chunks of 300 rows over 0..3000 cached tokens."""
+    w = wl.build_workload("pf64", 64_064, dtype=wl.BF16, n_q_heads=16, n_kv_heads=8, head_dim=64,
+                          prefill_q_lens=[300, 300, 300, 300], prefill_ctx_lens=[0, 1000, 2047, 3000], extra_blocks=3)
+    got = bits_of(run_prefill(w)).reshape(w.prefill.q.shape)
+    rows = np.unique(np.concatenate([np.arange(0, 1200, 37), [0, 299, 300, 599, 600, 899, 900, 1199]]))
+    check(got[rows], oracle_rows(w, rows), wl.BF16, "hd 64 long context")
     assert pa.pa_device_errors(clear=True) == 0
 
 
