@@ -15,7 +15,7 @@
  *    block_tables[seq][t / block_size], offset t % block_size (MiniLLM Runtime,
  *    "Core class relationships": logical token -> logical block + offset ->
  *    block_table -> physical address).
- *  - Supported shapes: block_size 16; head_dim 64 or 128; n_q_heads a multiple
+ *  - Supported shapes: block_size 16, 32, 64 or 128; head_dim 64 or 128; n_q_heads a multiple
  *    of n_kv_heads with group size G = n_q_heads / n_kv_heads in {1, 2, 4, 8};
  *    query head h reads KV head h / G.
  *  - stream is a cudaStream_t (NULL = legacy default stream).  Calls only

@@ -61,15 +61,16 @@ int device_state(DeviceState** out) {
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 // Tensor map over a paged cache [num_blocks, block_size, n_kv_heads, head_dim]: box of
-// 64 columns x 1 head x block_size rows x 1 block, 128-byte swizzled (one TMA load moves
-// one 128-byte column slab of one head's block tile).  Out-of-range block ids read zeros.
+// 64 columns x 1 head x 16 rows x 1 block, 128-byte swizzled (one TMA load moves one 128-byte
+// column slab of one head's 16-token chunk; with block_size 32..128 the kernels address the
+// chunk's rows inside its block by the row coordinate).  Out-of-range block ids read zeros.
 int encode_cache_map(CUtensorMap* m, const void* base, int dtype, int64_t num_blocks, int block_size,
                      int n_kv_heads, int head_dim) {
     cuuint64_t dims[4] = {(cuuint64_t)head_dim, (cuuint64_t)n_kv_heads, (cuuint64_t)block_size,
                           (cuuint64_t)num_blocks};
     cuuint64_t strides[3] = {(cuuint64_t)head_dim * 2, (cuuint64_t)n_kv_heads * head_dim * 2,
                              (cuuint64_t)block_size * n_kv_heads * head_dim * 2};
-    cuuint32_t box[4] = {64, 1, (cuuint32_t)block_size, 1};
+    cuuint32_t box[4] = {64, 1, 16, 1};  // 16 rows: block_size is a multiple of 16
     cuuint32_t estr[4] = {1, 1, 1, 1};
     CUresult r = g_encode(m, dtype == PA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 4,
                           const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -83,7 +84,7 @@ int check_heads(int n_q_heads, int n_kv_heads, int head_dim, int block_size, int
     const int G = n_q_heads / n_kv_heads;
     if (G != 1 && G != 2 && G != 4 && G != 8) return PA_ERR_UNSUPPORTED;
     if (head_dim != 64 && head_dim != 128) return PA_ERR_UNSUPPORTED;
-    if (block_size != 16) return PA_ERR_UNSUPPORTED;
+    if (block_size != 16 && block_size != 32 && block_size != 64 && block_size != 128) return PA_ERR_UNSUPPORTED;
     if (dtype != PA_F16 && dtype != PA_BF16) return PA_ERR_UNSUPPORTED;
     return PA_OK;
 }
@@ -143,6 +144,7 @@ int decode_impl(void* out, const void* q, const void* k_cache, const void* v_cac
     p.n_kv_heads = n_kv_heads;
     p.max_blocks_per_seq = max_blocks_per_seq;
     p.num_blocks = (int)num_blocks;
+    p.cpb_log2 = block_size == 16 ? 0 : block_size == 32 ? 1 : block_size == 64 ? 2 : 3;
     p.qk_scale_log2 = scale * 1.4426950408889634f;
     const int units = num_seqs * n_kv_heads;
     int grid = units;
@@ -392,6 +394,7 @@ int pa_prefill_chunk(void* out, const void* q, const void* k_cache, const void* 
     p.n_kv_heads = n_kv_heads;
     p.max_blocks_per_seq = max_blocks_per_seq;
     p.num_blocks = (int)num_blocks;
+    p.cpb_log2 = block_size == 16 ? 0 : block_size == 32 ? 1 : block_size == 64 ? 2 : 3;
     p.tiles_per_chunk = (int)(((int64_t)max_q_len * G + 127) / 128);
     p.qk_scale_log2 = scale * 1.4426950408889634f;
     if ((int64_t)p.tiles_per_chunk * num_chunks * n_kv_heads > INT32_MAX) return PA_ERR_UNSUPPORTED;

@@ -52,7 +52,7 @@ def test_validation_rejects_before_any_device_work(lib):
     assert lib.pa_decode_v1(vp, vp, vp, vp, vp, 8, vp, 1, 6, 4, 128, 16, 10, 0.1, 1, None) == -2
     # unsupported head_dim / block_size / dtype / group size
     assert lib.pa_decode_v1(vp, vp, vp, vp, vp, 8, vp, 1, 8, 8, 96, 16, 10, 0.1, 1, None) == -3
-    assert lib.pa_decode_v1(vp, vp, vp, vp, vp, 8, vp, 1, 8, 8, 128, 32, 10, 0.1, 1, None) == -3
+    assert lib.pa_decode_v1(vp, vp, vp, vp, vp, 8, vp, 1, 8, 8, 128, 24, 10, 0.1, 1, None) == -3
     assert lib.pa_decode_v1(vp, vp, vp, vp, vp, 8, vp, 1, 8, 8, 128, 16, 10, 0.1, 7, None) == -3
     assert lib.pa_decode_v1(vp, vp, vp, vp, vp, 8, vp, 1, 48, 3, 128, 16, 10, 0.1, 1, None) == -3
     # null pointers, misalignment

@@ -214,3 +214,18 @@ def test_zero_length_context_gives_zeros():
     for mode in ("v1", "splitk"):
         got = d.run(mode, cl=cl).reshape(2, 4, 128)
         assert np.all(got[0] == 0)
+
+
+@pytest.mark.parametrize("bs", [32, 64, 128])
+@pytest.mark.parametrize("mode,part", [("v1", 0), ("splitk", 0), ("splitk", 512)])
+def test_decode_block_sizes(bs, mode, part):
+    """Cache blocks of 32 / 64 / 128 tokens: 16-token chunks are read from their rows inside the
+    block (lengths straddling block and chunk boundaries, NaN in every unowned slot)."""
+    lens = [1, 15, 16, 17, bs - 1, bs, bs + 1, 3 * bs + 5, 2000]
+    for dt, hq, hkv, d in [(wl.BF16, 16, 8, 128), (wl.F16, 8, 2, 64)]:
+        w = wl.build_workload("bs", 900 + bs + d, dtype=dt, n_q_heads=hq, n_kv_heads=hkv, head_dim=d, block_size=bs,
+                              decode_lens=lens, extra_blocks=3)
+        pa.pa_device_errors(clear=True)
+        got = Dev(w).run(mode, part)
+        check(got, oracle_decode(w), dt, f"bs {bs} {mode}/{part} hd {d}")
+        assert pa.pa_device_errors(clear=True) == 0
