@@ -132,7 +132,7 @@ __device__ __forceinline__ float head_sum(float x) {
 }
 
 template <int D, int G, bool BF16>
-__global__ void __launch_bounds__(DecodeCfg<D, G, BF16>::THREADS)
+__global__ void __launch_bounds__(DecodeCfg<D, G, BF16>::THREADS, (G <= 4) ? 3 : 1)
 decode_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV) {
     using C = DecodeCfg<D, G, BF16>;
     using F = F16x2<BF16>;
