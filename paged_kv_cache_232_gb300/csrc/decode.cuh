@@ -131,8 +131,11 @@ __device__ __forceinline__ float head_sum(float x) {
     return x;
 }
 
+// Resident CTAs per SM the register allocation must allow: shared memory fits three; G <= 4
+// fits in the resulting 136 registers without spills (G = 4 would otherwise take ~150 and lose
+// a third of the warps); G = 8 at head_dim 64 fits two, at head_dim 128 only one without spills.
 template <int D, int G, bool BF16>
-__global__ void __launch_bounds__(DecodeCfg<D, G, BF16>::THREADS, (G <= 4) ? 3 : 1)
+__global__ void __launch_bounds__(DecodeCfg<D, G, BF16>::THREADS, (G <= 4) ? 3 : (D == 64 ? 2 : 1))
 decode_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV) {
     using C = DecodeCfg<D, G, BF16>;
     using F = F16x2<BF16>;
