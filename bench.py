@@ -296,7 +296,8 @@ def run_ours(args, rank, world, local_rank):
         bt, cl = dev_int(b.block_tables), dev_int(b.context_lens)
         maxL = int(b.context_lens.max())
         ws = torch.empty(max(pa.pa_decode_workspace_size(S, hq, D, maxL, 0), 16), dtype=torch.uint8, device=dev)
-        which, part = pa.pa_decode_plan(S, p.n_kv_heads, maxL)
+        which, part = pa.pa_decode_plan(S, hq, p.n_kv_heads, D, p.block_size, maxL,
+                                        pa.PA_BF16 if p.dtype == wl.BF16 else pa.PA_F16)
         if args.decode_path == "v1":
             which = 1
         elif args.decode_path == "splitk":

@@ -167,9 +167,15 @@ int pa_decode(void* out, const void* q, const void* k_cache, const void* v_cache
 /*
  * The dispatcher's decision for these sizes on the current device, without
  * launching: returns 1 for the one-pass kernel, 2 for split-K, or a negative
- * status.  *partition_tokens (if not NULL) receives the split-K piece length.
+ * status (PA_ERR_SHAPE / PA_ERR_UNSUPPORTED as pa_decode, PA_ERR_CUDA).
+ * *partition_tokens (if not NULL) receives the split-K piece length: a
+ * multiple of block_size, at least PA_DEFAULT_PARTITION_TOKENS, chosen so the
+ * grid fills whole waves of the CTAs resident on the device's SMs.  The first
+ * call for a (dtype, head_dim, group) on a device queries the kernel's
+ * occupancy; later calls make no CUDA call (safe inside a stream capture).
  */
-int pa_decode_plan(int num_seqs, int n_kv_heads, int max_context_len, int* partition_tokens);
+int pa_decode_plan(int num_seqs, int n_q_heads, int n_kv_heads, int head_dim, int block_size, int max_context_len,
+                   int dtype, int* partition_tokens);
 
 /*
  * pa_decode_v1 -- the one-pass decode kernel: one CTA per (sequence, KV head)

@@ -63,7 +63,7 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
     L.pa_decode_workspace_size.restype = sz
     L.pa_decode.argtypes = [vp, vp, vp, vp, vp, i32, vp, i32, i32, i32, i32, i32, i32, i64, f32, i32, vp, sz, vp]
     L.pa_decode.restype = i32
-    L.pa_decode_plan.argtypes = [i32, i32, i32, ctypes.POINTER(i32)]
+    L.pa_decode_plan.argtypes = [i32, i32, i32, i32, i32, i32, i32, ctypes.POINTER(i32)]
     L.pa_decode_plan.restype = i32
     L.pa_decode_v1.argtypes = [vp, vp, vp, vp, vp, i32, vp, i32, i32, i32, i32, i32, i64, f32, i32, vp]
     L.pa_decode_v1.restype = i32
@@ -184,10 +184,12 @@ def pa_decode_workspace_size(num_seqs: int, n_q_heads: int, head_dim: int, max_c
     return int(load().pa_decode_workspace_size(num_seqs, n_q_heads, head_dim, max_context_len, partition_tokens))
 
 
-def pa_decode_plan(num_seqs: int, n_kv_heads: int, max_context_len: int):
+def pa_decode_plan(num_seqs: int, n_q_heads: int, n_kv_heads: int, head_dim: int, block_size: int,
+                   max_context_len: int, dtype: int = PA_BF16):
     """(1 = one-pass kernel | 2 = split-K, partition_tokens) for these sizes on the current device."""
     pt = ctypes.c_int(0)
-    r = load().pa_decode_plan(num_seqs, n_kv_heads, max_context_len, ctypes.byref(pt))
+    r = load().pa_decode_plan(num_seqs, n_q_heads, n_kv_heads, head_dim, block_size, max_context_len, dtype,
+                              ctypes.byref(pt))
     if r < 0:
         raise PagedAttnError(r, "pa_decode_plan")
     return r, pt.value

@@ -183,17 +183,38 @@ int decode_impl(void* out, const void* q, const void* k_cache, const void* v_cac
 // Dispatcher (mini_engine, "Custom CUDA kernels": split-K when few sequences or long
 // contexts cannot fill the GPU, the one-pass kernel when there is enough parallelism).
 // The thresholds are this library's, set from GB300 measurements: the one-pass kernel wins
-// as soon as there is a (sequence, KV head) unit per SM and contexts are short; otherwise
-// split-K, with the piece doubled from 256 tokens while the grid still holds four pieces per
-// SM (longer pieces amortise each CTA's pipeline start and shrink the merge).
-int plan(int num_seqs, int n_kv_heads, int max_context_len, int sm_count, int* part_tokens) {
-    const int64_t units = (int64_t)num_seqs * n_kv_heads;
-    int part = PA_DEFAULT_PARTITION_TOKENS;
-    if (part_tokens) *part_tokens = part;
-    if (max_context_len <= PA_DEFAULT_PARTITION_TOKENS) return 1;
+// as soon as there is a (sequence, KV head) unit per SM and contexts are at most 8192 tokens;
+// otherwise split-K.  The piece length sizes the grid in whole waves of resident CTAs: taking
+// every context at the maximum, n equal pieces per unit cost waves(n) x (piece(n) + 64), the
+// 64 tokens standing for a CTA's pipeline start and its share of the merge (fitted to GB300
+// timings of 32 units of 32K tokens: one full wave of 2352-token pieces beats two of 1184 by
+// 3 % and 2.25 waves of 1024 by 10 %), and the plan takes the fewest pieces whose cost is
+// within 2 % of the best.  Pieces are at least 256 tokens, so a workspace sized for the
+// default piece fits every plan.
+int plan(int64_t units, int max_context_len, int sm_count, int resident, int block_size, int* part_tokens) {
+    const int min_piece = PA_DEFAULT_PARTITION_TOKENS;
+    if (part_tokens) *part_tokens = min_piece;
+    if (max_context_len <= min_piece) return 1;
     if (units >= sm_count && max_context_len <= 8192) return 1;
-    while (part < 4096 && units * ((max_context_len + 2 * part - 1) / (2 * part)) >= 4 * (int64_t)sm_count) part *= 2;
-    if (part_tokens) *part_tokens = part;
+    const int64_t slots = (int64_t)sm_count * (resident > 0 ? resident : 1);
+    const int64_t L = max_context_len;
+    const int n_max = (int)std::min<int64_t>((L + min_piece - 1) / min_piece, 1024);
+    int64_t best = INT64_MAX;
+    for (int n = 2; n <= n_max; ++n) {
+        const int64_t piece = std::max<int64_t>(min_piece, ((L + n - 1) / n + block_size - 1) / block_size * block_size);
+        const int64_t ctas = units * ((L + piece - 1) / piece);
+        best = std::min(best, (ctas + slots - 1) / slots * (piece + 64));
+    }
+    int chosen = min_piece;
+    for (int n = 2; n <= n_max; ++n) {
+        const int64_t piece = std::max<int64_t>(min_piece, ((L + n - 1) / n + block_size - 1) / block_size * block_size);
+        const int64_t ctas = units * ((L + piece - 1) / piece);
+        if ((ctas + slots - 1) / slots * (piece + 64) * 50 <= best * 51) {
+            chosen = (int)piece;
+            break;
+        }
+    }
+    if (part_tokens) *part_tokens = chosen;
     return 2;
 }
 
@@ -322,12 +343,17 @@ size_t pa_decode_workspace_size(int num_seqs, int n_q_heads, int head_dim, int m
     return ws_layout(num_seqs, n_q_heads, head_dim, max_parts).total;
 }
 
-int pa_decode_plan(int num_seqs, int n_kv_heads, int max_context_len, int* partition_tokens) {
-    if (num_seqs < 0 || n_kv_heads <= 0 || max_context_len < 0) return PA_ERR_SHAPE;
-    DeviceState* dev = nullptr;
-    int st = device_state(&dev);
+int pa_decode_plan(int num_seqs, int n_q_heads, int n_kv_heads, int head_dim, int block_size, int max_context_len,
+                   int dtype, int* partition_tokens) {
+    if (num_seqs < 0 || max_context_len < 0) return PA_ERR_SHAPE;
+    int st = check_heads(n_q_heads, n_kv_heads, head_dim, block_size, dtype);
     if (st != PA_OK) return st;
-    return plan(num_seqs, n_kv_heads, max_context_len, dev->sm_count, partition_tokens);
+    DeviceState* dev = nullptr;
+    if ((st = device_state(&dev)) != PA_OK) return st;
+    const int resident = pa::decode_resident_ctas(dtype == PA_BF16, head_dim, n_q_heads / n_kv_heads);
+    if (resident <= 0) return PA_ERR_CUDA;
+    return plan((int64_t)num_seqs * n_kv_heads, max_context_len, dev->sm_count, resident, block_size,
+                partition_tokens);
 }
 
 int pa_decode_v1(void* out, const void* q, const void* k_cache, const void* v_cache, const int32_t* block_tables,
@@ -357,7 +383,8 @@ int pa_decode(void* out, const void* q, const void* k_cache, const void* v_cache
     if (max_context_len < 0 || (int64_t)max_context_len > (int64_t)max_blocks_per_seq * block_size)
         return PA_ERR_BOUNDS;
     int part = 0;
-    const int which = pa_decode_plan(num_seqs, n_kv_heads > 0 ? n_kv_heads : 1, max_context_len, &part);
+    const int which = pa_decode_plan(num_seqs, n_q_heads, n_kv_heads, head_dim, block_size, max_context_len, dtype,
+                                     &part);
     if (which < 0) return which;
     if (which == 1)
         return pa_decode_v1(out, q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens, num_seqs,

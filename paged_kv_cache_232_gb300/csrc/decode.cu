@@ -3,13 +3,38 @@
 
 namespace pa {
 
+// per instantiation: the devices whose shared-memory limit for the kernel has been raised
+template <int D, int G, bool BF16>
+static std::atomic<unsigned long long>& smem_flag() {
+    static std::atomic<unsigned long long> f{0};
+    return f;
+}
+
+// CTAs of the instantiation resident per SM (registers, shared memory, launch bounds),
+// queried once per device and cached.
+template <int D, int G, bool BF16>
+static int resident_t() {
+    static std::atomic<int> cache[64];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    int r = cache[dev & 63].load(std::memory_order_acquire);
+    if (r > 0) return r;
+    using C = DecodeCfg<D, G, BF16>;
+    auto kern = decode_kernel<D, G, BF16>;
+    if (smem_limit_once(reinterpret_cast<const void*>(kern), C::SMEM_BYTES, smem_flag<D, G, BF16>()) != cudaSuccess)
+        return 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&r, kern, C::THREADS, C::SMEM_BYTES) != cudaSuccess || r < 1)
+        return 0;
+    cache[dev & 63].store(r, std::memory_order_release);
+    return r;
+}
+
 template <int D, int G, bool BF16>
 static cudaError_t launch_decode_t(const DecodeParams& p, const CUtensorMap& tmK, const CUtensorMap& tmV, int grid,
                                    bool with_reduce, cudaStream_t st) {
     using C = DecodeCfg<D, G, BF16>;
     auto kern = decode_kernel<D, G, BF16>;
-    static std::atomic<unsigned long long> s_done{0};
-    cudaError_t e = smem_limit_once(reinterpret_cast<const void*>(kern), C::SMEM_BYTES, s_done);
+    cudaError_t e = smem_limit_once(reinterpret_cast<const void*>(kern), C::SMEM_BYTES, smem_flag<D, G, BF16>());
     if (e != cudaSuccess) return e;
     kern<<<grid, C::THREADS, C::SMEM_BYTES, st>>>(p, tmK, tmV);
     e = cudaGetLastError();
@@ -37,6 +62,23 @@ static cudaError_t by_group(int group, const DecodeParams& p, const CUtensorMap&
         case 8: return launch_decode_t<D, 8, BF16>(p, k, v, grid, r, st);
         default: return cudaErrorInvalidValue;
     }
+}
+
+template <int D, bool BF16>
+static int resident_by_group(int group) {
+    switch (group) {
+        case 1: return resident_t<D, 1, BF16>();
+        case 2: return resident_t<D, 2, BF16>();
+        case 4: return resident_t<D, 4, BF16>();
+        case 8: return resident_t<D, 8, BF16>();
+        default: return 0;
+    }
+}
+
+int decode_resident_ctas(int bf16, int head_dim, int group) {
+    if (head_dim == 128) return bf16 ? resident_by_group<128, true>(group) : resident_by_group<128, false>(group);
+    if (head_dim == 64) return bf16 ? resident_by_group<64, true>(group) : resident_by_group<64, false>(group);
+    return 0;
 }
 
 cudaError_t launch_decode(int bf16, int head_dim, int group, const DecodeParams& p, const CUtensorMap& tmK,

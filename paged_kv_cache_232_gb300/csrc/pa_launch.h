@@ -28,6 +28,10 @@ inline cudaError_t smem_limit_once(const void* func, int bytes, std::atomic<unsi
 
 // Launch the decode piece kernel for (dtype, head_dim, group) on `grid` CTAs; when
 // params.part_tokens > 0 and any sequence has more than one piece, also launch the reduce.
+// CTAs of the decode kernel for (dtype, head_dim, group) that fit on one SM (0 on a CUDA error);
+// queried once per device, so a call inside a stream capture makes no CUDA call.
+int decode_resident_ctas(int bf16, int head_dim, int group);
+
 cudaError_t launch_decode(int bf16, int head_dim, int group, const DecodeParams& params, const CUtensorMap& tmK,
                           const CUtensorMap& tmV, int grid, bool with_reduce, cudaStream_t stream);
 

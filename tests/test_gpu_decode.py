@@ -106,7 +106,8 @@ EDGE_LENS = [1, 15, 16, 17, 255, 256, 257, 513, 4097]
 @pytest.mark.parametrize("dt,hq,hkv,d", [(wl.BF16, 16, 8, 128), (wl.F16, 2, 2, 64), (wl.BF16, 32, 8, 128),
                                          (wl.F16, 8, 1, 128), (wl.BF16, 8, 2, 64), (wl.F16, 16, 4, 128),
                                          (wl.BF16, 8, 1, 64)])
-@pytest.mark.parametrize("mode,part", [("v1", 0), ("splitk", 0), ("splitk", 64), ("splitk", 512)])
+@pytest.mark.parametrize("mode,part", [("v1", 0), ("splitk", 0), ("splitk", 64), ("splitk", 512), ("splitk", 48),
+                                       ("splitk", 400)])
 def test_decode_edge_lengths(dt, hq, hkv, d, mode, part):
     w = wl.build_workload("edge", 77 + hq + d, dtype=dt, n_q_heads=hq, n_kv_heads=hkv, head_dim=d,
                           decode_lens=EDGE_LENS, max_blocks_per_seq=300, extra_blocks=5)
@@ -230,3 +231,30 @@ def test_decode_block_sizes(bs, mode, part):
         got = Dev(w).run(mode, part)
         check(got, oracle_decode(w), dt, f"bs {bs} {mode}/{part} hd {d}")
         assert pa.pa_device_errors(clear=True) == 0
+
+
+@pytest.mark.parametrize("S,hq,hkv,d,bs,L", [(4, 32, 8, 128, 16, 32768), (2, 16, 8, 128, 16, 5000),
+                                            (8, 8, 1, 64, 64, 20000), (300, 16, 8, 128, 16, 16384),
+                                            (1, 2, 2, 64, 128, 300)])
+def test_dispatcher_plan_pieces(S, hq, hkv, d, bs, L):
+    """Split-K plans: pieces are a multiple of the block size and at least the default 256
+    tokens, so a workspace sized for the default piece fits every plan."""
+    which, part = pa.pa_decode_plan(S, hq, hkv, d, bs, L, pa.PA_BF16)
+    assert which == 2
+    assert part % bs == 0 and part >= 256
+    assert pa.pa_decode_workspace_size(S, hq, d, L, part) <= pa.pa_decode_workspace_size(S, hq, d, L, 0)
+    assert pa.pa_decode_plan(256, 16, 8, 128, 16, 2048)[0] == 1       # one-pass: enough units, short contexts
+
+
+def test_long_context_planned_pieces_match_oracle():
+    """The dispatcher's piece length for four 32K-token contexts (not a power of two) through
+    pa_decode, against the oracle."""
+    w = wl.make_workload(3)
+    b = w.decode
+    which, part = pa.pa_decode_plan(b.num_seqs, b.q.shape[1], w.pool.n_kv_heads, b.q.shape[2], 16,
+                                    int(b.context_lens.max()), pa.PA_BF16)
+    assert which == 2 and part % 16 == 0
+    pa.pa_device_errors(clear=True)
+    got = Dev(w).run("splitk", part)
+    check(got, oracle_decode(w), w.pool.dtype, f"config3/splitk {part}")
+    assert pa.pa_device_errors(clear=True) == 0
