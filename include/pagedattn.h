@@ -15,7 +15,7 @@
  *    block_tables[seq][t / block_size], offset t % block_size (MiniLLM Runtime,
  *    "Core class relationships": logical token -> logical block + offset ->
  *    block_table -> physical address).
- *  - Supported shapes: block_size 16, 32, 64 or 128; head_dim 64 or 128; n_q_heads a multiple
+ *  - Supported shapes: block_size 8, 16, 32, 64 or 128; head_dim 64 or 128; n_q_heads a multiple
  *    of n_kv_heads with group size G = n_q_heads / n_kv_heads in {1, 2, 4, 8};
  *    query head h reads KV head h / G.
  *  - stream is a cudaStream_t (NULL = legacy default stream).  Calls only
@@ -169,7 +169,7 @@ int pa_decode(void* out, const void* q, const void* k_cache, const void* v_cache
  * launching: returns 1 for the one-pass kernel, 2 for split-K, or a negative
  * status (PA_ERR_SHAPE / PA_ERR_UNSUPPORTED as pa_decode, PA_ERR_CUDA).
  * *partition_tokens (if not NULL) receives the split-K piece length: a
- * multiple of block_size, at least PA_DEFAULT_PARTITION_TOKENS, chosen so the
+ * multiple of block_size and of 16, at least PA_DEFAULT_PARTITION_TOKENS, chosen so the
  * grid fills whole waves of the CTAs resident on the device's SMs.  The first
  * call for a (dtype, head_dim, group) on a device queries the kernel's
  * occupancy; later calls make no CUDA call (safe inside a stream capture).
@@ -191,7 +191,7 @@ int pa_decode_v1(void* out, const void* q, const void* k_cache, const void* v_ca
 /*
  * pa_decode_splitk -- split-K decode (mini_engine, "Custom CUDA kernels", v2):
  * the context is cut into pieces of partition_tokens tokens (a multiple of
- * block_size; <= 0 means 256) processed by separate CTAs, each writing its max,
+ * block_size and of 16; <= 0 means 256) processed by separate CTAs, each writing its max,
  * exp-sum and normalised output to the workspace; a reduce kernel merges them
  * with weights l_p * exp(m_p - max m).  Sequences with one piece are written
  * directly.  Arguments as pa_decode.

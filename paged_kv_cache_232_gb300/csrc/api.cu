@@ -70,7 +70,8 @@ int encode_cache_map(CUtensorMap* m, const void* base, int dtype, int64_t num_bl
                           (cuuint64_t)num_blocks};
     cuuint64_t strides[3] = {(cuuint64_t)head_dim * 2, (cuuint64_t)n_kv_heads * head_dim * 2,
                              (cuuint64_t)block_size * n_kv_heads * head_dim * 2};
-    cuuint32_t box[4] = {64, 1, 16, 1};  // 16 rows: block_size is a multiple of 16
+    // one 16-token chunk of a block (an 8-token block is loaded whole, two per chunk)
+    cuuint32_t box[4] = {64, 1, (cuuint32_t)(block_size < 16 ? block_size : 16), 1};
     cuuint32_t estr[4] = {1, 1, 1, 1};
     CUresult r = g_encode(m, dtype == PA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 4,
                           const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -84,9 +85,15 @@ int check_heads(int n_q_heads, int n_kv_heads, int head_dim, int block_size, int
     const int G = n_q_heads / n_kv_heads;
     if (G != 1 && G != 2 && G != 4 && G != 8) return PA_ERR_UNSUPPORTED;
     if (head_dim != 64 && head_dim != 128) return PA_ERR_UNSUPPORTED;
-    if (block_size != 16 && block_size != 32 && block_size != 64 && block_size != 128) return PA_ERR_UNSUPPORTED;
+    if (block_size != 8 && block_size != 16 && block_size != 32 && block_size != 64 && block_size != 128)
+        return PA_ERR_UNSUPPORTED;
     if (dtype != PA_F16 && dtype != PA_BF16) return PA_ERR_UNSUPPORTED;
     return PA_OK;
+}
+
+// log2 of the 16-token chunks per cache block; -1 for blocks of 8 tokens (two per chunk)
+int cpb_log2_of(int block_size) {
+    return block_size == 8 ? -1 : block_size == 16 ? 0 : block_size == 32 ? 1 : block_size == 64 ? 2 : 3;
 }
 
 int partition_or_default(int part) { return part > 0 ? part : PA_DEFAULT_PARTITION_TOKENS; }
@@ -144,13 +151,13 @@ int decode_impl(void* out, const void* q, const void* k_cache, const void* v_cac
     p.n_kv_heads = n_kv_heads;
     p.max_blocks_per_seq = max_blocks_per_seq;
     p.num_blocks = (int)num_blocks;
-    p.cpb_log2 = block_size == 16 ? 0 : block_size == 32 ? 1 : block_size == 64 ? 2 : 3;
+    p.cpb_log2 = cpb_log2_of(block_size);
     p.qk_scale_log2 = scale * 1.4426950408889634f;
     const int units = num_seqs * n_kv_heads;
     int grid = units;
     bool reduce = false;
     if (part_tokens > 0) {
-        if (part_tokens % block_size) return PA_ERR_UNSUPPORTED;
+        if (part_tokens % (block_size < 16 ? 16 : block_size)) return PA_ERR_UNSUPPORTED;  // whole chunks and blocks
         if (max_context_len < 0 || (int64_t)max_context_len > (int64_t)max_blocks_per_seq * block_size)
             return PA_ERR_BOUNDS;
         const int max_parts = max_context_len > 0 ? (max_context_len + part_tokens - 1) / part_tokens : 1;
@@ -198,16 +205,17 @@ int plan(int64_t units, int max_context_len, int sm_count, int resident, int blo
     if (units >= sm_count && max_context_len <= 8192) return 1;
     const int64_t slots = (int64_t)sm_count * (resident > 0 ? resident : 1);
     const int64_t L = max_context_len;
+    const int64_t align = block_size < 16 ? 16 : block_size;  // pieces hold whole chunks and blocks
     const int n_max = (int)std::min<int64_t>((L + min_piece - 1) / min_piece, 1024);
     int64_t best = INT64_MAX;
     for (int n = 2; n <= n_max; ++n) {
-        const int64_t piece = std::max<int64_t>(min_piece, ((L + n - 1) / n + block_size - 1) / block_size * block_size);
+        const int64_t piece = std::max<int64_t>(min_piece, ((L + n - 1) / n + align - 1) / align * align);
         const int64_t ctas = units * ((L + piece - 1) / piece);
         best = std::min(best, (ctas + slots - 1) / slots * (piece + 64));
     }
     int chosen = min_piece;
     for (int n = 2; n <= n_max; ++n) {
-        const int64_t piece = std::max<int64_t>(min_piece, ((L + n - 1) / n + block_size - 1) / block_size * block_size);
+        const int64_t piece = std::max<int64_t>(min_piece, ((L + n - 1) / n + align - 1) / align * align);
         const int64_t ctas = units * ((L + piece - 1) / piece);
         if ((ctas + slots - 1) / slots * (piece + 64) * 50 <= best * 51) {
             chosen = (int)piece;
@@ -421,7 +429,7 @@ int pa_prefill_chunk(void* out, const void* q, const void* k_cache, const void* 
     p.n_kv_heads = n_kv_heads;
     p.max_blocks_per_seq = max_blocks_per_seq;
     p.num_blocks = (int)num_blocks;
-    p.cpb_log2 = block_size == 16 ? 0 : block_size == 32 ? 1 : block_size == 64 ? 2 : 3;
+    p.cpb_log2 = cpb_log2_of(block_size);
     p.tiles_per_chunk = (int)(((int64_t)max_q_len * G + 127) / 128);
     p.qk_scale_log2 = scale * 1.4426950408889634f;
     if ((int64_t)p.tiles_per_chunk * num_chunks * n_kv_heads > INT32_MAX) return PA_ERR_UNSUPPORTED;

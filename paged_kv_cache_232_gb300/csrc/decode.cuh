@@ -43,7 +43,7 @@ struct DecodeParams {
     int part_tokens;           // 0: whole context in one CTA
     int max_parts;             // P (grid pieces per (s, g))
     int num_blocks;
-    int cpb_log2;              // log2 of the 16-token chunks per cache block (block_size / 16)
+    int cpb_log2;              // log2 of the 16-token chunks per cache block; -1: blocks of 8 tokens
     float qk_scale_log2;       // scale * log2(e)
 };
 
@@ -160,7 +160,7 @@ decode_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmK, con
 
     // context length, clamped to what the table (and the split-K grid) can address
     int L = __ldg(p.context_lens + s);
-    int cap = (p.max_blocks_per_seq * C::BS) << p.cpb_log2;  // tokens the table row addresses
+    int cap = table_row_tokens(p.max_blocks_per_seq, p.cpb_log2);  // tokens the table row addresses
     if (p.part_tokens > 0 && p.max_parts * p.part_tokens < cap) cap = p.max_parts * p.part_tokens;
     if (L < 0 || L > cap) {
         if (piece == 0 && g == 0 && threadIdx.x == 0) flag_error(p.err, PA_DEVERR_LENGTH);
@@ -190,38 +190,51 @@ decode_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmK, con
             tma_prefetch_desc(&tmV);
         }
         const uint64_t pol = l2_policy_evict_first();
-        // 16-token chunk c of the sequence: table entry c >> cpb_log2, rows 16 (c mod 2^cpb_log2) + 0..15
+        // 16-token chunk c of the sequence: table entry c >> cpb_log2, rows 16 (c mod 2^cpb_log2) + 0..15;
+        // with blocks of 8 tokens, entries 2c and 2c + 1 (the second only if the context reaches it),
+        // each an 8-row box, the second landing 8 rows (1 KB) further
         const int32_t* bt = p.block_tables + (size_t)s * p.max_blocks_per_seq;
+        const bool half8 = p.cpb_log2 < 0;
+        const int per_load = half8 ? 16 : 32;  // chunks whose table entries one warp-wide load covers
         bool ok = true;
         int n_issued = 0;  // blocks whose loads were issued
-        for (int b0 = 0; b0 < nblk && ok; b0 += 32) {
-            int my = 0;
-            if (b0 + lane < nblk) {
-                my = __ldg(bt + ((blk0 + b0 + lane) >> p.cpb_log2));
+        for (int b0 = 0; b0 < nblk && ok; b0 += per_load) {
+            const int nb = min(per_load, nblk - b0);
+            int my = p.num_blocks;  // outside the tensor map: TMA fills zeros
+            const int e = half8 ? 2 * (blk0 + b0) + lane : (blk0 + b0 + lane) >> p.cpb_log2;
+            if (half8 ? (lane < 2 * nb && 8 * e < L) : (lane < nb)) {
+                my = __ldg(bt + e);
                 if (my < 0 || my >= p.num_blocks) {
                     flag_error(p.err, PA_DEVERR_BLOCK);
-                    my = p.num_blocks;  // outside the tensor map: TMA fills zeros
+                    my = p.num_blocks;
                 }
             }
-            const int nb = min(32, nblk - b0);
             for (int j = 0; j < nb; ++j) {
-                const int blk = __shfl_sync(0xffffffffu, my, j);
+                const int blk = __shfl_sync(0xffffffffu, my, half8 ? 2 * j : j);
+                const int blk_b = __shfl_sync(0xffffffffu, my, (2 * j + 1) & 31);  // half8 only
                 const int b = b0 + j;
                 const int st = b % C::NST;
                 const uint32_t ph = (b / C::NST) & 1;
                 if (lane == 0) {
-                    const int row0 = ((blk0 + b) & ((1 << p.cpb_log2) - 1)) * C::BS;  // chunk's first row in its block
+                    // chunk's first row in its block
+                    const int row0 = half8 ? 0 : ((blk0 + b) & ((1 << p.cpb_log2) - 1)) * C::BS;
                     if (b >= C::NST && !mbar_wait(bar_empty + 8 * st, ph ^ 1, p.err)) ok = false;
                     if (ok) {
                         const uint32_t dst = ring + st * C::STAGE_BYTES;
                         mbar_arrive_expect_tx(bar_full + 8 * st, C::STAGE_BYTES);
 #pragma unroll
-                        for (int hf = 0; hf < C::HALVES; ++hf)
-                            tma_load_4d(dst + hf * C::SLAB_BYTES, &tmK, hf * 64, g, row0, blk, bar_full + 8 * st, pol);
+                        for (int kv = 0; kv < 2; ++kv) {
+                            const CUtensorMap* map = kv ? &tmV : &tmK;
+                            const uint32_t tile = dst + kv * C::TILE_BYTES;
 #pragma unroll
-                        for (int hf = 0; hf < C::HALVES; ++hf)
-                            tma_load_4d(dst + C::TILE_BYTES + hf * C::SLAB_BYTES, &tmV, hf * 64, g, row0, blk,
-                                        bar_full + 8 * st, pol);
+                            for (int hf = 0; hf < C::HALVES; ++hf) {
+                                tma_load_4d(tile + hf * C::SLAB_BYTES, map, hf * 64, g, row0, blk, bar_full + 8 * st,
+                                            pol);
+                                if (half8)
+                                    tma_load_4d(tile + hf * C::SLAB_BYTES + 8 * 128, map, hf * 64, g, 0, blk_b,
+                                                bar_full + 8 * st, pol);
+                            }
+                        }
                     }
                 }
                 ok = __shfl_sync(0xffffffffu, ok, 0);
@@ -459,7 +472,7 @@ __global__ void __launch_bounds__(256) splitk_reduce_kernel(const DecodeParams p
     const int row = blockIdx.x;          // s * Hq + h
     const int s = row / p.n_q_heads;
     int L = __ldg(p.context_lens + s);
-    const int cap = min((p.max_blocks_per_seq * 16) << p.cpb_log2, p.max_parts * p.part_tokens);
+    const int cap = min(table_row_tokens(p.max_blocks_per_seq, p.cpb_log2), p.max_parts * p.part_tokens);
     L = L < 0 ? 0 : (L > cap ? cap : L);
     const int n_parts = (L + p.part_tokens - 1) / p.part_tokens;
     if (n_parts <= 1) return;  // written directly by the piece kernel

@@ -26,6 +26,13 @@ __device__ __forceinline__ void flag_error(unsigned* err, unsigned bit) {
     if (err) atomicOr(err, bit);
 }
 
+// Cache blocks are read in 16-token chunks.  cpb_log2 >= 0: a block holds 2^cpb_log2 chunks
+// (block_size 16 << cpb_log2); cpb_log2 == -1: blocks of 8 tokens, two table entries per chunk.
+// Tokens a block-table row of mb entries addresses:
+__host__ __device__ __forceinline__ int table_row_tokens(int mb, int cpb_log2) {
+    return cpb_log2 < 0 ? mb * 8 : (mb * 16) << cpb_log2;
+}
+
 __device__ __forceinline__ uint32_t smem_addr(const void* p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }

@@ -102,7 +102,7 @@ template <int SPAN>
 __device__ __forceinline__ int lpt_unit(const PrefillParams& p, unsigned char* scratch) {
     const int C = p.num_chunks, per_unit = C * p.n_kv_heads;
     const int U = p.tiles_per_chunk * per_unit;
-    const int cap = (p.max_blocks_per_seq * 16) << p.cpb_log2;
+    const int cap = table_row_tokens(p.max_blocks_per_seq, p.cpb_log2);
     const int ncost = cap / pf::BN + 2;
     int* qsl = reinterpret_cast<int*>(scratch);
     int* kvl = qsl + C + 1;
@@ -297,7 +297,7 @@ prefill_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmK, c
     const int q0 = p.lpt ? sched[c] : __ldg(p.query_start_loc + c);
     const int q_len = (p.lpt ? sched[c + 1] : __ldg(p.query_start_loc + c + 1)) - q0;
     const int kv_len = p.lpt ? sched[p.num_chunks + 1 + c] : __ldg(p.seq_lens + c);
-    if (q_len < 0 || kv_len < q_len || kv_len > ((p.max_blocks_per_seq * 16) << p.cpb_log2)) {
+    if (q_len < 0 || kv_len < q_len || kv_len > table_row_tokens(p.max_blocks_per_seq, p.cpb_log2)) {
         if (unit == 0 && g == 0 && threadIdx.x == 0) flag_error(p.err, PA_DEVERR_LENGTH);
         return;
     }
@@ -440,14 +440,16 @@ prefill_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmK, c
         const int32_t* bt = p.block_tables + (size_t)c * p.max_blocks_per_seq;
         const uint32_t full0 = bars + 8 * (kv ? V_FULL : K_FULL), empty0 = bars + 8 * (kv ? V_EMPTY : K_EMPTY);
         const uint32_t dst_base = kv ? sV : sK;
+        const bool half8 = p.cpb_log2 < 0;  // blocks of 8 tokens
         bool ok = true;
         for (int i = 0; i < n_max && ok; ++i) {
             const int st = i & 1;
             const uint32_t ph = (i >> 1) & 1;
+            // 16-token chunk b: table entry b >> cpb_log2; blocks of 8 tokens: one entry per 8 rows
             int my = p.num_blocks;  // past the sequence (or invalid): out-of-range coordinate, zero fill
-            const int b = i * 8 + (lane & 7);
-            if (lane < 8 && b < nblk_seq) {  // 16-token chunk b: table entry b >> cpb_log2
-                my = __ldg(bt + (b >> p.cpb_log2));
+            const int e = half8 ? i * 16 + lane : (i * 8 + (lane & 7)) >> p.cpb_log2;
+            if (half8 ? (lane < 16 && 8 * e < kv_len) : (lane < 8 && i * 8 + lane < nblk_seq)) {
+                my = __ldg(bt + e);
                 if (my < 0 || my >= p.num_blocks) {
                     if (kv == 0) flag_error(p.err, PA_DEVERR_BLOCK);
                     my = p.num_blocks;
@@ -463,13 +465,19 @@ prefill_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmK, c
             const uint32_t dst0 = dst_base + st * TILE;
             if (lane == 0) mbar_arrive_expect_tx(full, TILE);
             __syncwarp();
-            {
-                // lanes 0 .. 8 SLABS - 1 each issue one box: block lane % 8, 64-column slab lane / 8
+            if (!half8) {
+                // lanes 0 .. 8 SLABS - 1 each issue one box: chunk lane % 8, 64-column slab lane / 8
                 const int blk = __shfl_sync(0xffffffffu, my, lane & 7);
                 const int sl = lane >> 3;
                 const int row0 = ((i * 8 + (lane & 7)) & ((1 << p.cpb_log2) - 1)) * 16;  // chunk's first row
                 if (lane < 8 * SLABS)
                     tma_load_4d(dst0 + sl * SLAB + (lane & 7) * 2048, map, sl * 64, g, row0, blk, full, pol);
+            } else {
+                // lanes 0 .. 16 SLABS - 1: 8-row block lane % 16, slab lane / 16
+                const int blk = __shfl_sync(0xffffffffu, my, lane & 15);
+                const int sl = lane >> 4;
+                if (lane < 16 * SLABS)
+                    tma_load_4d(dst0 + sl * SLAB + (lane & 15) * 1024, map, sl * 64, g, 0, blk, full, pol);
             }
             if (kv == 1 && i == n_max - 1) {
                 // Rows of the sequence's last, partial block past kv_len may hold anything (P
@@ -595,7 +603,7 @@ static cudaError_t launch_prefill_t(const PrefillParams& p, const CUtensorMap& t
     const int units = (p.tiles_per_chunk + pf::NQT - 1) / pf::NQT;
     PrefillParams q = p;
     q.tiles_per_chunk = units;
-    const int ncost = ((p.max_blocks_per_seq * 16) << p.cpb_log2) / pf::BN + 2;
+    const int ncost = table_row_tokens(p.max_blocks_per_seq, p.cpb_log2) / pf::BN + 2;
     const long sched_words = 2L * p.num_chunks + 1 + ncost + 3 + pf::THREADS / 32;
     q.lpt = (sched_words * 4 <= pf::SCHED_BYTES) ? 1 : 0;
     const int grid = units * p.num_chunks * p.n_kv_heads;

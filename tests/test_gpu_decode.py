@@ -218,11 +218,14 @@ def test_zero_length_context_gives_zeros():
         assert np.all(got[0] == 0)
 
 
-@pytest.mark.parametrize("bs", [32, 64, 128])
-@pytest.mark.parametrize("mode,part", [("v1", 0), ("splitk", 0), ("splitk", 512)])
+@pytest.mark.parametrize("bs", [8, 32, 64, 128])
+@pytest.mark.parametrize("mode,part", [("v1", 0), ("splitk", 0), ("splitk", 512), ("splitk", 48)])
 def test_decode_block_sizes(bs, mode, part):
-    """Cache blocks of 32 / 64 / 128 tokens: 16-token chunks are read from their rows inside the
-    block (lengths straddling block and chunk boundaries, NaN in every unowned slot)."""
+    """Cache blocks of 8 / 32 / 64 / 128 tokens: 16-token chunks are read from their rows inside
+    the block, or from two 8-token blocks (lengths straddling block and chunk boundaries, NaN in
+    every unowned slot and in the poison block padding the tables)."""
+    if part % max(bs, 16):
+        pytest.skip("split-K pieces hold whole blocks")
     lens = [1, 15, 16, 17, bs - 1, bs, bs + 1, 3 * bs + 5, 2000]
     for dt, hq, hkv, d in [(wl.BF16, 16, 8, 128), (wl.F16, 8, 2, 64)]:
         w = wl.build_workload("bs", 900 + bs + d, dtype=dt, n_q_heads=hq, n_kv_heads=hkv, head_dim=d, block_size=bs,

@@ -52,6 +52,12 @@ def test_write_shapes_and_ragged_counts(n, hkv, d, dt):
     assert assert_write_matches_oracle(w) == 0
 
 
+@pytest.mark.parametrize("bs", [8, 32, 128])
+def test_write_block_sizes(bs):
+    w = wl.write_rows_case(2000 + bs, 777, n_kv_heads=4, head_dim=128, block_size=bs, pad_frac=0.2, nan_canaries=True)
+    assert assert_write_matches_oracle(w) == 0
+
+
 def test_write_all_padded_changes_nothing():
     w = wl.write_rows_case(5, 64)
     sm = np.full(64, -1, dtype=np.int64)

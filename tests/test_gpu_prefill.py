@@ -191,7 +191,7 @@ def test_unified_mixed_batch_single_launch():
     check(got[S:][rows], oracle_rows(w, rows), p.dtype, "unified: prefill rows")
 
 
-@pytest.mark.parametrize("bs", [32, 64])
+@pytest.mark.parametrize("bs", [8, 32, 64])
 @pytest.mark.parametrize("d", [128, 64])
 def test_prefill_block_sizes(bs, d):
     w = wl.build_workload("pfbs", 950 + bs + d, dtype=wl.BF16, n_q_heads=16, n_kv_heads=8, head_dim=d, block_size=bs,
@@ -202,8 +202,9 @@ def test_prefill_block_sizes(bs, d):
     assert pa.pa_device_errors(clear=True) == 0
 
 
-def test_write_then_decode_block_size_32():
-    w = wl.build_workload("wbs", 977, dtype=wl.BF16, n_q_heads=16, n_kv_heads=8, head_dim=128, block_size=32,
+@pytest.mark.parametrize("bs", [8, 32])
+def test_write_then_decode_block_sizes(bs):
+    w = wl.build_workload("wbs", 977 + bs, dtype=wl.BF16, n_q_heads=16, n_kv_heads=8, head_dim=128, block_size=bs,
                           decode_lens=[33, 64, 65, 500], write_rows=True, extra_blocks=2)
     p, b, wr = w.pool, w.decode, w.write
     kc, vc = to_dev(p.k_cache, p.dtype), to_dev(p.v_cache, p.dtype)
@@ -213,8 +214,8 @@ def test_write_then_decode_block_size_32():
     pa.pa_decode_v1(out, q, kc, vc, to_dev_i(b.block_tables, torch.int32), to_dev_i(b.context_lens, torch.int32),
                     b.scale)
     torch.cuda.synchronize()
-    k2, v2, _ = oracle.kv_write(p.k_cache, p.v_cache, wr.key, wr.value, wr.slot_mapping, 32)
+    k2, v2, _ = oracle.kv_write(p.k_cache, p.v_cache, wr.key, wr.value, wr.slot_mapping, bs)
     assert np.array_equal(bits_of(kc), k2) and np.array_equal(bits_of(vc), v2)
     ex = oracle.decode(b.q, k2, v2, b.block_tables, b.context_lens, b.scale, p.dtype)
     cd = oracle.decode(b.q, k2, abs_bits(v2), b.block_tables, b.context_lens, b.scale, p.dtype)
-    check_attention(bits_of(out), ex, p.dtype, "bs 32 write + decode", cond=cd)
+    check_attention(bits_of(out), ex, p.dtype, f"bs {bs} write + decode", cond=cd)
