@@ -15,7 +15,8 @@
  *    block_tables[seq][t / block_size], offset t % block_size (MiniLLM Runtime,
  *    "Core class relationships": logical token -> logical block + offset ->
  *    block_table -> physical address).
- *  - Supported shapes: block_size 8, 16, 32, 64 or 128; head_dim 64 or 128; n_q_heads a multiple
+ *  - Supported shapes: block_size 8, 16, 32, 64 or 128; head_dim 64, 96 or 128 (96 runs in the
+ *    128-column kernels with the extra columns zero); n_q_heads a multiple
  *    of n_kv_heads with group size G = n_q_heads / n_kv_heads in {1, 2, 4, 8};
  *    query head h reads KV head h / G.
  *  - stream is a cudaStream_t (NULL = legacy default stream).  Calls only
@@ -115,7 +116,7 @@ int pa_rope_table(float* out, int64_t max_position, int head_dim, double theta);
  *  positions    [num_tokens] int64 in [0, max_position); a row outside is left untouched (q
  *               and cache) and sets PA_DEVERR_POSITION
  *  cos_sin      [max_position, head_dim] float32, device copy of pa_rope_table's output
- *  head_dim 64 or 128; n_q_heads >= 0 (ignored when q is NULL).  num_tokens == 0 launches
+ *  head_dim 64, 96 or 128; n_q_heads >= 0 (ignored when q is NULL).  num_tokens == 0 launches
  *  nothing and returns PA_OK.
  */
 int pa_rope_reshape_and_cache(void* q, const void* key, const void* value, void* k_cache, void* v_cache,
@@ -233,7 +234,7 @@ int pa_decode_splitk_static(void* out, const void* q, const void* k_cache, const
 
 /*
  * pa_prefill_chunk -- attention for ragged prefill chunks that attend to their
- * earlier cached context, on the tcgen05 tensor cores (head_dim 64 or 128).
+ * earlier cached context, on the tcgen05 tensor cores (head_dim 64, 96 or 128).
  * Source: mini_engine, "Custom CUDA kernels" (paged prefill attention: tiled,
  * online softmax, K/V read from the paged pool itself, ragged batches, prefix
  * hits and chunks over earlier chunks in one launch); miniserve, "Engine"

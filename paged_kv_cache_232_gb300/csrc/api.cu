@@ -84,12 +84,16 @@ int check_heads(int n_q_heads, int n_kv_heads, int head_dim, int block_size, int
     if (n_q_heads <= 0 || n_kv_heads <= 0 || n_q_heads % n_kv_heads) return PA_ERR_SHAPE;
     const int G = n_q_heads / n_kv_heads;
     if (G != 1 && G != 2 && G != 4 && G != 8) return PA_ERR_UNSUPPORTED;
-    if (head_dim != 64 && head_dim != 128) return PA_ERR_UNSUPPORTED;
+    if (head_dim != 64 && head_dim != 96 && head_dim != 128) return PA_ERR_UNSUPPORTED;
     if (block_size != 8 && block_size != 16 && block_size != 32 && block_size != 64 && block_size != 128)
         return PA_ERR_UNSUPPORTED;
     if (dtype != PA_F16 && dtype != PA_BF16) return PA_ERR_UNSUPPORTED;
     return PA_OK;
 }
+
+// head_dim the attention kernels are instantiated for: 96 runs in the 128-column kernels, the
+// columns past 96 zero (the tensor maps fill them, q loads and output stores skip them)
+int kernel_dim(int head_dim) { return head_dim == 96 ? 128 : head_dim; }
 
 // log2 of the 16-token chunks per cache block; -1 for blocks of 8 tokens (two per chunk)
 int cpb_log2_of(int block_size) {
@@ -153,6 +157,7 @@ int decode_impl(void* out, const void* q, const void* k_cache, const void* v_cac
     p.num_blocks = (int)num_blocks;
     p.cpb_log2 = cpb_log2_of(block_size);
     p.qk_scale_log2 = scale * 1.4426950408889634f;
+    p.hd = head_dim;
     const int units = num_seqs * n_kv_heads;
     int grid = units;
     bool reduce = false;
@@ -162,7 +167,7 @@ int decode_impl(void* out, const void* q, const void* k_cache, const void* v_cac
             return PA_ERR_BOUNDS;
         const int max_parts = max_context_len > 0 ? (max_context_len + part_tokens - 1) / part_tokens : 1;
         if ((int64_t)units * max_parts > INT32_MAX) return PA_ERR_UNSUPPORTED;
-        const WsLayout w = ws_layout(num_seqs, n_q_heads, head_dim, max_parts);
+        const WsLayout w = ws_layout(num_seqs, n_q_heads, kernel_dim(head_dim), max_parts);
         if (max_parts > 1) {
             if (!workspace || workspace_bytes < w.total) return PA_ERR_WORKSPACE;
             if (!aligned16(workspace)) return PA_ERR_ALIGN;
@@ -182,7 +187,7 @@ int decode_impl(void* out, const void* q, const void* k_cache, const void* v_cac
     CUtensorMap tk, tv;
     if ((st = encode_cache_map(&tk, k_cache, dtype, num_blocks, block_size, n_kv_heads, head_dim)) != PA_OK) return st;
     if ((st = encode_cache_map(&tv, v_cache, dtype, num_blocks, block_size, n_kv_heads, head_dim)) != PA_OK) return st;
-    cudaError_t e = pa::launch_decode(dtype == PA_BF16, head_dim, n_q_heads / n_kv_heads, p, tk, tv, grid, reduce,
+    cudaError_t e = pa::launch_decode(dtype == PA_BF16, kernel_dim(head_dim), n_q_heads / n_kv_heads, p, tk, tv, grid, reduce,
                                       stream);
     return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
@@ -308,7 +313,7 @@ int pa_rope_reshape_and_cache(void* q, const void* key, const void* value, void*
         max_position <= 0 || (q && n_q_heads <= 0))
         return PA_ERR_SHAPE;
     if (dtype != PA_F16 && dtype != PA_BF16) return PA_ERR_UNSUPPORTED;
-    if (head_dim != 64 && head_dim != 128) return PA_ERR_UNSUPPORTED;
+    if (head_dim != 64 && head_dim != 96 && head_dim != 128) return PA_ERR_UNSUPPORTED;
     if (num_tokens == 0) return PA_OK;
     if (!key || !value || !k_cache || !v_cache || !slot_mapping || !positions || !cos_sin) return PA_ERR_NULL;
     if (!aligned16(key) || !aligned16(value) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(cos_sin) ||
@@ -331,13 +336,18 @@ int pa_rope_reshape_and_cache(void* q, const void* key, const void* value, void*
             static_cast<uint4*>(k_cache), static_cast<uint4*>(v_cache), slot_mapping, positions, cos_sin, num_tokens,
             n_q_heads, n_kv_heads, num_blocks * block_size, max_position, dev->err);
     };
-    const bool bf = dtype == PA_BF16, d128 = head_dim == 128;
+    const bool bf = dtype == PA_BF16;
+    auto by_dim = [&](auto k64, auto k96, auto k128) {
+        if (head_dim == 128) launch(k128);
+        else if (head_dim == 96) launch(k96);
+        else launch(k64);
+    };
     if (rows == 2) {
-        if (bf) d128 ? launch(pa::rope_write_kernel<true, 128, 2>) : launch(pa::rope_write_kernel<true, 64, 2>);
-        else d128 ? launch(pa::rope_write_kernel<false, 128, 2>) : launch(pa::rope_write_kernel<false, 64, 2>);
+        if (bf) by_dim(pa::rope_write_kernel<true, 64, 2>, pa::rope_write_kernel<true, 96, 2>, pa::rope_write_kernel<true, 128, 2>);
+        else by_dim(pa::rope_write_kernel<false, 64, 2>, pa::rope_write_kernel<false, 96, 2>, pa::rope_write_kernel<false, 128, 2>);
     } else {
-        if (bf) d128 ? launch(pa::rope_write_kernel<true, 128, 1>) : launch(pa::rope_write_kernel<true, 64, 1>);
-        else d128 ? launch(pa::rope_write_kernel<false, 128, 1>) : launch(pa::rope_write_kernel<false, 64, 1>);
+        if (bf) by_dim(pa::rope_write_kernel<true, 64, 1>, pa::rope_write_kernel<true, 96, 1>, pa::rope_write_kernel<true, 128, 1>);
+        else by_dim(pa::rope_write_kernel<false, 64, 1>, pa::rope_write_kernel<false, 96, 1>, pa::rope_write_kernel<false, 128, 1>);
     }
     return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
@@ -348,7 +358,7 @@ size_t pa_decode_workspace_size(int num_seqs, int n_q_heads, int head_dim, int m
     const int part = partition_or_default(partition_tokens);
     const int max_parts = max_context_len > 0 ? (max_context_len + part - 1) / part : 1;
     if (max_parts <= 1) return 0;
-    return ws_layout(num_seqs, n_q_heads, head_dim, max_parts).total;
+    return ws_layout(num_seqs, n_q_heads, kernel_dim(head_dim), max_parts).total;
 }
 
 int pa_decode_plan(int num_seqs, int n_q_heads, int n_kv_heads, int head_dim, int block_size, int max_context_len,
@@ -358,7 +368,7 @@ int pa_decode_plan(int num_seqs, int n_q_heads, int n_kv_heads, int head_dim, in
     if (st != PA_OK) return st;
     DeviceState* dev = nullptr;
     if ((st = device_state(&dev)) != PA_OK) return st;
-    const int resident = pa::decode_resident_ctas(dtype == PA_BF16, head_dim, n_q_heads / n_kv_heads);
+    const int resident = pa::decode_resident_ctas(dtype == PA_BF16, kernel_dim(head_dim), n_q_heads / n_kv_heads);
     if (resident <= 0) return PA_ERR_CUDA;
     return plan((int64_t)num_seqs * n_kv_heads, max_context_len, dev->sm_count, resident, block_size,
                 partition_tokens);
@@ -432,11 +442,12 @@ int pa_prefill_chunk(void* out, const void* q, const void* k_cache, const void* 
     p.cpb_log2 = cpb_log2_of(block_size);
     p.tiles_per_chunk = (int)(((int64_t)max_q_len * G + 127) / 128);
     p.qk_scale_log2 = scale * 1.4426950408889634f;
+    p.hd = head_dim;
     if ((int64_t)p.tiles_per_chunk * num_chunks * n_kv_heads > INT32_MAX) return PA_ERR_UNSUPPORTED;
     CUtensorMap tk, tv;
     if ((st = encode_cache_map(&tk, k_cache, dtype, num_blocks, block_size, n_kv_heads, head_dim)) != PA_OK) return st;
     if ((st = encode_cache_map(&tv, v_cache, dtype, num_blocks, block_size, n_kv_heads, head_dim)) != PA_OK) return st;
-    cudaError_t e = pa::launch_prefill(dtype == PA_BF16, head_dim, G, p, tk, tv, static_cast<cudaStream_t>(stream));
+    cudaError_t e = pa::launch_prefill(dtype == PA_BF16, kernel_dim(head_dim), G, p, tk, tv, static_cast<cudaStream_t>(stream));
     if (e == cudaErrorNotSupported) return PA_ERR_UNSUPPORTED;
     return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }

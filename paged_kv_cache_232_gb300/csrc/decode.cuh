@@ -31,8 +31,8 @@
 namespace pa {
 
 struct DecodeParams {
-    void* out;                 // [S, Hq, D] T
-    const void* q;             // [S, Hq, D] T
+    void* out;                 // [S, Hq, hd] T
+    const void* q;             // [S, Hq, hd] T
     const int32_t* block_tables;
     const int32_t* context_lens;
     float* ws_m;               // [S, Hq, P]   (split-K only)
@@ -45,6 +45,7 @@ struct DecodeParams {
     int num_blocks;
     int cpb_log2;              // log2 of the 16-token chunks per cache block; -1: blocks of 8 tokens
     float qk_scale_log2;       // scale * log2(e)
+    int hd;                    // head_dim of q, out and the cache (<= D; columns hd .. D-1 are zero)
 };
 
 template <int D, int G, bool BF16>
@@ -269,12 +270,12 @@ decode_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmK, con
         chunk_col[j] = half * 64 + c * 8;
     }
     {
-        const uint16_t* qrow = static_cast<const uint16_t*>(p.q) + ((size_t)s * p.n_q_heads + (size_t)g * G) * D;
+        const uint16_t* qrow = static_cast<const uint16_t*>(p.q) + ((size_t)s * p.n_q_heads + (size_t)g * G) * p.hd;
 #pragma unroll
         for (int h = 0; h < G; ++h)
 #pragma unroll
             for (int j = 0; j < C::CPL; ++j) {
-                uint4 raw = ldg_nc_128(qrow + h * D + chunk_col[j]);
+                uint4 raw = chunk_col[j] < p.hd ? ldg_nc_128(qrow + h * p.hd + chunk_col[j]) : make_uint4(0u, 0u, 0u, 0u);
                 unpack8<BF16>(raw, qf[h][j]);
 #pragma unroll
                 for (int e = 0; e < 8; ++e) qf[h][j][e] *= p.qk_scale_log2;
@@ -449,7 +450,7 @@ decode_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmK, con
         const size_t row = (size_t)s * p.n_q_heads + hq0 + h;
         if (direct) {
             uint32_t packed = F::pack_rn(o0 * inv, o1 * inv);
-            *reinterpret_cast<uint32_t*>(static_cast<uint16_t*>(p.out) + row * D + d) = packed;
+            if (d < p.hd) *reinterpret_cast<uint32_t*>(static_cast<uint16_t*>(p.out) + row * p.hd + d) = packed;
         } else {
             const size_t pr = row * p.max_parts + piece;
             *reinterpret_cast<float2*>(p.ws_o + pr * D + d) = make_float2(o0 * inv, o1 * inv);
@@ -541,7 +542,7 @@ __global__ void __launch_bounds__(256) splitk_reduce_kernel(const DecodeParams p
         *reinterpret_cast<float4*>(acc + warp * D + lane * 4) = a;
     }
     __syncthreads();
-    if (tid < D / 2) {
+    if (2 * tid < p.hd) {
         const int d = 2 * tid;
         float s0 = 0.f, s1 = 0.f;
 #pragma unroll
@@ -550,7 +551,7 @@ __global__ void __launch_bounds__(256) splitk_reduce_kernel(const DecodeParams p
             s1 += acc[w * D + d + 1];
         }
         const float inv = (Wsh > 0.f) ? 1.f / Wsh : 0.f;
-        *reinterpret_cast<uint32_t*>(static_cast<uint16_t*>(p.out) + (size_t)row * D + d) = F::pack_rn(s0 * inv, s1 * inv);
+        *reinterpret_cast<uint32_t*>(static_cast<uint16_t*>(p.out) + (size_t)row * p.hd + d) = F::pack_rn(s0 * inv, s1 * inv);
     }
 }
 

@@ -36,8 +36,8 @@ cudaError_t launch_decode(int bf16, int head_dim, int group, const DecodeParams&
                           const CUtensorMap& tmV, int grid, bool with_reduce, cudaStream_t stream);
 
 struct PrefillParams {
-    void* out;                  // [total_q, Hq, D]
-    const void* q;              // [total_q, Hq, D]
+    void* out;                  // [total_q, Hq, hd]
+    const void* q;              // [total_q, Hq, hd]
     const int32_t* block_tables;
     const int32_t* query_start_loc;
     const int32_t* seq_lens;
@@ -47,6 +47,7 @@ struct PrefillParams {
     int cpb_log2;               // log2 of the 16-token chunks per cache block; -1: blocks of 8 tokens
     int lpt;                    // 1: CTAs take units longest-first (schedule fits in shared memory)
     float qk_scale_log2;
+    int hd;                     // head_dim of q, out and the cache (<= D; columns hd .. D-1 are zero)
 };
 
 cudaError_t launch_prefill(int bf16, int head_dim, int group, const PrefillParams& params, const CUtensorMap& tmK,

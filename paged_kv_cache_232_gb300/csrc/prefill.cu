@@ -367,9 +367,9 @@ prefill_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmK, c
             for (int i = 0; i < CPR; ++i) {
                 const int R = (warp & 3) * 32 + RPI * i + lane / CPR;
                 const int tok = jt0 + R / G;
-                const uint16_t* src =
-                    static_cast<const uint16_t*>(p.q) + ((size_t)(q0 + tok) * p.n_q_heads + g * G + R % G) * D + ch * 8;
-                v[i] = (tok < q_len) ? ldg_nc_128(src) : make_uint4(0u, 0u, 0u, 0u);
+                const uint16_t* src = static_cast<const uint16_t*>(p.q) +
+                                      ((size_t)(q0 + tok) * p.n_q_heads + g * G + R % G) * p.hd + ch * 8;
+                v[i] = (tok < q_len && ch * 8 < p.hd) ? ldg_nc_128(src) : make_uint4(0u, 0u, 0u, 0u);
             }
 #pragma unroll
             for (int i = 0; i < CPR; ++i) {
@@ -380,7 +380,7 @@ prefill_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmK, c
             mbar_arrive(bars + 8 * Q_FULL);
         }
         // this row's output, formed before the loop so that only the pointer stays live across it
-        uint16_t* const dst = static_cast<uint16_t*>(p.out) + ((size_t)(q0 + jr) * p.n_q_heads + hr) * D;
+        uint16_t* const dst = static_cast<uint16_t*>(p.out) + ((size_t)(q0 + jr) * p.n_q_heads + hr) * p.hd;
         const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
         const uint32_t tS = tmem + lane_base + (uint32_t)(t * 128);
         const uint32_t tO = tmem + lane_base + O_COL + (uint32_t)(t * D);
@@ -414,7 +414,7 @@ prefill_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmK, c
                 uint32_t o[32];
                 tc::ld32(tO + 32 * q, o);
                 tc::wait_ld();
-                if (row_valid) {
+                if (row_valid && 32 * q < p.hd) {
 #pragma unroll
                     for (int v = 0; v < 4; ++v) {
                         uint4 w;

@@ -51,7 +51,7 @@ def test_validation_rejects_before_any_device_work(lib):
     # n_q_heads not a multiple of n_kv_heads
     assert lib.pa_decode_v1(vp, vp, vp, vp, vp, 8, vp, 1, 6, 4, 128, 16, 10, 0.1, 1, None) == -2
     # unsupported head_dim / block_size / dtype / group size
-    assert lib.pa_decode_v1(vp, vp, vp, vp, vp, 8, vp, 1, 8, 8, 96, 16, 10, 0.1, 1, None) == -3
+    assert lib.pa_decode_v1(vp, vp, vp, vp, vp, 8, vp, 1, 8, 8, 80, 16, 10, 0.1, 1, None) == -3
     assert lib.pa_decode_v1(vp, vp, vp, vp, vp, 8, vp, 1, 8, 8, 128, 24, 10, 0.1, 1, None) == -3
     assert lib.pa_decode_v1(vp, vp, vp, vp, vp, 8, vp, 1, 8, 8, 128, 16, 10, 0.1, 7, None) == -3
     assert lib.pa_decode_v1(vp, vp, vp, vp, vp, 8, vp, 1, 48, 3, 128, 16, 10, 0.1, 1, None) == -3
@@ -89,7 +89,7 @@ def test_rope_table_matches_the_formula_and_validates(lib):
 def test_rope_write_validation_rejects_before_any_device_work(lib):
     vp = ctypes.c_void_p(16)
     args = lambda q=vp, d=128, n=4, dt=1, mp=100: (q, vp, vp, vp, vp, vp, vp, vp, n, 16, 8, d, 16, 10, mp, dt, None)
-    assert lib.pa_rope_reshape_and_cache(*args(d=96)) == -3          # head_dim
+    assert lib.pa_rope_reshape_and_cache(*args(d=80)) == -3          # head_dim
     assert lib.pa_rope_reshape_and_cache(*args(dt=7)) == -3          # dtype
     assert lib.pa_rope_reshape_and_cache(*args(mp=0)) == -2          # empty table
     assert lib.pa_rope_reshape_and_cache(*args(n=0)) == 0            # nothing to do

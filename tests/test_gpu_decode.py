@@ -105,7 +105,7 @@ EDGE_LENS = [1, 15, 16, 17, 255, 256, 257, 513, 4097]
 
 @pytest.mark.parametrize("dt,hq,hkv,d", [(wl.BF16, 16, 8, 128), (wl.F16, 2, 2, 64), (wl.BF16, 32, 8, 128),
                                          (wl.F16, 8, 1, 128), (wl.BF16, 8, 2, 64), (wl.F16, 16, 4, 128),
-                                         (wl.BF16, 8, 1, 64)])
+                                         (wl.BF16, 8, 1, 64), (wl.BF16, 16, 8, 96), (wl.F16, 32, 4, 96)])
 @pytest.mark.parametrize("mode,part", [("v1", 0), ("splitk", 0), ("splitk", 64), ("splitk", 512), ("splitk", 48),
                                        ("splitk", 400)])
 def test_decode_edge_lengths(dt, hq, hkv, d, mode, part):

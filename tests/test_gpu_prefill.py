@@ -64,7 +64,8 @@ def check(got_bits, ref, dt, what):
 
 
 SHAPES = [(wl.BF16, 16, 8, 128), (wl.F16, 16, 8, 128), (wl.BF16, 8, 8, 128), (wl.BF16, 32, 8, 128),
-          (wl.F16, 16, 2, 128), (wl.BF16, 16, 8, 64), (wl.F16, 8, 8, 64), (wl.BF16, 32, 4, 64), (wl.F16, 2, 2, 64)]
+          (wl.F16, 16, 2, 128), (wl.BF16, 16, 8, 64), (wl.F16, 8, 8, 64), (wl.BF16, 32, 4, 64), (wl.F16, 2, 2, 64),
+          (wl.BF16, 16, 8, 96), (wl.F16, 8, 2, 96)]
 
 
 @pytest.mark.parametrize("dt,hq,hkv,d", SHAPES)
