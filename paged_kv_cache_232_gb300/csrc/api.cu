@@ -183,6 +183,12 @@ int decode_impl(void* out, const void* q, const void* k_cache, const void* v_cac
     } else {
         p.part_tokens = 0;
         p.max_parts = 1;
+        // longest-first order pays only when the grid is longer than one wave of resident CTAs,
+        // and needs its scratch (lengths + a chunk-count histogram) to fit in the ring
+        const int resident = pa::decode_resident_ctas(dtype == PA_BF16, kernel_dim(head_dim), n_q_heads / n_kv_heads);
+        const int64_t scratch = (int64_t)num_seqs + ((int64_t)max_blocks_per_seq * block_size + 15) / 16 + 2;
+        p.lpt = (resident > 0 && units > (int64_t)dev->sm_count * resident &&
+                 scratch * 4 <= pa::decode_ring_bytes(kernel_dim(head_dim))) ? 1 : 0;
     }
     CUtensorMap tk, tv;
     if ((st = encode_cache_map(&tk, k_cache, dtype, num_blocks, block_size, n_kv_heads, head_dim)) != PA_OK) return st;

@@ -46,7 +46,67 @@ struct DecodeParams {
     int cpb_log2;              // log2 of the 16-token chunks per cache block; -1: blocks of 8 tokens
     float qk_scale_log2;       // scale * log2(e)
     int hd;                    // head_dim of q, out and the cache (<= D; columns hd .. D-1 are zero)
+    int lpt;                   // one-pass grid only: CTAs take sequences longest first
 };
+
+// Longest-first order of the one-pass grid: sequences ranked by 16-token chunk count
+// (descending, ties by index); CTA b takes KV head b mod Hkv of the sequence at rank b / Hkv,
+// so the hardware's in-order CTA dispatch becomes longest-processing-time list scheduling and
+// the short sequences fill in behind.  Every CTA ranks the same lengths the same way.  scratch
+// (ints, S + cap/16 + 2 of them) is shared memory nothing else uses yet; all threads call this;
+// the result is valid in warp 0.
+__device__ __forceinline__ int seq_at_rank(const DecodeParams& p, int r, int* scratch) {
+    const int S = p.num_seqs, tid = threadIdx.x, lane = tid & 31;
+    const int cap = table_row_tokens(p.max_blocks_per_seq, p.cpb_log2);
+    const int nb = (cap + 15) / 16 + 1;
+    int* len = scratch;    // chunk count per sequence
+    int* hist = scratch + S;
+    for (int i = tid; i < nb; i += blockDim.x) hist[i] = 0;
+    for (int i = tid; i < S; i += blockDim.x) {
+        int L = __ldg(p.context_lens + i);
+        L = L < 0 ? 0 : min(L, cap);
+        len[i] = (L + 15) >> 4;
+    }
+    __syncthreads();
+    for (int i = tid; i < S; i += blockDim.x) atomicAdd(&hist[len[i]], 1);
+    __syncthreads();
+    if (tid >= 32) return 0;
+    // descending scan of the histogram: the chunk count holding rank r, and r's rank inside it
+    int want = 0, rank = 0, before = 0;
+    for (int top = nb - 1; top >= 0; top -= 32) {
+        const int k = top - lane;
+        const int v = (k >= 0) ? hist[k] : 0;
+        int incl = v;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += y;
+        }
+        const int start = before + incl - v;
+        const unsigned found = __ballot_sync(0xffffffffu, v > 0 && r >= start && r < start + v);
+        if (found) {
+            const int src = __ffs(found) - 1;
+            want = __shfl_sync(0xffffffffu, k, src);
+            rank = r - __shfl_sync(0xffffffffu, start, src);
+            break;
+        }
+        before += __shfl_sync(0xffffffffu, incl, 31);
+    }
+    // the rank-th sequence (ascending index) with that chunk count
+    int seen = 0;
+    for (int base = 0; base < S; base += 32) {
+        const int i = base + lane;
+        const bool hit = i < S && len[i] == want;
+        const unsigned bal = __ballot_sync(0xffffffffu, hit);
+        const int n = __popc(bal);
+        if (seen + n > rank) {
+            const unsigned mine = __ballot_sync(0xffffffffu, hit && __popc(bal & ((1u << lane) - 1u)) == rank - seen);
+            return base + __ffs(mine) - 1;
+        }
+        seen += n;
+    }
+    return 0;  // not reached: r < S
+}
 
 template <int D, int G, bool BF16>
 struct DecodeCfg {
@@ -70,7 +130,8 @@ struct DecodeCfg {
     static constexpr int A_BYTES = NCW * 8 * 4;
     static constexpr int MERGE_BYTES = NCW * (G * D + 2 * G) * 4;  // aliases the ring
     static constexpr int BAR_OFF = RING_BYTES + P_BYTES + A_BYTES;
-    static constexpr int SMEM_BYTES = BAR_OFF + 2 * NST * 8 + 1024;  // + alignment slack
+    static constexpr int SLOT_OFF = BAR_OFF + 2 * NST * 8;           // the sequence picked by the order step
+    static constexpr int SMEM_BYTES = SLOT_OFF + 16 + 1024;           // + alignment slack
     static_assert(MERGE_BYTES <= RING_BYTES, "merge area must fit in the ring");
     // Consumer warp w takes blocks b = w, w + NCW, ...; with NST a multiple of NCW every ring stage
     // belongs to one warp, which waits on its phases in order -- a stage's full barrier is then
@@ -156,8 +217,21 @@ decode_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmK, con
     // behind them (longest-first without knowing the lengths on the host)
     const int qpos = (int)(blockIdx.x / units);
     const int piece = (p.max_parts - 1) - qpos;
-    const int sg = (int)blockIdx.x - qpos * units;
-    const int s = sg / p.n_kv_heads, g = sg - s * p.n_kv_heads;
+    int s, g;
+    if (p.lpt) {
+        volatile int* slot = reinterpret_cast<volatile int*>(smem + C::SLOT_OFF);
+        const int r = (int)blockIdx.x / p.n_kv_heads;
+        const int picked = seq_at_rank(p, r, reinterpret_cast<int*>(smem));
+        if (threadIdx.x == 0) *slot = picked;
+        fence_proxy_async_smem();  // the scratch (ring) is written by TMA next
+        __syncthreads();
+        s = *slot;
+        g = (int)blockIdx.x - r * p.n_kv_heads;
+    } else {
+        const int sg = (int)blockIdx.x - qpos * units;
+        s = sg / p.n_kv_heads;
+        g = sg - s * p.n_kv_heads;
+    }
 
     // context length, clamped to what the table (and the split-K grid) can address
     int L = __ldg(p.context_lens + s);

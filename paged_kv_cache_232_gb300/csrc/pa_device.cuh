@@ -33,6 +33,9 @@ __host__ __device__ __forceinline__ int table_row_tokens(int mb, int cpb_log2) {
     return cpb_log2 < 0 ? mb * 8 : (mb * 16) << cpb_log2;
 }
 
+// Orders this thread's generic-proxy shared-memory accesses before later async-proxy (TMA) ones.
+__device__ __forceinline__ void fence_proxy_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+
 __device__ __forceinline__ uint32_t smem_addr(const void* p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
