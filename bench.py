@@ -603,9 +603,6 @@ def run_reference(args, rank, world):
 # ----------------------------------------------------------------------------- distributed glue
 
 
-_PG = None
-
-
 def barrier(world):
     if world > 1:
         import torch.distributed as dist
