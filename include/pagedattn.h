@@ -15,8 +15,9 @@
  *    block_tables[seq][t / block_size], offset t % block_size (MiniLLM Runtime,
  *    "Core class relationships": logical token -> logical block + offset ->
  *    block_table -> physical address).
- *  - Supported shapes: block_size 8, 16, 32, 64 or 128; head_dim 64, 96 or 128 (96 runs in the
- *    128-column kernels with the extra columns zero); n_q_heads a multiple
+ *  - Supported shapes: block_size 8, 16, 32, 64 or 128; head_dim 64, 96, 128 or 256 (96 runs in
+ *    the 128-column kernels with the extra columns zero; 256 with group size 1, 2 or 4, and not in
+ *    pa_prefill_chunk); n_q_heads a multiple
  *    of n_kv_heads with group size G = n_q_heads / n_kv_heads in {1, 2, 4, 8};
  *    query head h reads KV head h / G.
  *  - stream is a cudaStream_t (NULL = legacy default stream).  Calls only
@@ -116,7 +117,7 @@ int pa_rope_table(float* out, int64_t max_position, int head_dim, double theta);
  *  positions    [num_tokens] int64 in [0, max_position); a row outside is left untouched (q
  *               and cache) and sets PA_DEVERR_POSITION
  *  cos_sin      [max_position, head_dim] float32, device copy of pa_rope_table's output
- *  head_dim 64, 96 or 128; n_q_heads >= 0 (ignored when q is NULL).  num_tokens == 0 launches
+ *  head_dim 64, 96, 128 or 256; n_q_heads >= 0 (ignored when q is NULL).  num_tokens == 0 launches
  *  nothing and returns PA_OK.
  */
 int pa_rope_reshape_and_cache(void* q, const void* key, const void* value, void* k_cache, void* v_cache,

@@ -84,7 +84,8 @@ int check_heads(int n_q_heads, int n_kv_heads, int head_dim, int block_size, int
     if (n_q_heads <= 0 || n_kv_heads <= 0 || n_q_heads % n_kv_heads) return PA_ERR_SHAPE;
     const int G = n_q_heads / n_kv_heads;
     if (G != 1 && G != 2 && G != 4 && G != 8) return PA_ERR_UNSUPPORTED;
-    if (head_dim != 64 && head_dim != 96 && head_dim != 128) return PA_ERR_UNSUPPORTED;
+    if (head_dim != 64 && head_dim != 96 && head_dim != 128 && head_dim != 256) return PA_ERR_UNSUPPORTED;
+    if (head_dim == 256 && G > 4) return PA_ERR_UNSUPPORTED;  // decode keeps q for the group in registers
     if (block_size != 8 && block_size != 16 && block_size != 32 && block_size != 64 && block_size != 128)
         return PA_ERR_UNSUPPORTED;
     if (dtype != PA_F16 && dtype != PA_BF16) return PA_ERR_UNSUPPORTED;
@@ -319,7 +320,7 @@ int pa_rope_reshape_and_cache(void* q, const void* key, const void* value, void*
         max_position <= 0 || (q && n_q_heads <= 0))
         return PA_ERR_SHAPE;
     if (dtype != PA_F16 && dtype != PA_BF16) return PA_ERR_UNSUPPORTED;
-    if (head_dim != 64 && head_dim != 96 && head_dim != 128) return PA_ERR_UNSUPPORTED;
+    if (head_dim != 64 && head_dim != 96 && head_dim != 128 && head_dim != 256) return PA_ERR_UNSUPPORTED;
     if (num_tokens == 0) return PA_OK;
     if (!key || !value || !k_cache || !v_cache || !slot_mapping || !positions || !cos_sin) return PA_ERR_NULL;
     if (!aligned16(key) || !aligned16(value) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(cos_sin) ||
@@ -343,17 +344,22 @@ int pa_rope_reshape_and_cache(void* q, const void* key, const void* value, void*
             n_q_heads, n_kv_heads, num_blocks * block_size, max_position, dev->err);
     };
     const bool bf = dtype == PA_BF16;
-    auto by_dim = [&](auto k64, auto k96, auto k128) {
-        if (head_dim == 128) launch(k128);
+    auto by_dim = [&](auto k64, auto k96, auto k128, auto k256) {
+        if (head_dim == 256) launch(k256);
+        else if (head_dim == 128) launch(k128);
         else if (head_dim == 96) launch(k96);
         else launch(k64);
     };
     if (rows == 2) {
-        if (bf) by_dim(pa::rope_write_kernel<true, 64, 2>, pa::rope_write_kernel<true, 96, 2>, pa::rope_write_kernel<true, 128, 2>);
-        else by_dim(pa::rope_write_kernel<false, 64, 2>, pa::rope_write_kernel<false, 96, 2>, pa::rope_write_kernel<false, 128, 2>);
+        if (bf) by_dim(pa::rope_write_kernel<true, 64, 2>, pa::rope_write_kernel<true, 96, 2>,
+                       pa::rope_write_kernel<true, 128, 2>, pa::rope_write_kernel<true, 256, 2>);
+        else by_dim(pa::rope_write_kernel<false, 64, 2>, pa::rope_write_kernel<false, 96, 2>,
+                    pa::rope_write_kernel<false, 128, 2>, pa::rope_write_kernel<false, 256, 2>);
     } else {
-        if (bf) by_dim(pa::rope_write_kernel<true, 64, 1>, pa::rope_write_kernel<true, 96, 1>, pa::rope_write_kernel<true, 128, 1>);
-        else by_dim(pa::rope_write_kernel<false, 64, 1>, pa::rope_write_kernel<false, 96, 1>, pa::rope_write_kernel<false, 128, 1>);
+        if (bf) by_dim(pa::rope_write_kernel<true, 64, 1>, pa::rope_write_kernel<true, 96, 1>,
+                       pa::rope_write_kernel<true, 128, 1>, pa::rope_write_kernel<true, 256, 1>);
+        else by_dim(pa::rope_write_kernel<false, 64, 1>, pa::rope_write_kernel<false, 96, 1>,
+                    pa::rope_write_kernel<false, 128, 1>, pa::rope_write_kernel<false, 256, 1>);
     }
     return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
@@ -425,6 +431,7 @@ int pa_prefill_chunk(void* out, const void* q, const void* k_cache, const void* 
     if (num_chunks < 0 || max_q_len < 0 || max_blocks_per_seq <= 0 || num_blocks <= 0) return PA_ERR_SHAPE;
     int st = check_heads(n_q_heads, n_kv_heads, head_dim, block_size, dtype);
     if (st != PA_OK) return st;
+    if (head_dim == 256) return PA_ERR_UNSUPPORTED;  // two O accumulators of 256 columns fill TMEM
     if (num_blocks > INT32_MAX) return PA_ERR_UNSUPPORTED;
     if (num_chunks == 0 || max_q_len == 0) return PA_OK;
     if (!out || !q || !k_cache || !v_cache || !block_tables || !query_start_loc || !seq_lens) return PA_ERR_NULL;

@@ -59,7 +59,9 @@ static cudaError_t by_group(int group, const DecodeParams& p, const CUtensorMap&
         case 1: return launch_decode_t<D, 1, BF16>(p, k, v, grid, r, st);
         case 2: return launch_decode_t<D, 2, BF16>(p, k, v, grid, r, st);
         case 4: return launch_decode_t<D, 4, BF16>(p, k, v, grid, r, st);
-        case 8: return launch_decode_t<D, 8, BF16>(p, k, v, grid, r, st);
+        case 8:
+            if constexpr (D != 256) return launch_decode_t<D, 8, BF16>(p, k, v, grid, r, st);
+            return cudaErrorInvalidValue;
         default: return cudaErrorInvalidValue;
     }
 }
@@ -70,12 +72,15 @@ static int resident_by_group(int group) {
         case 1: return resident_t<D, 1, BF16>();
         case 2: return resident_t<D, 2, BF16>();
         case 4: return resident_t<D, 4, BF16>();
-        case 8: return resident_t<D, 8, BF16>();
+        case 8:
+            if constexpr (D != 256) return resident_t<D, 8, BF16>();
+            return 0;
         default: return 0;
     }
 }
 
 int decode_resident_ctas(int bf16, int head_dim, int group) {
+    if (head_dim == 256) return bf16 ? resident_by_group<256, true>(group) : resident_by_group<256, false>(group);
     if (head_dim == 128) return bf16 ? resident_by_group<128, true>(group) : resident_by_group<128, false>(group);
     if (head_dim == 64) return bf16 ? resident_by_group<64, true>(group) : resident_by_group<64, false>(group);
     return 0;
@@ -83,6 +88,9 @@ int decode_resident_ctas(int bf16, int head_dim, int group) {
 
 cudaError_t launch_decode(int bf16, int head_dim, int group, const DecodeParams& p, const CUtensorMap& tmK,
                           const CUtensorMap& tmV, int grid, bool with_reduce, cudaStream_t st) {
+    if (head_dim == 256)
+        return bf16 ? by_group<256, true>(group, p, tmK, tmV, grid, with_reduce, st)
+                    : by_group<256, false>(group, p, tmK, tmV, grid, with_reduce, st);
     if (head_dim == 128)
         return bf16 ? by_group<128, true>(group, p, tmK, tmV, grid, with_reduce, st)
                     : by_group<128, false>(group, p, tmK, tmV, grid, with_reduce, st);

@@ -115,7 +115,7 @@ struct DecodeCfg {
     static constexpr int SLAB_BYTES = BS * 128;       // one slab of one block tile
     static constexpr int TILE_BYTES = HALVES * SLAB_BYTES;
     static constexpr int STAGE_BYTES = 2 * TILE_BYTES;  // K tile + V tile
-    static constexpr int NST = (D == 128) ? 8 : 16;
+    static constexpr int NST = (D == 256) ? 4 : (D == 128) ? 8 : 16;  // 64 KB of K/V in flight
     static constexpr int NCW = 4;                     // consumer warps
     static constexpr int THREADS = (NCW + 1) * 32;
     static constexpr int CPL = HALVES;                // 16-byte chunks per lane for q.K
@@ -137,7 +137,8 @@ struct DecodeCfg {
     // belongs to one warp, which waits on its phases in order -- a stage's full barrier is then
     // never two phases behind the phase its warp waits for (where the parity test would pass early).
     static_assert(NST % NCW == 0, "ring stages must be a multiple of the consumer warps");
-    static_assert(D == 64 || D == 128, "head_dim 64 or 128");
+    static_assert(D == 64 || D == 128 || D == 256, "head_dim 64, 128 or 256");
+    static_assert(D != 256 || G <= 4, "head_dim 256: group size 1, 2 or 4 (q takes 32 G registers)");
     static_assert(G == 1 || G == 2 || G == 4 || G == 8, "group size 1, 2, 4 or 8");
 };
 
@@ -197,7 +198,8 @@ __device__ __forceinline__ float head_sum(float x) {
 // fits in the resulting 136 registers without spills (G = 4 would otherwise take ~150 and lose
 // a third of the warps); G = 8 at head_dim 64 fits two, at head_dim 128 only one without spills.
 template <int D, int G, bool BF16>
-__global__ void __launch_bounds__(DecodeCfg<D, G, BF16>::THREADS, (G <= 4) ? 3 : (D == 64 ? 2 : 1))
+__global__ void __launch_bounds__(DecodeCfg<D, G, BF16>::THREADS,
+                                  D == 256 ? (G <= 2 ? 2 : 1) : ((G <= 4) ? 3 : (D == 64 ? 2 : 1)))
 decode_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV) {
     using C = DecodeCfg<D, G, BF16>;
     using F = F16x2<BF16>;
@@ -339,7 +341,8 @@ decode_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmK, con
     int chunk_col[C::CPL];  // first column (element index) of each of this lane's chunks
 #pragma unroll
     for (int j = 0; j < C::CPL; ++j) {
-        const int half = (C::HALVES == 2) ? (dl >> 2) : 0;
+        // HALVES = 4: chunk dl of every slab; 2: two chunks of one slab, staggered; 1: chunk dl
+        const int half = (C::HALVES == 4) ? j : (C::HALVES == 2) ? (dl >> 2) : 0;
         const int c = (C::HALVES == 2) ? ((2 * (dl & 3) + half + j) & 7) : dl;
         chunk_col[j] = half * 64 + c * 8;
     }
@@ -590,10 +593,10 @@ __global__ void __launch_bounds__(256) splitk_reduce_kernel(const DecodeParams p
     }
     __syncthreads();
 
-    constexpr int LPR = D / 4;  // lanes per row (float4 each)
-    float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (lane < LPR) {
-        const float* ob = p.ws_o + (size_t)row * p.max_parts * D + lane * 4;
+    // each lane sums float4 columns lane * 4 + 128 k of the row's pieces (warp w: pieces w, w + 8, ...)
+    for (int c0 = lane * 4; c0 < D; c0 += 128) {
+        float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
+        const float* ob = p.ws_o + (size_t)row * p.max_parts * D + c0;
         int i = warp;
         for (; i + 24 < n_parts; i += 32) {
             float4 x0 = *reinterpret_cast<const float4*>(ob + (size_t)i * D);
@@ -613,7 +616,7 @@ __global__ void __launch_bounds__(256) splitk_reduce_kernel(const DecodeParams p
                 a.x += w * x.x; a.y += w * x.y; a.z += w * x.z; a.w += w * x.w;
             }
         }
-        *reinterpret_cast<float4*>(acc + warp * D + lane * 4) = a;
+        *reinterpret_cast<float4*>(acc + warp * D + c0) = a;
     }
     __syncthreads();
     if (2 * tid < p.hd) {

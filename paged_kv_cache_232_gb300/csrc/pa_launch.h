@@ -28,9 +28,11 @@ inline cudaError_t smem_limit_once(const void* func, int bytes, std::atomic<unsi
 
 // Launch the decode piece kernel for (dtype, head_dim, group) on `grid` CTAs; when
 // params.part_tokens > 0 and any sequence has more than one piece, also launch the reduce.
-// Bytes of the decode kernel's ring for head_dim (64 or 128).
+// Bytes of the decode kernel's ring for head_dim (64, 128 or 256).
 inline int decode_ring_bytes(int head_dim) {
-    return head_dim == 128 ? DecodeCfg<128, 1, true>::RING_BYTES : DecodeCfg<64, 1, true>::RING_BYTES;
+    return head_dim == 256   ? DecodeCfg<256, 1, true>::RING_BYTES
+           : head_dim == 128 ? DecodeCfg<128, 1, true>::RING_BYTES
+                             : DecodeCfg<64, 1, true>::RING_BYTES;
 }
 
 // CTAs of the decode kernel for (dtype, head_dim, group) that fit on one SM (0 on a CUDA error);

@@ -40,12 +40,13 @@ def test_barrier_and_max_over_ranks_two_gloo_ranks(tmp_path):
         got = bench.max_over_ranks(1.5 + rank, world)
         assert got == 1.5 + (world - 1), got
         assert bench.max_over_ranks(7.0, 1) == 7.0          # one rank: no collective
-        print("rank", rank, "max", got, flush=True)
+        with open(os.path.join({str(tmp_path)!r}, f"rank{{rank}}.txt"), "w") as f:
+            f.write(repr(got))
         dist.destroy_process_group()
     """))
     r = _torchrun([str(worker)])
     assert r.returncode == 0, r.stdout[-2000:] + r.stderr[-2000:]
-    assert r.stdout.count("max 2.5") == 2
+    assert [(tmp_path / f"rank{i}.txt").read_text() for i in range(2)] == ["2.5", "2.5"]
 
 
 def test_reference_arm_two_ranks_prints_one_line():

@@ -105,7 +105,8 @@ EDGE_LENS = [1, 15, 16, 17, 255, 256, 257, 513, 4097]
 
 @pytest.mark.parametrize("dt,hq,hkv,d", [(wl.BF16, 16, 8, 128), (wl.F16, 2, 2, 64), (wl.BF16, 32, 8, 128),
                                          (wl.F16, 8, 1, 128), (wl.BF16, 8, 2, 64), (wl.F16, 16, 4, 128),
-                                         (wl.BF16, 8, 1, 64), (wl.BF16, 16, 8, 96), (wl.F16, 32, 4, 96)])
+                                         (wl.BF16, 8, 1, 64), (wl.BF16, 16, 8, 96), (wl.F16, 32, 4, 96),
+                                         (wl.BF16, 8, 8, 256), (wl.F16, 16, 8, 256), (wl.BF16, 16, 4, 256)])
 @pytest.mark.parametrize("mode,part", [("v1", 0), ("splitk", 0), ("splitk", 64), ("splitk", 512), ("splitk", 48),
                                        ("splitk", 400)])
 def test_decode_edge_lengths(dt, hq, hkv, d, mode, part):
@@ -260,4 +261,17 @@ def test_long_context_planned_pieces_match_oracle():
     pa.pa_device_errors(clear=True)
     got = Dev(w).run("splitk", part)
     check(got, oracle_decode(w), w.pool.dtype, f"config3/splitk {part}")
+    assert pa.pa_device_errors(clear=True) == 0
+
+
+def test_head_dim_256_batch_longer_than_a_wave():
+    """head_dim 256 (G = 2: two CTAs per SM) with more (sequence, KV head) units than resident
+    CTAs, so the one-pass grid runs longest first; and the split-K path on the same batch."""
+    lens = wl.uniform_ints(wl.derive_seed(256, 1), 200, 100, 1500).tolist()
+    w = wl.build_workload("hd256", 2561, dtype=wl.BF16, n_q_heads=8, n_kv_heads=4, head_dim=256, decode_lens=lens,
+                          extra_blocks=3)
+    ref = oracle_decode(w)
+    pa.pa_device_errors(clear=True)
+    for mode in ("auto", "splitk"):
+        check(Dev(w).run(mode), ref, w.pool.dtype, f"hd 256 {mode}")
     assert pa.pa_device_errors(clear=True) == 0

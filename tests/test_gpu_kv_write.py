@@ -46,7 +46,8 @@ def test_write_bandwidth_scale_64k_rows():
 
 
 @pytest.mark.parametrize("n,hkv,d,dt", [(1, 8, 128, wl.BF16), (3, 2, 64, wl.F16), (37, 1, 64, wl.BF16),
-                                        (1023, 4, 128, wl.F16), (4099, 8, 64, wl.BF16), (513, 8, 96, wl.BF16)])
+                                        (1023, 4, 128, wl.F16), (4099, 8, 64, wl.BF16), (513, 8, 96, wl.BF16),
+                                        (300, 4, 256, wl.F16)])
 def test_write_shapes_and_ragged_counts(n, hkv, d, dt):
     w = wl.write_rows_case(1000 + n, n, n_kv_heads=hkv, head_dim=d, dtype=dt, pad_frac=0.25, nan_canaries=True)
     assert assert_write_matches_oracle(w) == 0

@@ -103,7 +103,7 @@ def test_rope_write_bandwidth_scale_64k_rows():
 
 @pytest.mark.parametrize("dt,hq,hkv,d,with_q", [(wl.F16, 8, 8, 64, True), (wl.BF16, 32, 8, 128, True),
                                                (wl.F16, 16, 4, 128, False), (wl.BF16, 2, 2, 64, True),
-                                               (wl.BF16, 16, 8, 96, True)])
+                                               (wl.BF16, 16, 8, 96, True), (wl.F16, 8, 4, 256, True)])
 def test_rope_write_shapes(dt, hq, hkv, d, with_q):
     w = wl.write_rows_case(700 + hq + d, 333, n_kv_heads=hkv, head_dim=d, dtype=dt, pad_frac=0.2, nan_canaries=True)
     n = w.write.key.shape[0]
