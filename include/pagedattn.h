@@ -16,8 +16,7 @@
  *    "Core class relationships": logical token -> logical block + offset ->
  *    block_table -> physical address).
  *  - Supported shapes: block_size 8, 16, 32, 64 or 128; head_dim 64, 96, 128 or 256 (96 runs in
- *    the 128-column kernels with the extra columns zero; 256 with group size 1, 2 or 4, and not in
- *    pa_prefill_chunk); n_q_heads a multiple
+ *    the 128-column kernels with the extra columns zero; 256 with group size 1, 2 or 4); n_q_heads a multiple
  *    of n_kv_heads with group size G = n_q_heads / n_kv_heads in {1, 2, 4, 8};
  *    query head h reads KV head h / G.
  *  - stream is a cudaStream_t (NULL = legacy default stream).  Calls only
@@ -235,7 +234,7 @@ int pa_decode_splitk_static(void* out, const void* q, const void* k_cache, const
 
 /*
  * pa_prefill_chunk -- attention for ragged prefill chunks that attend to their
- * earlier cached context, on the tcgen05 tensor cores (head_dim 64, 96 or 128).
+ * earlier cached context, on the tcgen05 tensor cores (head_dim 64, 96, 128 or 256).
  * Source: mini_engine, "Custom CUDA kernels" (paged prefill attention: tiled,
  * online softmax, K/V read from the paged pool itself, ragged batches, prefix
  * hits and chunks over earlier chunks in one launch); miniserve, "Engine"

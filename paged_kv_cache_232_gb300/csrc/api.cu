@@ -431,7 +431,6 @@ int pa_prefill_chunk(void* out, const void* q, const void* k_cache, const void* 
     if (num_chunks < 0 || max_q_len < 0 || max_blocks_per_seq <= 0 || num_blocks <= 0) return PA_ERR_SHAPE;
     int st = check_heads(n_q_heads, n_kv_heads, head_dim, block_size, dtype);
     if (st != PA_OK) return st;
-    if (head_dim == 256) return PA_ERR_UNSUPPORTED;  // two O accumulators of 256 columns fill TMEM
     if (num_blocks > INT32_MAX) return PA_ERR_UNSUPPORTED;
     if (num_chunks == 0 || max_q_len == 0) return PA_OK;
     if (!out || !q || !k_cache || !v_cache || !block_tables || !query_start_loc || !seq_lens) return PA_ERR_NULL;

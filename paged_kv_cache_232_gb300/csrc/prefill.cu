@@ -10,6 +10,8 @@
 //  * A query tile is 128 rows = 128 / G query tokens x the G heads of one KV head, so every
 //    K/V tile feeds all G heads (GQA sharing) and the MMA M dimension is a full 128.  One CTA
 //    owns two consecutive query tiles of one (chunk, KV head): both read the same K/V tiles.
+//    At head_dim 256 a CTA owns one query tile and streams K/V in stages of 64 keys (its O
+//    accumulator takes 256 TMEM columns, and two stages of K and V must fit beside Q).
 //  * Two producer warps (one for K, one for V) gather tiles of 128 keys (8 paged blocks) with
 //    one 4-D TMA load per block and 64-column slab, 128-byte swizzled, into two-stage rings.
 //    Block ids come from the chunk's block-table row; blocks past the sequence load zeros
@@ -43,29 +45,37 @@ namespace pa {
 namespace pf {
 
 constexpr int BM = 128;                 // query rows per tile
-constexpr int BN = 128;                 // keys per tile
-constexpr int NQT = 2;                  // query tiles per CTA
-constexpr int SLAB = BN * 128;          // 128 rows x 128 bytes: one 64-column slab
-constexpr int BS = 64;                  // keys per S sub-tile (two per K/V stage)
+constexpr int BN = 128;                 // keys per unit of the scheduling cost
+constexpr int NQT = 2;                  // query-tile roles per CTA (head_dim 256 uses one)
+constexpr int BS = 64;                  // keys per S sub-tile
 // barriers: K_FULL / V_FULL per ring stage; K_EMPTY / V_EMPTY, S_FULL and P_FULL per (query tile,
 // buffer) at index 2 t + b; PV_DONE and DRAIN per query tile; V_ZERO once (last V stage cleaned)
 enum Bar { Q_FULL = 0, K_FULL = 1, V_FULL = 3, K_EMPTY = 5, V_EMPTY = 9, S_FULL = 13, P_FULL = 17, PV_DONE = 21,
            DRAIN = 23, V_ZERO = 25, NUM_BARS = 26 };
 static_assert(NUM_BARS <= 32, "barrier area");
 constexpr int SCHED_BYTES = 24 * 1024;
-// Shared-memory layout for head_dim D (64 or 128): a [128 x D] 16-bit tile is D / 64 slabs.
+// Shared-memory layout for head_dim D: a 16-bit tile of R rows x D columns is D / 64 slabs of
+// R x 128 bytes.  head_dim 64 / 128: two query tiles per CTA and K/V stages of 128 keys (two S
+// sub-tiles); head_dim 256: one query tile (its O takes 256 of the 512 TMEM columns) and stages
+// of 64 keys (one sub-tile), so that two stages of K and of V still fit next to the Q tile.
 template <int D>
 struct Layout {
-    static_assert(D == 64 || D == 128, "head_dim 64 or 128");
+    static_assert(D == 64 || D == 128 || D == 256, "head_dim 64, 128 or 256");
     static constexpr int SLABS = D / 64;
-    static constexpr int TILE = SLABS * SLAB;
-    static constexpr int Q_OFF = 0;                 // NQT tiles
-    static constexpr int K_OFF = NQT * TILE;        // two stages
-    static constexpr int V_OFF = K_OFF + 2 * TILE;  // two stages
-    static constexpr int BAR_OFF = V_OFF + 2 * TILE;
+    static constexpr int NQ = (D == 256) ? 1 : 2;       // query tiles per CTA
+    static constexpr int SK = (D == 256) ? 64 : 128;    // keys per K/V stage
+    static constexpr int SPS = SK / BS;                 // S sub-tiles per stage
+    static constexpr int CHUNKS = SK / 16;              // 16-token chunks per stage
+    static constexpr int QSLAB = BM * 128, KSLAB = SK * 128;
+    static constexpr int QTILE = SLABS * QSLAB, KTILE = SLABS * KSLAB;
+    static constexpr int Q_OFF = 0;                     // NQ tiles
+    static constexpr int K_OFF = NQ * QTILE;            // two stages
+    static constexpr int V_OFF = K_OFF + 2 * KTILE;     // two stages
+    static constexpr int BAR_OFF = V_OFF + 2 * KTILE;
     static constexpr int TMEM_SLOT_OFF = BAR_OFF + 32 * 8;
     static constexpr int SCHED_OFF = TMEM_SLOT_OFF + 16;  // CTA-order scratch: query_start_loc, seq_lens, histogram
     static constexpr int SMEM_BYTES = SCHED_OFF + SCHED_BYTES + 1024;  // + alignment slack
+    static_assert(SMEM_BYTES <= 227 * 1024, "shared memory per CTA");
 };
 // warpgroups 0..NQT-1: softmax (one per query tile); warpgroup NQT: K loads, MMA issue for tile 0,
 // V loads, MMA issue for tile 1
@@ -272,7 +282,8 @@ __global__ void __launch_bounds__(pf::THREADS, 1)
 prefill_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV) {
     using namespace pf;
     using L = Layout<D>;
-    constexpr int SLABS = L::SLABS, TILE = L::TILE;
+    constexpr int SLABS = L::SLABS, NQ = L::NQ, SPS = L::SPS, SK = L::SK, CHUNKS = L::CHUNKS;
+    constexpr int QSLAB = L::QSLAB, KSLAB = L::KSLAB, QTILE = L::QTILE, KTILE = L::KTILE;
     using F = F16x2<BF16>;
     constexpr int TQ = BM / G;  // query tokens per tile
     extern __shared__ __align__(1024) unsigned char smem_raw[];
@@ -287,7 +298,7 @@ prefill_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmK, c
     // so handing out units longest-first gives longest-processing-time list scheduling.
     const int per_unit = p.num_chunks * p.n_kv_heads;
     int u_sel = (p.tiles_per_chunk - 1 - (int)(blockIdx.x / per_unit)) * per_unit + (int)(blockIdx.x % per_unit);
-    if (p.lpt) u_sel = lpt_unit<TQ * NQT>(p, smem + L::SCHED_OFF);
+    if (p.lpt) u_sel = lpt_unit<TQ * NQ>(p, smem + L::SCHED_OFF);
     const int unit = u_sel / per_unit;
     const int rem = u_sel % per_unit;
     const int c = rem / p.n_kv_heads, g = rem % p.n_kv_heads;
@@ -301,21 +312,21 @@ prefill_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmK, c
         if (unit == 0 && g == 0 && threadIdx.x == 0) flag_error(p.err, PA_DEVERR_LENGTH);
         return;
     }
-    const int j0 = unit * NQT * TQ;
+    const int j0 = unit * NQ * TQ;
     if (j0 >= q_len) return;  // whole CTA: past the chunk
     const int ctx = kv_len - q_len;
     int n_sub[NQT];           // 64-key S sub-tiles each query tile needs (0: tile past the chunk)
 #pragma unroll
     for (int t = 0; t < NQT; ++t) {
         const int jt = j0 + t * TQ;
-        n_sub[t] = (jt < q_len) ? (ctx + min(jt + TQ, q_len) + BS - 1) / BS : 0;
+        n_sub[t] = (t < NQ && jt < q_len) ? (ctx + min(jt + TQ, q_len) + BS - 1) / BS : 0;
     }
     const int nsub_max = n_sub[NQT - 1] > n_sub[0] ? n_sub[NQT - 1] : n_sub[0];
-    const int n_max = (nsub_max + 1) / 2;  // 128-key K/V stages to stream
+    const int n_max = (nsub_max + SPS - 1) / SPS;  // K/V stages to stream
     const int nblk_seq = (kv_len + 15) / 16;
 
     if (threadIdx.x == 0) {
-        mbar_init(bars + 8 * Q_FULL, NQT * BM);
+        mbar_init(bars + 8 * Q_FULL, NQ * BM);
         for (int s = 0; s < 2; ++s) {
             mbar_init(bars + 8 * (K_FULL + s), 1);
             mbar_init(bars + 8 * (V_FULL + s), 1);
@@ -344,8 +355,9 @@ prefill_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmK, c
     else
         asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(REGS_PRODUCER));
 
-    if (warp < 4 * NQT) {
-        // ------------------------------------------------------------ softmax warpgroups
+    if (warp < 4 * NQ) {
+        // ------------------------------------------------------------ softmax warpgroups (with
+        // one query tile per CTA the second warpgroup has no work)
         const int t = warp >> 2;                    // query tile of this warpgroup
         const int r = threadIdx.x & 127;            // row of the tile == TMEM lane
         const int jt0 = j0 + t * TQ;
@@ -360,21 +372,25 @@ prefill_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmK, c
             // instruction (consecutive rows are contiguous when G >= 2), each lane one 16-byte
             // chunk into its 128-byte-swizzled place
             constexpr int CPR = D / 8, RPI = 32 / CPR;  // chunks per row, rows per instruction
-            const uint32_t qt = sQ + t * TILE;
+            constexpr int PASS = CPR < 16 ? CPR : 16;   // loads in flight per lane
+            const uint32_t qt = sQ + t * QTILE;
             const int ch = lane % CPR;
-            uint4 v[CPR];
 #pragma unroll
-            for (int i = 0; i < CPR; ++i) {
-                const int R = (warp & 3) * 32 + RPI * i + lane / CPR;
-                const int tok = jt0 + R / G;
-                const uint16_t* src = static_cast<const uint16_t*>(p.q) +
-                                      ((size_t)(q0 + tok) * p.n_q_heads + g * G + R % G) * p.hd + ch * 8;
-                v[i] = (tok < q_len && ch * 8 < p.hd) ? ldg_nc_128(src) : make_uint4(0u, 0u, 0u, 0u);
-            }
+            for (int i0 = 0; i0 < CPR; i0 += PASS) {
+                uint4 v[PASS];
 #pragma unroll
-            for (int i = 0; i < CPR; ++i) {
-                const int R = (warp & 3) * 32 + RPI * i + lane / CPR;
-                sts128(qt + (ch >> 3) * SLAB + swz128(R, ch & 7), v[i]);
+                for (int i = 0; i < PASS; ++i) {
+                    const int R = (warp & 3) * 32 + RPI * (i0 + i) + lane / CPR;
+                    const int tok = jt0 + R / G;
+                    const uint16_t* src = static_cast<const uint16_t*>(p.q) +
+                                          ((size_t)(q0 + tok) * p.n_q_heads + g * G + R % G) * p.hd + ch * 8;
+                    v[i] = (tok < q_len && ch * 8 < p.hd) ? ldg_nc_128(src) : make_uint4(0u, 0u, 0u, 0u);
+                }
+#pragma unroll
+                for (int i = 0; i < PASS; ++i) {
+                    const int R = (warp & 3) * 32 + RPI * (i0 + i) + lane / CPR;
+                    sts128(qt + (ch >> 3) * QSLAB + swz128(R, ch & 7), v[i]);
+                }
             }
             tc::fence_async_smem();
             mbar_arrive(bars + 8 * Q_FULL);
@@ -430,9 +446,9 @@ prefill_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmK, c
     } else if (warp == TMA_WARP || warp == TMA_V_WARP) {
         // ------------------------------------------------------------ TMA producers: K (warp
         // TMA_WARP) and V (warp TMA_V_WARP) rings, issued by separate warps so that the two
-        // tiles' box loads are in flight together.  Stage i reuses the buffer of stage i - 2
-        // once every query tile that read stage i - 2 has released it (tile t reads stages
-        // 0 .. (n_sub[t] + 1) / 2 - 1).
+        // tiles' box loads are in flight together.  Stage i (keys SK i .. SK i + SK - 1) reuses the
+        // buffer of stage i - 2 once every query tile that read stage i - 2 has released it (tile t
+        // reads stages 0 .. (n_sub[t] + SPS - 1) / SPS - 1).
         const int kv = (warp == TMA_V_WARP) ? 1 : 0;
         const CUtensorMap* map = kv ? &tmV : &tmK;
         if (lane == 0) tma_prefetch_desc(map);
@@ -447,8 +463,8 @@ prefill_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmK, c
             const uint32_t ph = (i >> 1) & 1;
             // 16-token chunk b: table entry b >> cpb_log2; blocks of 8 tokens: one entry per 8 rows
             int my = p.num_blocks;  // past the sequence (or invalid): out-of-range coordinate, zero fill
-            const int e = half8 ? i * 16 + lane : (i * 8 + (lane & 7)) >> p.cpb_log2;
-            if (half8 ? (lane < 16 && 8 * e < kv_len) : (lane < 8 && i * 8 + lane < nblk_seq)) {
+            const int e = half8 ? i * 2 * CHUNKS + lane : (i * CHUNKS + lane % CHUNKS) >> p.cpb_log2;
+            if (half8 ? (lane < 2 * CHUNKS && 8 * e < kv_len) : (lane < CHUNKS && i * CHUNKS + lane < nblk_seq)) {
                 my = __ldg(bt + e);
                 if (my < 0 || my >= p.num_blocks) {
                     if (kv == 0) flag_error(p.err, PA_DEVERR_BLOCK);
@@ -458,26 +474,26 @@ prefill_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmK, c
             if (lane == 0 && i >= 2) {
 #pragma unroll
                 for (int t = 0; t < NQT; ++t)
-                    if (ok && 2 * (i - 2) < n_sub[t]) ok = mbar_wait(empty0 + 8 * (2 * t + st), ph ^ 1, p.err);
+                    if (ok && (i - 2) * SPS < n_sub[t]) ok = mbar_wait(empty0 + 8 * (2 * t + st), ph ^ 1, p.err);
             }
             if (!__shfl_sync(0xffffffffu, ok, 0)) break;
             const uint32_t full = full0 + 8 * st;
-            const uint32_t dst0 = dst_base + st * TILE;
-            if (lane == 0) mbar_arrive_expect_tx(full, TILE);
+            const uint32_t dst0 = dst_base + st * KTILE;
+            if (lane == 0) mbar_arrive_expect_tx(full, KTILE);
             __syncwarp();
             if (!half8) {
-                // lanes 0 .. 8 SLABS - 1 each issue one box: chunk lane % 8, 64-column slab lane / 8
-                const int blk = __shfl_sync(0xffffffffu, my, lane & 7);
-                const int sl = lane >> 3;
-                const int row0 = ((i * 8 + (lane & 7)) & ((1 << p.cpb_log2) - 1)) * 16;  // chunk's first row
-                if (lane < 8 * SLABS)
-                    tma_load_4d(dst0 + sl * SLAB + (lane & 7) * 2048, map, sl * 64, g, row0, blk, full, pol);
+                // lanes 0 .. CHUNKS SLABS - 1 each issue one box: chunk lane % CHUNKS, slab lane / CHUNKS
+                const int c16 = lane % CHUNKS, sl = lane / CHUNKS;
+                const int blk = __shfl_sync(0xffffffffu, my, c16);
+                const int row0 = ((i * CHUNKS + c16) & ((1 << p.cpb_log2) - 1)) * 16;  // chunk's first row
+                if (lane < CHUNKS * SLABS)
+                    tma_load_4d(dst0 + sl * KSLAB + c16 * 2048, map, sl * 64, g, row0, blk, full, pol);
             } else {
-                // lanes 0 .. 16 SLABS - 1: 8-row block lane % 16, slab lane / 16
-                const int blk = __shfl_sync(0xffffffffu, my, lane & 15);
-                const int sl = lane >> 4;
-                if (lane < 16 * SLABS)
-                    tma_load_4d(dst0 + sl * SLAB + (lane & 15) * 1024, map, sl * 64, g, 0, blk, full, pol);
+                // lanes 0 .. 2 CHUNKS SLABS - 1: 8-row block lane % (2 CHUNKS), slab lane / (2 CHUNKS)
+                const int b8 = lane % (2 * CHUNKS), sl = lane / (2 * CHUNKS);
+                const int blk = __shfl_sync(0xffffffffu, my, b8);
+                if (lane < 2 * CHUNKS * SLABS)
+                    tma_load_4d(dst0 + sl * KSLAB + b8 * 1024, map, sl * 64, g, 0, blk, full, pol);
             }
             if (kv == 1 && i == n_max - 1) {
                 // Rows of the sequence's last, partial block past kv_len may hold anything (P
@@ -485,11 +501,11 @@ prefill_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmK, c
                 // then release the stage to the MMA issuers through V_ZERO.
                 if (lane == 0) ok = mbar_wait(full, ph, p.err);
                 if (!__shfl_sync(0xffffffffu, ok, 0)) break;
-                const int z0 = max(kv_len, i * BN), z1 = min(((kv_len + 15) / 16) * 16, (i + 1) * BN);
+                const int z0 = max(kv_len, i * SK), z1 = min(((kv_len + 15) / 16) * 16, (i + 1) * SK);
                 constexpr int CPR = D / 8;  // 16-byte chunks per row
                 for (int e = lane; e < CPR * max(z1 - z0, 0); e += 32) {
-                    const int row = z0 - i * BN + e / CPR, chk = e % CPR;
-                    sts128(dst0 + (chk >> 3) * SLAB + row * 128 + (chk & 7) * 16, make_uint4(0u, 0u, 0u, 0u));
+                    const int row = z0 - i * SK + e / CPR, chk = e % CPR;
+                    sts128(dst0 + (chk >> 3) * KSLAB + row * 128 + (chk & 7) * 16, make_uint4(0u, 0u, 0u, 0u));
                 }
                 tc::fence_async_smem();
                 __syncwarp();
@@ -507,8 +523,8 @@ prefill_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmK, c
         constexpr uint32_t ID_PV = tc::idesc_f16(BF16, true, BM, D);
         // descriptors of the tile bases as (low, high) words; a K-step adds its byte offset >> 4
         // to the start-address field in the low word (addresses stay below 256 KB: no carry)
-        const uint64_t dq = tc::sdesc_sw128(sQ + t * TILE, 16, 1024), dk = tc::sdesc_sw128(sK, 16, 1024);
-        const uint64_t dv = tc::sdesc_sw128(sV, SLAB, 1024);
+        const uint64_t dq = tc::sdesc_sw128(sQ + t * QTILE, 16, 1024), dk = tc::sdesc_sw128(sK, 16, 1024);
+        const uint64_t dv = tc::sdesc_sw128(sV, KSLAB, 1024);
         const uint32_t q_lo = (uint32_t)dq, q_hi = (uint32_t)(dq >> 32);
         const uint32_t k_lo = (uint32_t)dk, k_hi = (uint32_t)(dk >> 32);
         const uint32_t v_lo = (uint32_t)dv, v_hi = (uint32_t)(dv >> 32);
@@ -531,16 +547,19 @@ prefill_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmK, c
             v_ready = j;
             return true;
         };
-        // S_t(v) = Q_t K^T for keys 64v .. 64v+63 (rows (v & 1) * 64 of stage v / 2), into buffer v & 1
+        // S_t(v) = Q_t K^T for keys 64v .. 64v+63 (rows (v % SPS) * 64 of stage v / SPS), into buffer v & 1
         auto issue_s = [&](int v) -> bool {
-            if (!wait_k(v >> 1)) return false;
+            const int j = v / SPS;
+            if (!wait_k(j)) return false;
             tc::fence_after();
-            const uint32_t ka = k_lo + (uint32_t)((((v >> 1) & 1) * TILE + (v & 1) * (BS * 128)) >> 4);
+            const uint32_t ka = k_lo + (uint32_t)(((j & 1) * KTILE + (v % SPS) * (BS * 128)) >> 4);
             const uint32_t dS = dS0 + (uint32_t)((v & 1) * BS);
 #pragma unroll
             for (int kk = 0; kk < D / 16; ++kk) {
-                const uint32_t off = (uint32_t)((((kk >> 2) * SLAB) + (kk & 3) * 32) >> 4);
-                tc::mma_f16_ss_w(dS, q_lo + off, q_hi, ka + off, k_hi, ID_QK, kk > 0);
+                // K-step kk: 32 bytes into slab kk / 4 of the Q tile and of the K stage
+                const uint32_t qo = (uint32_t)((((kk >> 2) * QSLAB) + (kk & 3) * 32) >> 4);
+                const uint32_t ko = (uint32_t)((((kk >> 2) * KSLAB) + (kk & 3) * 32) >> 4);
+                tc::mma_f16_ss_w(dS, q_lo + qo, q_hi, ka + ko, k_hi, ID_QK, kk > 0);
             }
             tc::commit(bars + 8 * (S_FULL + 2 * t + (v & 1)));
             issued = true;
@@ -548,9 +567,10 @@ prefill_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmK, c
         };
         // O_t += P_t(u) V for keys 64u .. 64u+63 (P_hi and P_lo from the S buffer u & 1)
         auto issue_pv = [&](int u) -> bool {
-            if (!wait_v(u >> 1)) return false;
+            const int j = u / SPS;
+            if (!wait_v(j)) return false;
             tc::fence_after();
-            const uint32_t va = v_lo + (uint32_t)((((u >> 1) & 1) * TILE + (u & 1) * (BS * 128)) >> 4);
+            const uint32_t va = v_lo + (uint32_t)(((j & 1) * KTILE + (u % SPS) * (BS * 128)) >> 4);
             const uint32_t pS = dS0 + (uint32_t)((u & 1) * BS);
 #pragma unroll
             for (int kk = 0; kk < BS / 16; ++kk) {
@@ -565,17 +585,19 @@ prefill_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmK, c
             return true;
         };
         // the last of this tile's sub-tiles that reads stage j
-        auto stage_last = [&](int j) { return min(2 * j + 1, nst - 1); };
-        // prologue: both S buffers
-        for (int v = 0; v < 2 && v < nst && ok; ++v) ok = issue_s(v);
-        if (ok) tc::commit(bars + 8 * (K_EMPTY + 2 * t));
+        auto stage_last = [&](int j) { return min(SPS * j + SPS - 1, nst - 1); };
+        // prologue: both S buffers (a stage's K is released after the QK of its last sub-tile)
+        for (int v = 0; v < 2 && v < nst && ok; ++v) {
+            ok = issue_s(v);
+            if (ok && v == stage_last(v / SPS)) tc::commit(bars + 8 * (K_EMPTY + 2 * t + ((v / SPS) & 1)));
+        }
         for (int u = 0; u < nst && ok; ++u) {
             ok = mbar_wait(bars + 8 * (P_FULL + 2 * t + (u & 1)), (u >> 1) & 1, p.err) && issue_pv(u);
             if (ok && u + 2 < nst) ok = issue_s(u + 2);
             if (!ok) break;
-            if (u == stage_last(u >> 1)) tc::commit(bars + 8 * (V_EMPTY + 2 * t + ((u >> 1) & 1)));
+            if (u == stage_last(u / SPS)) tc::commit(bars + 8 * (V_EMPTY + 2 * t + ((u / SPS) & 1)));
             const int v = u + 2;
-            if (v < nst && v == stage_last(v >> 1)) tc::commit(bars + 8 * (K_EMPTY + 2 * t + ((v >> 1) & 1)));
+            if (v < nst && v == stage_last(v / SPS)) tc::commit(bars + 8 * (K_EMPTY + 2 * t + ((v / SPS) & 1)));
         }
         // every MMA this thread issued must be complete before TMEM is released
         if (issued) {
@@ -600,7 +622,8 @@ static cudaError_t launch_prefill_t(const PrefillParams& p, const CUtensorMap& t
     cudaError_t e = smem_limit_once(reinterpret_cast<const void*>(kern), pf::Layout<D>::SMEM_BYTES, s_done);
     if (e != cudaSuccess) return e;
     // one CTA per pair of 128-row query tiles of a (chunk, KV head)
-    const int units = (p.tiles_per_chunk + pf::NQT - 1) / pf::NQT;
+    constexpr int NQ = pf::Layout<D>::NQ;
+    const int units = (p.tiles_per_chunk + NQ - 1) / NQ;
     PrefillParams q = p;
     q.tiles_per_chunk = units;
     const int ncost = table_row_tokens(p.max_blocks_per_seq, p.cpb_log2) / pf::BN + 2;
@@ -618,13 +641,17 @@ static cudaError_t by_group(int group, const PrefillParams& p, const CUtensorMap
         case 1: return launch_prefill_t<1, BF16, D>(p, k, v, st);
         case 2: return launch_prefill_t<2, BF16, D>(p, k, v, st);
         case 4: return launch_prefill_t<4, BF16, D>(p, k, v, st);
-        case 8: return launch_prefill_t<8, BF16, D>(p, k, v, st);
+        case 8:
+            if constexpr (D != 256) return launch_prefill_t<8, BF16, D>(p, k, v, st);
+            return cudaErrorNotSupported;
         default: return cudaErrorInvalidValue;
     }
 }
 
 cudaError_t launch_prefill(int bf16, int head_dim, int group, const PrefillParams& p, const CUtensorMap& tmK,
                            const CUtensorMap& tmV, cudaStream_t st) {
+    if (head_dim == 256)
+        return bf16 ? by_group<true, 256>(group, p, tmK, tmV, st) : by_group<false, 256>(group, p, tmK, tmV, st);
     if (head_dim == 128)
         return bf16 ? by_group<true, 128>(group, p, tmK, tmV, st) : by_group<false, 128>(group, p, tmK, tmV, st);
     if (head_dim == 64)

@@ -55,9 +55,9 @@ def test_validation_rejects_before_any_device_work(lib):
     assert lib.pa_decode_v1(vp, vp, vp, vp, vp, 8, vp, 1, 8, 8, 128, 24, 10, 0.1, 1, None) == -3
     assert lib.pa_decode_v1(vp, vp, vp, vp, vp, 8, vp, 1, 8, 8, 128, 16, 10, 0.1, 7, None) == -3
     assert lib.pa_decode_v1(vp, vp, vp, vp, vp, 8, vp, 1, 48, 3, 128, 16, 10, 0.1, 1, None) == -3
-    # head_dim 256: decode up to group size 4 only, no prefill
+    # head_dim 256: group size up to 4
     assert lib.pa_decode_v1(vp, vp, vp, vp, vp, 8, vp, 1, 64, 8, 256, 16, 10, 0.1, 1, None) == -3
-    assert lib.pa_prefill_chunk(vp, vp, vp, vp, vp, 8, vp, vp, 1, 1, 8, 8, 256, 16, 10, 0.1, 1, None) == -3
+    assert lib.pa_prefill_chunk(vp, vp, vp, vp, vp, 8, vp, vp, 1, 1, 64, 8, 256, 16, 10, 0.1, 1, None) == -3
     # null pointers, misalignment
     assert lib.pa_decode_v1(None, vp, vp, vp, vp, 8, vp, 1, 8, 8, 128, 16, 10, 0.1, 1, None) == -1
     assert lib.pa_decode_v1(ctypes.c_void_p(8), vp, vp, vp, vp, 8, vp, 1, 8, 8, 128, 16, 10, 0.1, 1, None) == -6

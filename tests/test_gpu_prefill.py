@@ -65,7 +65,7 @@ def check(got_bits, ref, dt, what):
 
 SHAPES = [(wl.BF16, 16, 8, 128), (wl.F16, 16, 8, 128), (wl.BF16, 8, 8, 128), (wl.BF16, 32, 8, 128),
           (wl.F16, 16, 2, 128), (wl.BF16, 16, 8, 64), (wl.F16, 8, 8, 64), (wl.BF16, 32, 4, 64), (wl.F16, 2, 2, 64),
-          (wl.BF16, 16, 8, 96), (wl.F16, 8, 2, 96)]
+          (wl.BF16, 16, 8, 96), (wl.F16, 8, 2, 96), (wl.BF16, 16, 8, 256), (wl.F16, 8, 2, 256), (wl.BF16, 4, 4, 256)]
 
 
 @pytest.mark.parametrize("dt,hq,hkv,d", SHAPES)
@@ -193,7 +193,7 @@ def test_unified_mixed_batch_single_launch():
 
 
 @pytest.mark.parametrize("bs", [8, 32, 64])
-@pytest.mark.parametrize("d", [128, 64])
+@pytest.mark.parametrize("d", [128, 64, 256])
 def test_prefill_block_sizes(bs, d):
     w = wl.build_workload("pfbs", 950 + bs + d, dtype=wl.BF16, n_q_heads=16, n_kv_heads=8, head_dim=d, block_size=bs,
                           prefill_q_lens=[1, 7, 64, 65, 128, 200, 17],
@@ -220,3 +220,14 @@ def test_write_then_decode_block_sizes(bs):
     ex = oracle.decode(b.q, k2, v2, b.block_tables, b.context_lens, b.scale, p.dtype)
     cd = oracle.decode(b.q, k2, abs_bits(v2), b.block_tables, b.context_lens, b.scale, p.dtype)
     check_attention(bits_of(out), ex, p.dtype, f"bs {bs} write + decode", cond=cd)
+
+
+def test_prefill_head_dim_256_long_context_sampled_rows():
+    """head_dim 256 (one query tile per CTA, 64-key stages) over long cached contexts: every
+    row of a sample against the oracle."""
+    w = wl.build_workload("pf256", 25_625, dtype=wl.BF16, n_q_heads=16, n_kv_heads=8, head_dim=256,
+                          prefill_q_lens=[300, 129, 64], prefill_ctx_lens=[2500, 700, 4000], extra_blocks=3)
+    got = bits_of(run_prefill(w))
+    rows = np.arange(0, w.prefill.q.shape[0], 7)
+    check(got[rows], oracle_rows(w, rows), wl.BF16, "prefill hd 256 long")
+    assert pa.pa_device_errors(clear=True) == 0
