@@ -12,13 +12,15 @@
 //    owns two consecutive query tiles of one (chunk, KV head): both read the same K/V tiles.
 //    At head_dim 256 a CTA owns one query tile and streams K/V in stages of 64 keys (its O
 //    accumulator takes 256 TMEM columns, and two stages of K and V must fit beside Q).
-//  * Two producer warps (one for K, one for V) gather tiles of 128 keys (8 paged blocks) with
-//    one 4-D TMA load per block and 64-column slab, 128-byte swizzled, into two-stage rings.
+//  * Two producer warps (one for K, one for V) gather stages of 128 keys (64 at head_dim 256)
+//    with one 4-D TMA load per 16-token chunk (or 8-token block) and 64-column slab, 128-byte
+//    swizzled, into two-stage rings.
 //    Block ids come from the chunk's block-table row; blocks past the sequence load zeros
 //    (out-of-range block coordinate); the V producer zeroes the stray rows of the sequence's
 //    last, partial block before it hands the last stage over.
 //  * TMEM (512 columns): for each query tile t two 64-column S buffers at 128 t and the O
-//    accumulator (head_dim columns; head_dim 64 or 128) at 256 + head_dim t.  Keys are processed in 64-key sub-tiles u: S_t(u) = Q_t K^T
+//    accumulator (head_dim columns) at 256 + head_dim t.  Keys are processed in 64-key
+//    sub-tiles u: S_t(u) = Q_t K^T
 //    (both operands from shared memory, K-major) lands in buffer u % 2, so the next
 //    sub-tile's S is computed while the softmax works on this one; O_t += P_t(u) V reads the
 //    weights from TMEM (the A operand) and V from shared memory (MN-major).
