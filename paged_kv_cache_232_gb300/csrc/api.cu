@@ -185,11 +185,19 @@ int decode_impl(void* out, const void* q, const void* k_cache, const void* v_cac
         p.part_tokens = 0;
         p.max_parts = 1;
         // longest-first order pays only when the grid is longer than one wave of resident CTAs,
-        // and needs its scratch (lengths + a chunk-count histogram) to fit in the ring
+        // and needs its scratch (lengths + a chunk-count histogram) to fit in the ring; from two
+        // waves on, at group size 1 or 2, one CTA per resident slot runs a list of units
+        // (decode_kernel_persistent: no start-up per unit, the next unit's loads overlap this
+        // one's merge) when the lists fit
         const int resident = pa::decode_resident_ctas(dtype == PA_BF16, kernel_dim(head_dim), n_q_heads / n_kv_heads);
-        const int64_t scratch = (int64_t)num_seqs + ((int64_t)max_blocks_per_seq * block_size + 15) / 16 + 2;
-        p.lpt = (resident > 0 && units > (int64_t)dev->sm_count * resident &&
-                 scratch * 4 <= pa::decode_ring_bytes(kernel_dim(head_dim))) ? 1 : 0;
+        const int64_t slots = (int64_t)dev->sm_count * resident;
+        const int64_t nb = ((int64_t)max_blocks_per_seq * block_size + 15) / 16 + 2;
+        const int ring = pa::decode_ring_bytes(kernel_dim(head_dim));
+        p.lpt = (resident > 0 && units > slots && ((int64_t)num_seqs + nb) * 4 <= ring) ? 1 : 0;
+        p.persist = (p.lpt && n_q_heads / n_kv_heads <= 2 && units >= 2 * slots &&
+                     units <= (int64_t)pa::decode_list_max() * slots && (2 * (int64_t)num_seqs + 2 * nb) * 4 <= ring)
+                        ? 1 : 0;
+        if (p.persist) grid = (int)slots;
     }
     CUtensorMap tk, tv;
     if ((st = encode_cache_map(&tk, k_cache, dtype, num_blocks, block_size, n_kv_heads, head_dim)) != PA_OK) return st;

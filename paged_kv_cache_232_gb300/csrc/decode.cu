@@ -3,8 +3,8 @@
 
 namespace pa {
 
-// per instantiation: the devices whose shared-memory limit for the kernel has been raised
-template <int D, int G, bool BF16>
+// per kernel instantiation: the devices whose shared-memory limit for it has been raised
+template <int D, int G, bool BF16, bool PERSIST>
 static std::atomic<unsigned long long>& smem_flag() {
     static std::atomic<unsigned long long> f{0};
     return f;
@@ -21,7 +21,8 @@ static int resident_t() {
     if (r > 0) return r;
     using C = DecodeCfg<D, G, BF16>;
     auto kern = decode_kernel<D, G, BF16>;
-    if (smem_limit_once(reinterpret_cast<const void*>(kern), C::SMEM_BYTES, smem_flag<D, G, BF16>()) != cudaSuccess)
+    if (smem_limit_once(reinterpret_cast<const void*>(kern), C::SMEM_BYTES, smem_flag<D, G, BF16, false>()) !=
+        cudaSuccess)
         return 0;
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&r, kern, C::THREADS, C::SMEM_BYTES) != cudaSuccess || r < 1)
         return 0;
@@ -33,10 +34,23 @@ template <int D, int G, bool BF16>
 static cudaError_t launch_decode_t(const DecodeParams& p, const CUtensorMap& tmK, const CUtensorMap& tmV, int grid,
                                    bool with_reduce, cudaStream_t st) {
     using C = DecodeCfg<D, G, BF16>;
-    auto kern = decode_kernel<D, G, BF16>;
-    cudaError_t e = smem_limit_once(reinterpret_cast<const void*>(kern), C::SMEM_BYTES, smem_flag<D, G, BF16>());
-    if (e != cudaSuccess) return e;
-    kern<<<grid, C::THREADS, C::SMEM_BYTES, st>>>(p, tmK, tmV);
+    cudaError_t e;
+    if (p.persist) {
+        // group sizes 1 and 2 only: larger groups run out of registers in the unit loop
+        if constexpr (G <= 2) {
+            auto kern = decode_kernel_persistent<D, G, BF16>;
+            e = smem_limit_once(reinterpret_cast<const void*>(kern), C::P_SMEM_BYTES, smem_flag<D, G, BF16, true>());
+            if (e != cudaSuccess) return e;
+            kern<<<grid, C::THREADS, C::P_SMEM_BYTES, st>>>(p, tmK, tmV);
+        } else {
+            return cudaErrorInvalidValue;
+        }
+    } else {
+        auto kern = decode_kernel<D, G, BF16>;
+        e = smem_limit_once(reinterpret_cast<const void*>(kern), C::SMEM_BYTES, smem_flag<D, G, BF16, false>());
+        if (e != cudaSuccess) return e;
+        kern<<<grid, C::THREADS, C::SMEM_BYTES, st>>>(p, tmK, tmV);
+    }
     e = cudaGetLastError();
     if (e != cudaSuccess || !with_reduce) return e;
     const size_t red_smem = (size_t)(((p.max_parts + 3) & ~3) + 8 * D) * sizeof(float);

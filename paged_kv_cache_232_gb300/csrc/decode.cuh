@@ -47,6 +47,7 @@ struct DecodeParams {
     float qk_scale_log2;       // scale * log2(e)
     int hd;                    // head_dim of q, out and the cache (<= D; columns hd .. D-1 are zero)
     int lpt;                   // one-pass grid only: CTAs take sequences longest first
+    int persist;               // one-pass grid only: decode_kernel_persistent, gridDim.x CTAs run unit lists
 };
 
 // Longest-first order of the one-pass grid: sequences ranked by 16-token chunk count
@@ -108,6 +109,72 @@ __device__ __forceinline__ int seq_at_rank(const DecodeParams& p, int r, int* sc
     return 0;  // not reached: r < S
 }
 
+// The persistent grid's unit lists: the (sequence, KV head) units ranked as in seq_at_rank
+// (unit rank r = sequence rank r / Hkv, KV head r mod Hkv); CTA c of P takes ranks
+// c, 2P - 1 - c, 2P + c, 4P - 1 - c, ... (a snake over the longest-first order, so that every
+// CTA's list sums to about the same length).  scratch (ints, 2 S + 2 (cap/16 + 1) of them) is
+// shared memory nothing else uses yet; all threads call this; list gets (seq, KV head, 0) per
+// unit; returns the count (valid in thread 0).
+__device__ __forceinline__ int lpt_units(const DecodeParams& p, int* scratch, int* list, int list_max) {
+    const int S = p.num_seqs, tid = threadIdx.x, lane = tid & 31;
+    const int cap = table_row_tokens(p.max_blocks_per_seq, p.cpb_log2);
+    const int nb = (cap + 15) / 16 + 1;
+    int* len = scratch;        // chunk count per sequence
+    int* hist = len + S;       // sequences per chunk count
+    int* start = hist + nb;    // first rank of each chunk count
+    int* order = start + nb;   // sequence at each rank
+    for (int i = tid; i < nb; i += blockDim.x) hist[i] = 0;
+    for (int i = tid; i < S; i += blockDim.x) {
+        int L = __ldg(p.context_lens + i);
+        L = L < 0 ? 0 : min(L, cap);
+        len[i] = (L + 15) >> 4;
+    }
+    __syncthreads();
+    for (int i = tid; i < S; i += blockDim.x) atomicAdd(&hist[len[i]], 1);
+    __syncthreads();
+    if (tid < 32) {
+        // descending exclusive scan: start[k] = sequences with more than k chunks
+        int before = 0;
+        for (int top = nb - 1; top >= 0; top -= 32) {
+            const int k = top - lane;
+            const int v = (k >= 0) ? hist[k] : 0;
+            int incl = v;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int y = __shfl_up_sync(0xffffffffu, incl, o);
+                if (lane >= o) incl += y;
+            }
+            if (k >= 0) start[k] = before + incl - v;
+            before += __shfl_sync(0xffffffffu, incl, 31);
+        }
+        __syncwarp();
+        // stable placement in index order, 32 sequences at a time
+        for (int base = 0; base < S; base += 32) {
+            const int i = base + lane;
+            const int key = i < S ? len[i] : -1;
+            const unsigned same = __match_any_sync(0xffffffffu, key);
+            if (i < S) order[start[key] + __popc(same & ((1u << lane) - 1u))] = i;
+            __syncwarp();
+            if (i < S && lane == __ffs(same) - 1) start[key] += __popc(same);
+            __syncwarp();
+        }
+    }
+    __syncthreads();
+    int n = 0;
+    if (tid == 0) {
+        const int P = (int)gridDim.x, c = (int)blockIdx.x, units = S * p.n_kv_heads;
+        for (int k = 0; n < list_max; ++k) {
+            const int r = k * P + ((k & 1) ? P - 1 - c : c);
+            if (r >= units) break;
+            list[3 * n] = order[r / p.n_kv_heads];
+            list[3 * n + 1] = r % p.n_kv_heads;
+            list[3 * n + 2] = 0;
+            ++n;
+        }
+    }
+    return n;
+}
+
 template <int D, int G, bool BF16>
 struct DecodeCfg {
     static constexpr int BS = 16;
@@ -133,6 +200,14 @@ struct DecodeCfg {
     static constexpr int SLOT_OFF = BAR_OFF + 2 * NST * 8;           // the sequence picked by the order step
     static constexpr int SMEM_BYTES = SLOT_OFF + 16 + 1024;           // + alignment slack
     static_assert(MERGE_BYTES <= RING_BYTES, "merge area must fit in the ring");
+    // decode_kernel_persistent: ring | p buffers | alpha | merge area (the ring keeps streaming the
+    // next unit during a merge) | barriers | unit list | flags
+    static constexpr int P_MERGE_OFF = RING_BYTES + P_BYTES + A_BYTES;
+    static constexpr int P_BAR_OFF = P_MERGE_OFF + MERGE_BYTES;
+    static constexpr int LIST_MAX = 32;                                 // units one persistent CTA may run
+    static constexpr int P_LIST_OFF = P_BAR_OFF + 2 * NST * 8;          // [LIST_MAX][3] (seq, KV head, 0)
+    static constexpr int P_FLAG_OFF = P_LIST_OFF + LIST_MAX * 3 * 4;    // unit count, abort flag
+    static constexpr int P_SMEM_BYTES = P_FLAG_OFF + 16 + 1024;
     // Consumer warp w takes blocks b = w, w + NCW, ...; with NST a multiple of NCW every ring stage
     // belongs to one warp, which waits on its phases in order -- a stage's full barrier is then
     // never two phases behind the phase its warp waits for (where the parity test would pass early).
@@ -537,6 +612,386 @@ decode_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmK, con
             }
         }
     }
+}
+
+// The persistent one-pass grid (p.persist): gridDim.x CTAs (one per resident slot), each running
+// the list of (sequence, KV head) units lpt_units gives it, whole contexts, no split-K.  The
+// producer streams the next unit's blocks into the ring while the consumers merge this one, and
+// no CTA pays the start-up (barriers, ordering) more than once.  The per-block work is that of
+// decode_kernel.
+template <int D, int G, bool BF16>
+__global__ void __launch_bounds__(DecodeCfg<D, G, BF16>::THREADS,
+                                  D == 256 ? (G <= 2 ? 2 : 1) : ((G <= 4) ? 3 : (D == 64 ? 2 : 1)))
+decode_kernel_persistent(const DecodeParams p, const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV) {
+    using C = DecodeCfg<D, G, BF16>;
+    using F = F16x2<BF16>;
+    extern __shared__ __align__(1024) unsigned char smem_raw[];
+    // 1024-byte alignment for the 128-byte swizzle pattern of TMA
+    unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const uint32_t ring = smem_addr(smem);
+    float* p_buf = reinterpret_cast<float*>(smem + C::RING_BYTES);
+    float* a_buf = reinterpret_cast<float*>(smem + C::RING_BYTES + C::P_BYTES);
+    const uint32_t bar_full = ring + C::P_BAR_OFF;
+    const uint32_t bar_empty = bar_full + C::NST * 8;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int units = p.num_seqs * p.n_kv_heads;
+    int* list = reinterpret_cast<int*>(smem + C::P_LIST_OFF);
+    volatile int* flags = reinterpret_cast<volatile int*>(smem + C::P_FLAG_OFF);  // [0] units, [1] abort
+
+    // ---- the units this CTA runs
+    {
+        const int n = lpt_units(p, reinterpret_cast<int*>(smem), list, C::LIST_MAX);
+        if (threadIdx.x == 0) flags[0] = n;
+    }
+    if (threadIdx.x == 0) {
+        flags[1] = 0;
+        for (int i = 0; i < C::NST; ++i) {
+            mbar_init(bar_full + 8 * i, 1);
+            mbar_init(bar_empty + 8 * i, 1);
+        }
+        fence_barrier_init();
+    }
+    fence_proxy_async_smem();  // the ordering scratch (ring) is written by TMA next
+    __syncthreads();
+    const int n_units = flags[0];
+
+    // context length, clamped to what the table (and the split-K grid) can address; the unit's
+    // token range [t_begin, t_end) and 16-token chunk count
+    const int cap_table = table_row_tokens(p.max_blocks_per_seq, p.cpb_log2);
+    const int cap = (p.part_tokens > 0 && p.max_parts * p.part_tokens < cap_table) ? p.max_parts * p.part_tokens
+                                                                                    : cap_table;
+    struct Unit {
+        int s, g, piece, L, t_begin, t_end, nblk, blk0;
+        bool direct, skip;
+    };
+    auto unit_at = [&](int k, bool report) {
+        Unit u;
+        u.s = list[3 * k];
+        u.g = list[3 * k + 1];
+        u.piece = list[3 * k + 2];
+        int L = __ldg(p.context_lens + u.s);
+        if (L < 0 || L > cap) {
+            if (report && u.piece == 0 && u.g == 0 && threadIdx.x == 0) flag_error(p.err, PA_DEVERR_LENGTH);
+            L = L < 0 ? 0 : cap;
+        }
+        u.L = L;
+        u.t_begin = p.part_tokens > 0 ? u.piece * p.part_tokens : 0;
+        u.t_end = p.part_tokens > 0 ? min(L, u.t_begin + p.part_tokens) : L;
+        const int n_parts = p.part_tokens > 0 ? (L + p.part_tokens - 1) / p.part_tokens : 1;
+        u.skip = (u.t_begin >= u.t_end && u.piece > 0);  // split-K piece past this sequence's context
+        u.nblk = u.skip ? 0 : (u.t_end - u.t_begin + C::BS - 1) / C::BS;
+        u.blk0 = u.t_begin / C::BS;
+        u.direct = (n_parts <= 1);
+        return u;
+    };
+
+    if (warp == C::NCW) {
+        // ------------------------------------------------------------ producer warp
+        if (lane == 0) {
+            tma_prefetch_desc(&tmK);
+            tma_prefetch_desc(&tmV);
+        }
+        const uint64_t pol = l2_policy_evict_first();
+        const bool half8 = p.cpb_log2 < 0;
+        const int per_load = half8 ? 16 : 32;  // chunks whose table entries one warp-wide load covers
+        bool ok = true;
+        int n_issued = 0;  // blocks (ring stages) whose loads were issued, over all units
+        for (int k = 0; k < n_units && ok; ++k) {
+            const Unit u = unit_at(k, false);
+            // 16-token chunk c of the sequence: table entry c >> cpb_log2, rows 16 (c mod 2^cpb_log2) + 0..15;
+            // with blocks of 8 tokens, entries 2c and 2c + 1 (the second only if the context reaches
+            // it), each an 8-row box, the second landing 8 rows (1 KB) further
+            const int32_t* bt = p.block_tables + (size_t)u.s * p.max_blocks_per_seq;
+            for (int b0 = 0; b0 < u.nblk && ok; b0 += per_load) {
+                const int nb = min(per_load, u.nblk - b0);
+                int my = p.num_blocks;  // outside the tensor map: TMA fills zeros
+                const int e = half8 ? 2 * (u.blk0 + b0) + lane : (u.blk0 + b0 + lane) >> p.cpb_log2;
+                if (half8 ? (lane < 2 * nb && 8 * e < u.L) : (lane < nb)) {
+                    my = __ldg(bt + e);
+                    if (my < 0 || my >= p.num_blocks) {
+                        flag_error(p.err, PA_DEVERR_BLOCK);
+                        my = p.num_blocks;
+                    }
+                }
+                for (int j = 0; j < nb; ++j) {
+                    const int blk = __shfl_sync(0xffffffffu, my, half8 ? 2 * j : j);
+                    const int blk_b = __shfl_sync(0xffffffffu, my, (2 * j + 1) & 31);  // half8 only
+                    const int gb = n_issued;
+                    const int st = gb % C::NST;
+                    const uint32_t ph = (gb / C::NST) & 1;
+                    if (lane == 0) {
+                        // chunk's first row in its block
+                        const int row0 = half8 ? 0 : ((u.blk0 + b0 + j) & ((1 << p.cpb_log2) - 1)) * C::BS;
+                        if (gb >= C::NST && !mbar_wait(bar_empty + 8 * st, ph ^ 1, p.err)) ok = false;
+                        if (ok) {
+                            const uint32_t dst = ring + st * C::STAGE_BYTES;
+                            mbar_arrive_expect_tx(bar_full + 8 * st, C::STAGE_BYTES);
+#pragma unroll
+                            for (int kv = 0; kv < 2; ++kv) {
+                                const CUtensorMap* map = kv ? &tmV : &tmK;
+                                const uint32_t tile = dst + kv * C::TILE_BYTES;
+#pragma unroll
+                                for (int hf = 0; hf < C::HALVES; ++hf) {
+                                    tma_load_4d(tile + hf * C::SLAB_BYTES, map, hf * 64, u.g, row0, blk,
+                                                bar_full + 8 * st, pol);
+                                    if (half8)
+                                        tma_load_4d(tile + hf * C::SLAB_BYTES + 8 * 128, map, hf * 64, u.g, 0, blk_b,
+                                                    bar_full + 8 * st, pol);
+                                }
+                            }
+                        }
+                    }
+                    ok = __shfl_sync(0xffffffffu, ok, 0);
+                    if (!ok) break;
+                    n_issued = gb + 1;
+                }
+            }
+        }
+        // No load may still be landing when the CTA exits (after a time-out the consumers may not
+        // have taken every stage): wait, with the time limit, for the last phase of every stage
+        // that was filled, then release the consumers' final barrier.  Each of those phases is the
+        // one just issued or already done.
+        if (lane == 0) {
+            for (int st = 0; st < C::NST && st < n_issued; ++st) {
+                const int b_last = st + ((n_issued - 1 - st) / C::NST) * C::NST;
+                (void)mbar_wait(bar_full + 8 * st, (b_last / C::NST) & 1, p.err);
+            }
+        }
+        __syncwarp();
+        asm volatile("bar.arrive 2, %0;" ::"n"(C::THREADS) : "memory");
+        return;
+    }
+
+    // ---------------------------------------------------------------- consumer warps
+    const int tg = lane >> 3, dl = lane & 7;  // q.K layout: token group, lane within token
+    int chunk_col[C::CPL];  // first column (element index) of each of this lane's chunks
+#pragma unroll
+    for (int j = 0; j < C::CPL; ++j) {
+        // HALVES = 4: chunk dl of every slab; 2: two chunks of one slab, staggered; 1: chunk dl
+        const int half = (C::HALVES == 4) ? j : (C::HALVES == 2) ? (dl >> 2) : 0;
+        const int c = (C::HALVES == 2) ? ((2 * (dl & 3) + half + j) & 7) : dl;
+        chunk_col[j] = half * 64 + c * 8;
+    }
+    // this lane's head in the reduced-score layout, and whether it reports that head
+    const int n0 = 4 * G;
+    int my_h;
+    {
+        int base = ((lane & 4) ? n0 / 2 : 0) + ((lane & 2) ? n0 / 4 : 0) + ((n0 >= 8 && (lane & 1)) ? n0 / 8 : 0);
+        my_h = base / 4;
+    }
+    const int hmask = (G == 1) ? 0 : (G == 2) ? 4 : (G == 4) ? 6 : 7;
+    const bool rep = (tg == 0) && ((dl & ~hmask) == 0);
+    const int dg = lane % C::CR, tgp = lane / C::CR;  // P.V layout
+    float* pw = p_buf + warp * C::BS * G;
+    float* aw = a_buf + warp * 8;
+
+    bool ok = true;
+    int base_blk = 0;  // ring index of the unit's first block
+    for (int k = 0; k < n_units; ++k) {
+        int t_begin, t_end, nblk, s, g, piece;
+        bool direct;
+        // q for the G heads of this group, this lane's CPL chunks, pre-scaled by scale*log2(e)
+        float qf[G][C::CPL][8];
+        {
+            const Unit u = unit_at(k, true);
+            if (u.skip) continue;
+            t_begin = u.t_begin;
+            t_end = u.t_end;
+            nblk = u.nblk;
+            s = u.s;
+            g = u.g;
+            piece = u.piece;
+            direct = u.direct;
+            const uint16_t* qrow =
+                static_cast<const uint16_t*>(p.q) + ((size_t)u.s * p.n_q_heads + (size_t)u.g * G) * p.hd;
+#pragma unroll
+            for (int h = 0; h < G; ++h)
+#pragma unroll
+                for (int j = 0; j < C::CPL; ++j) {
+                    uint4 raw = chunk_col[j] < p.hd ? ldg_nc_128(qrow + h * p.hd + chunk_col[j])
+                                                    : make_uint4(0u, 0u, 0u, 0u);
+                    unpack8<BF16>(raw, qf[h][j]);
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) qf[h][j][e] *= p.qk_scale_log2;
+                }
+        }
+
+        float m_run = -INFINITY, l_run = 0.f;
+        float o[G][8];
+#pragma unroll
+        for (int h = 0; h < G; ++h)
+#pragma unroll
+            for (int e = 0; e < 8; ++e) o[h][e] = 0.f;
+
+        // this warp's blocks: ring indices base_blk + b with (base_blk + b) mod NCW == warp, so that a
+        // ring stage always belongs to the same warp
+        for (int b = (warp - base_blk % C::NCW + C::NCW) % C::NCW; ok && b < nblk; b += C::NCW) {
+            const int gb = base_blk + b;
+            const int st = gb % C::NST;
+            const uint32_t ph = (gb / C::NST) & 1;
+            const bool arrived = mbar_wait(bar_full + 8 * st, ph, p.err);
+            if (!__all_sync(0xffffffffu, arrived)) { ok = false; break; }  // leave the loop warp-uniformly
+            const uint32_t kt = ring + st * C::STAGE_BYTES;
+            const uint32_t vt = kt + C::TILE_BYTES;
+            const int nvalid = min(C::BS, t_end - (t_begin + b * C::BS));
+
+            // ---- q.K: 4 tokens x G heads of partial dots per lane
+            float acc[4 * G];
+#pragma unroll
+            for (int kk = 0; kk < 4 * G; ++kk) acc[kk] = 0.f;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const int t = tg + 4 * i;
+#pragma unroll
+                for (int j = 0; j < C::CPL; ++j) {
+                    const int half = chunk_col[j] >> 6, c = (chunk_col[j] >> 3) & 7;
+                    uint4 raw = lds128(kt + half * C::SLAB_BYTES + swz128(t, c));
+                    float kf[8];
+                    unpack8<BF16>(raw, kf);
+#pragma unroll
+                    for (int h = 0; h < G; ++h)
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) acc[h * 4 + i] = fmaf(qf[h][j][e], kf[e], acc[h * 4 + i]);
+                }
+            }
+            const int rbase = transpose_reduce<G>(acc, lane);
+
+            // ---- online softmax for this lane's head over the block's 16 tokens
+            float sc[C::R];
+            float bmax = -INFINITY;
+#pragma unroll
+            for (int r = 0; r < C::R; ++r) {
+                const int i = (rbase + r) & 3;
+                const int t = tg + 4 * i;
+                sc[r] = (t < nvalid) ? acc[r] : -INFINITY;
+                bmax = fmaxf(bmax, sc[r]);
+            }
+            bmax = head_max<G>(bmax);
+            const float m_new = fmaxf(m_run, bmax);
+            const float alpha = (m_new == -INFINITY) ? 1.f : ex2(m_run - m_new);
+            float psum = 0.f;
+#pragma unroll
+            for (int r = 0; r < C::R; ++r) {
+                const int i = (rbase + r) & 3;
+                const int t = tg + 4 * i;
+                const float pr = (m_new == -INFINITY) ? 0.f : ex2(sc[r] - m_new);
+                psum += pr;
+                if (G > 1 || (lane & 1) == 0) pw[t * G + my_h] = pr;
+            }
+            psum = head_sum<G>(psum);
+            l_run = l_run * alpha + psum;
+            m_run = m_new;
+            if (rep) aw[my_h] = alpha;
+            __syncwarp();
+
+            // ---- P.V: this lane's 8 columns for all G heads, its TPL tokens
+            bool rescale = false;
+            float al[G];
+#pragma unroll
+            for (int h = 0; h < G; ++h) {
+                al[h] = aw[h];
+                rescale |= (al[h] != 1.f);
+            }
+            if (__any_sync(0xffffffffu, rescale)) {
+#pragma unroll
+                for (int h = 0; h < G; ++h)
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) o[h][e] *= al[h];
+            }
+            const int half = dg >> 3, c = dg & 7;
+#pragma unroll
+            for (int i = 0; i < C::TPL; ++i) {
+                const int t = tgp + C::TGP * i;
+                if (t < nvalid) {
+                    uint4 raw = lds128(vt + half * C::SLAB_BYTES + swz128(t, c));
+                    float vf[8];
+                    unpack8<BF16>(raw, vf);
+#pragma unroll
+                    for (int h = 0; h < G; ++h) {
+                        const float pr = pw[t * G + h];
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) o[h][e] = fmaf(pr, vf[e], o[h][e]);
+                    }
+                }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar_empty + 8 * st);
+        }
+        base_blk += nblk;
+
+        // fold the token groups of the P.V layout
+#pragma unroll
+        for (int h = 0; h < G; ++h)
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                float x = o[h][e];
+                if constexpr (C::TGP >= 2) x += __shfl_xor_sync(0xffffffffu, x, C::CR);
+                if constexpr (C::TGP >= 4) x += __shfl_xor_sync(0xffffffffu, x, 2 * C::CR);
+                o[h][e] = x;
+            }
+
+        // ------------------------------------------------------------ merge the 4 warps
+        float* mo = reinterpret_cast<float*>(smem + C::P_MERGE_OFF);  // [NCW][G][D]
+        float* mm = mo + C::NCW * G * D;                             // [NCW][G]
+        float* ml = mm + C::NCW * G;                                 // [NCW][G]
+        volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::P_FLAG_OFF) + 1;
+        if (!ok) {
+            m_run = -INFINITY;
+            l_run = 0.f;
+            if (lane == 0) *abort_flag = 1;  // every consumer warp stops after this unit
+        }
+        if (tgp == 0) {
+#pragma unroll
+            for (int h = 0; h < G; ++h) {
+                float4* dst = reinterpret_cast<float4*>(mo + (warp * G + h) * D + dg * 8);
+                dst[0] = make_float4(o[h][0], o[h][1], o[h][2], o[h][3]);
+                dst[1] = make_float4(o[h][4], o[h][5], o[h][6], o[h][7]);
+            }
+        }
+        if (rep) {
+            mm[warp * G + my_h] = m_run;
+            ml[warp * G + my_h] = l_run;
+        }
+        asm volatile("bar.sync 1, %0;" ::"n"(C::NCW * 32) : "memory");
+
+        const int tid = threadIdx.x;  // 0 .. 127
+        const int hq0 = g * G;
+        for (int idx = 2 * tid; idx < G * D; idx += 2 * C::NCW * 32) {
+            const int h = idx / D, d = idx - h * D;
+            float M = -INFINITY;
+#pragma unroll
+            for (int w = 0; w < C::NCW; ++w) M = fmaxf(M, mm[w * G + h]);
+            float Lsum = 0.f, o0 = 0.f, o1 = 0.f;
+            if (M != -INFINITY) {
+#pragma unroll
+                for (int w = 0; w < C::NCW; ++w) {
+                    const float wt = ex2(mm[w * G + h] - M);
+                    Lsum = fmaf(ml[w * G + h], wt, Lsum);
+                    o0 = fmaf(mo[(w * G + h) * D + d], wt, o0);
+                    o1 = fmaf(mo[(w * G + h) * D + d + 1], wt, o1);
+                }
+            }
+            const float inv = (Lsum > 0.f) ? 1.f / Lsum : 0.f;
+            const size_t row = (size_t)s * p.n_q_heads + hq0 + h;
+            if (direct) {
+                uint32_t packed = F::pack_rn(o0 * inv, o1 * inv);
+                if (d < p.hd) *reinterpret_cast<uint32_t*>(static_cast<uint16_t*>(p.out) + row * p.hd + d) = packed;
+            } else {
+                const size_t pr = row * p.max_parts + piece;
+                *reinterpret_cast<float2*>(p.ws_o + pr * D + d) = make_float2(o0 * inv, o1 * inv);
+                if (d == 0) {
+                    p.ws_m[pr] = M * 0.69314718055994531f;  // back to natural-log units
+                    p.ws_l[pr] = Lsum;
+                }
+            }
+        }
+        // the merge area is rewritten by the next unit; every warp has seen the abort flag
+        asm volatile("bar.sync 1, %0;" ::"n"(C::NCW * 32) : "memory");
+        if (*abort_flag) break;
+    }
+    // the producer has seen every load land (barrier 2 counts it too)
+    asm volatile("bar.sync 2, %0;" ::"n"(C::THREADS) : "memory");
 }
 
 // Split-K merge (mini_engine, "Custom CUDA kernels", v2 reduce): for each (s, h) with more

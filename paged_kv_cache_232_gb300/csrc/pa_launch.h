@@ -35,6 +35,10 @@ inline int decode_ring_bytes(int head_dim) {
                              : DecodeCfg<64, 1, true>::RING_BYTES;
 }
 
+// Units one CTA of the persistent decode grid can run.
+inline int decode_list_max() { return DecodeCfg<128, 1, true>::LIST_MAX; }
+
+
 // CTAs of the decode kernel for (dtype, head_dim, group) that fit on one SM (0 on a CUDA error);
 // queried once per device, so a call inside a stream capture makes no CUDA call.
 int decode_resident_ctas(int bf16, int head_dim, int group);

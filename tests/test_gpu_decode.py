@@ -275,3 +275,19 @@ def test_head_dim_256_batch_longer_than_a_wave():
     for mode in ("auto", "splitk"):
         check(Dev(w).run(mode), ref, w.pool.dtype, f"hd 256 {mode}")
     assert pa.pa_device_errors(clear=True) == 0
+
+
+@pytest.mark.parametrize("dt,hq,hkv,d,bs", [(wl.BF16, 16, 8, 128, 8), (wl.F16, 8, 8, 96, 32), (wl.BF16, 16, 8, 64, 16),
+                                            (wl.F16, 4, 2, 256, 16)])
+def test_many_short_sequences_persistent_grid(dt, hq, hkv, d, bs):
+    """More than two waves of (sequence, KV head) units at group size <= 2: the dispatcher's
+    one-pass grid runs one CTA per resident slot over longest-first unit lists.  Lengths from 0
+    to 300 (empty contexts included), NaN in every unowned slot."""
+    S = 400 if d != 256 else 700
+    lens = wl.uniform_ints(wl.derive_seed(4242 + d + bs, 1), S, 0, 300).tolist()
+    w = wl.build_workload("many", 4242 + d + bs, dtype=dt, n_q_heads=hq, n_kv_heads=hkv, head_dim=d, block_size=bs,
+                          decode_lens=lens, extra_blocks=2)
+    pa.pa_device_errors(clear=True)
+    got = Dev(w).run("auto")
+    check(got, oracle_decode(w), dt, f"many short {hq}/{hkv} hd {d} bs {bs}")
+    assert pa.pa_device_errors(clear=True) == 0
