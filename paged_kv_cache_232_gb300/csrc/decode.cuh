@@ -269,6 +269,101 @@ __device__ __forceinline__ float head_sum(float x) {
     return x;
 }
 
+// One 16-token chunk of K and V (the ring stage at kt, nvalid tokens valid): q.K for the G
+// heads, the online-softmax update of (m_run, l_run) and o, and P.V into o.  Shared by
+// decode_kernel and decode_kernel_persistent; the caller waits for the stage and releases it.
+template <int D, int G, bool BF16>
+__device__ __forceinline__ void consume_chunk(const uint32_t kt, const int nvalid,
+                                              const float (&qf)[G][DecodeCfg<D, G, BF16>::CPL][8],
+                                              const int (&chunk_col)[DecodeCfg<D, G, BF16>::CPL], const int lane,
+                                              const int my_h, const bool rep, float* pw, float* aw, float& m_run,
+                                              float& l_run, float (&o)[G][8]) {
+    using C = DecodeCfg<D, G, BF16>;
+    const int tg = lane >> 3;
+    const int dg = lane % C::CR, tgp = lane / C::CR;  // P.V layout
+    const uint32_t vt = kt + C::TILE_BYTES;
+
+    // ---- q.K: 4 tokens x G heads of partial dots per lane
+    float acc[4 * G];
+#pragma unroll
+    for (int k = 0; k < 4 * G; ++k) acc[k] = 0.f;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const int t = tg + 4 * i;
+#pragma unroll
+        for (int j = 0; j < C::CPL; ++j) {
+            const int half = chunk_col[j] >> 6, c = (chunk_col[j] >> 3) & 7;
+            uint4 raw = lds128(kt + half * C::SLAB_BYTES + swz128(t, c));
+            float kf[8];
+            unpack8<BF16>(raw, kf);
+#pragma unroll
+            for (int h = 0; h < G; ++h)
+#pragma unroll
+                for (int e = 0; e < 8; ++e) acc[h * 4 + i] = fmaf(qf[h][j][e], kf[e], acc[h * 4 + i]);
+        }
+    }
+    const int base = transpose_reduce<G>(acc, lane);
+
+    // ---- online softmax for this lane's head over the block's 16 tokens
+    float sc[C::R];
+    float bmax = -INFINITY;
+#pragma unroll
+    for (int r = 0; r < C::R; ++r) {
+        const int i = (base + r) & 3;
+        const int t = tg + 4 * i;
+        sc[r] = (t < nvalid) ? acc[r] : -INFINITY;
+        bmax = fmaxf(bmax, sc[r]);
+    }
+    bmax = head_max<G>(bmax);
+    const float m_new = fmaxf(m_run, bmax);
+    const float alpha = (m_new == -INFINITY) ? 1.f : ex2(m_run - m_new);
+    float psum = 0.f;
+#pragma unroll
+    for (int r = 0; r < C::R; ++r) {
+        const int i = (base + r) & 3;
+        const int t = tg + 4 * i;
+        const float pr = (m_new == -INFINITY) ? 0.f : ex2(sc[r] - m_new);
+        psum += pr;
+        if (G > 1 || (lane & 1) == 0) pw[t * G + my_h] = pr;
+    }
+    psum = head_sum<G>(psum);
+    l_run = l_run * alpha + psum;
+    m_run = m_new;
+    if (rep) aw[my_h] = alpha;
+    __syncwarp();
+
+    // ---- P.V: this lane's 8 columns for all G heads, its TPL tokens
+    bool rescale = false;
+    float al[G];
+#pragma unroll
+    for (int h = 0; h < G; ++h) {
+        al[h] = aw[h];
+        rescale |= (al[h] != 1.f);
+    }
+    if (__any_sync(0xffffffffu, rescale)) {
+#pragma unroll
+        for (int h = 0; h < G; ++h)
+#pragma unroll
+            for (int e = 0; e < 8; ++e) o[h][e] *= al[h];
+    }
+    const int half = dg >> 3, c = dg & 7;
+#pragma unroll
+    for (int i = 0; i < C::TPL; ++i) {
+        const int t = tgp + C::TGP * i;
+        if (t < nvalid) {
+            uint4 raw = lds128(vt + half * C::SLAB_BYTES + swz128(t, c));
+            float vf[8];
+            unpack8<BF16>(raw, vf);
+#pragma unroll
+            for (int h = 0; h < G; ++h) {
+                const float pr = pw[t * G + h];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) o[h][e] = fmaf(pr, vf[e], o[h][e]);
+            }
+        }
+    }
+}
+
 // Resident CTAs per SM the register allocation must allow: shared memory fits three; G <= 4
 // fits in the resulting 136 registers without spills (G = 4 would otherwise take ~150 and lose
 // a third of the warps); G = 8 at head_dim 64 fits two, at head_dim 128 only one without spills.
@@ -462,88 +557,8 @@ decode_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmK, con
         const bool arrived = mbar_wait(bar_full + 8 * st, ph, p.err);
         if (!__all_sync(0xffffffffu, arrived)) { ok = false; break; }  // leave the loop warp-uniformly
         const uint32_t kt = ring + st * C::STAGE_BYTES;
-        const uint32_t vt = kt + C::TILE_BYTES;
         const int nvalid = min(C::BS, t_end - (t_begin + b * C::BS));
-
-        // ---- q.K: 4 tokens x G heads of partial dots per lane
-        float acc[4 * G];
-#pragma unroll
-        for (int k = 0; k < 4 * G; ++k) acc[k] = 0.f;
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const int t = tg + 4 * i;
-#pragma unroll
-            for (int j = 0; j < C::CPL; ++j) {
-                const int half = chunk_col[j] >> 6, c = (chunk_col[j] >> 3) & 7;
-                uint4 raw = lds128(kt + half * C::SLAB_BYTES + swz128(t, c));
-                float kf[8];
-                unpack8<BF16>(raw, kf);
-#pragma unroll
-                for (int h = 0; h < G; ++h)
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) acc[h * 4 + i] = fmaf(qf[h][j][e], kf[e], acc[h * 4 + i]);
-            }
-        }
-        const int base = transpose_reduce<G>(acc, lane);
-
-        // ---- online softmax for this lane's head over the block's 16 tokens
-        float sc[C::R];
-        float bmax = -INFINITY;
-#pragma unroll
-        for (int r = 0; r < C::R; ++r) {
-            const int i = (base + r) & 3;
-            const int t = tg + 4 * i;
-            sc[r] = (t < nvalid) ? acc[r] : -INFINITY;
-            bmax = fmaxf(bmax, sc[r]);
-        }
-        bmax = head_max<G>(bmax);
-        const float m_new = fmaxf(m_run, bmax);
-        const float alpha = (m_new == -INFINITY) ? 1.f : ex2(m_run - m_new);
-        float psum = 0.f;
-#pragma unroll
-        for (int r = 0; r < C::R; ++r) {
-            const int i = (base + r) & 3;
-            const int t = tg + 4 * i;
-            const float pr = (m_new == -INFINITY) ? 0.f : ex2(sc[r] - m_new);
-            psum += pr;
-            if (G > 1 || (lane & 1) == 0) pw[t * G + my_h] = pr;
-        }
-        psum = head_sum<G>(psum);
-        l_run = l_run * alpha + psum;
-        m_run = m_new;
-        if (rep) aw[my_h] = alpha;
-        __syncwarp();
-
-        // ---- P.V: this lane's 8 columns for all G heads, its TPL tokens
-        bool rescale = false;
-        float al[G];
-#pragma unroll
-        for (int h = 0; h < G; ++h) {
-            al[h] = aw[h];
-            rescale |= (al[h] != 1.f);
-        }
-        if (__any_sync(0xffffffffu, rescale)) {
-#pragma unroll
-            for (int h = 0; h < G; ++h)
-#pragma unroll
-                for (int e = 0; e < 8; ++e) o[h][e] *= al[h];
-        }
-        const int half = dg >> 3, c = dg & 7;
-#pragma unroll
-        for (int i = 0; i < C::TPL; ++i) {
-            const int t = tgp + C::TGP * i;
-            if (t < nvalid) {
-                uint4 raw = lds128(vt + half * C::SLAB_BYTES + swz128(t, c));
-                float vf[8];
-                unpack8<BF16>(raw, vf);
-#pragma unroll
-                for (int h = 0; h < G; ++h) {
-                    const float pr = pw[t * G + h];
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) o[h][e] = fmaf(pr, vf[e], o[h][e]);
-                }
-            }
-        }
+        consume_chunk<D, G, BF16>(kt, nvalid, qf, chunk_col, lane, my_h, rep, pw, aw, m_run, l_run, o);
         __syncwarp();
         if (lane == 0) mbar_arrive(bar_empty + 8 * st);
     }
@@ -833,88 +848,8 @@ decode_kernel_persistent(const DecodeParams p, const __grid_constant__ CUtensorM
             const bool arrived = mbar_wait(bar_full + 8 * st, ph, p.err);
             if (!__all_sync(0xffffffffu, arrived)) { ok = false; break; }  // leave the loop warp-uniformly
             const uint32_t kt = ring + st * C::STAGE_BYTES;
-            const uint32_t vt = kt + C::TILE_BYTES;
             const int nvalid = min(C::BS, t_end - (t_begin + b * C::BS));
-
-            // ---- q.K: 4 tokens x G heads of partial dots per lane
-            float acc[4 * G];
-#pragma unroll
-            for (int kk = 0; kk < 4 * G; ++kk) acc[kk] = 0.f;
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const int t = tg + 4 * i;
-#pragma unroll
-                for (int j = 0; j < C::CPL; ++j) {
-                    const int half = chunk_col[j] >> 6, c = (chunk_col[j] >> 3) & 7;
-                    uint4 raw = lds128(kt + half * C::SLAB_BYTES + swz128(t, c));
-                    float kf[8];
-                    unpack8<BF16>(raw, kf);
-#pragma unroll
-                    for (int h = 0; h < G; ++h)
-#pragma unroll
-                        for (int e = 0; e < 8; ++e) acc[h * 4 + i] = fmaf(qf[h][j][e], kf[e], acc[h * 4 + i]);
-                }
-            }
-            const int rbase = transpose_reduce<G>(acc, lane);
-
-            // ---- online softmax for this lane's head over the block's 16 tokens
-            float sc[C::R];
-            float bmax = -INFINITY;
-#pragma unroll
-            for (int r = 0; r < C::R; ++r) {
-                const int i = (rbase + r) & 3;
-                const int t = tg + 4 * i;
-                sc[r] = (t < nvalid) ? acc[r] : -INFINITY;
-                bmax = fmaxf(bmax, sc[r]);
-            }
-            bmax = head_max<G>(bmax);
-            const float m_new = fmaxf(m_run, bmax);
-            const float alpha = (m_new == -INFINITY) ? 1.f : ex2(m_run - m_new);
-            float psum = 0.f;
-#pragma unroll
-            for (int r = 0; r < C::R; ++r) {
-                const int i = (rbase + r) & 3;
-                const int t = tg + 4 * i;
-                const float pr = (m_new == -INFINITY) ? 0.f : ex2(sc[r] - m_new);
-                psum += pr;
-                if (G > 1 || (lane & 1) == 0) pw[t * G + my_h] = pr;
-            }
-            psum = head_sum<G>(psum);
-            l_run = l_run * alpha + psum;
-            m_run = m_new;
-            if (rep) aw[my_h] = alpha;
-            __syncwarp();
-
-            // ---- P.V: this lane's 8 columns for all G heads, its TPL tokens
-            bool rescale = false;
-            float al[G];
-#pragma unroll
-            for (int h = 0; h < G; ++h) {
-                al[h] = aw[h];
-                rescale |= (al[h] != 1.f);
-            }
-            if (__any_sync(0xffffffffu, rescale)) {
-#pragma unroll
-                for (int h = 0; h < G; ++h)
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) o[h][e] *= al[h];
-            }
-            const int half = dg >> 3, c = dg & 7;
-#pragma unroll
-            for (int i = 0; i < C::TPL; ++i) {
-                const int t = tgp + C::TGP * i;
-                if (t < nvalid) {
-                    uint4 raw = lds128(vt + half * C::SLAB_BYTES + swz128(t, c));
-                    float vf[8];
-                    unpack8<BF16>(raw, vf);
-#pragma unroll
-                    for (int h = 0; h < G; ++h) {
-                        const float pr = pw[t * G + h];
-#pragma unroll
-                        for (int e = 0; e < 8; ++e) o[h][e] = fmaf(pr, vf[e], o[h][e]);
-                    }
-                }
-            }
+            consume_chunk<D, G, BF16>(kt, nvalid, qf, chunk_col, lane, my_h, rep, pw, aw, m_run, l_run, o);
             __syncwarp();
             if (lane == 0) mbar_arrive(bar_empty + 8 * st);
         }
