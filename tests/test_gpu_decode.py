@@ -291,3 +291,25 @@ def test_many_short_sequences_persistent_grid(dt, hq, hkv, d, bs):
     got = Dev(w).run("auto")
     check(got, oracle_decode(w), dt, f"many short {hq}/{hkv} hd {d} bs {bs}")
     assert pa.pa_device_errors(clear=True) == 0
+
+
+def test_persistent_grid_flags_bad_entries_and_finishes_the_rest():
+    """The persistent one-pass grid with an out-of-pool block id in one sequence and a context
+    longer than the table in another: both are flagged, no fault, every other row is right."""
+    lens = wl.uniform_ints(wl.derive_seed(5151, 1), 300, 10, 300).tolist()
+    w = wl.build_workload("pbad", 5151, dtype=wl.BF16, n_q_heads=16, n_kv_heads=8, head_dim=128, decode_lens=lens,
+                          extra_blocks=2)
+    d = Dev(w)
+    bt = w.decode.block_tables.copy()
+    bt[5, 0] = w.pool.num_blocks + 3
+    d.bt = to_dev_i(bt, torch.int32)
+    cl = w.decode.context_lens.copy()
+    cl[7] = 1_000_000
+    pa.pa_device_errors(clear=True)
+    got = d.run("auto", cl=to_dev_i(cl, torch.int32)).reshape(300, 16, 128)
+    errs = pa.pa_device_errors(clear=True)
+    assert errs & pa.PA_DEVERR_BLOCK and errs & pa.PA_DEVERR_LENGTH
+    ex, cd = oracle_decode(w)
+    keep = np.array([i for i in range(300) if i not in (5, 7)])
+    check_attention(got[keep], ex.reshape(300, 16, 128)[keep], wl.BF16, "persistent grid, good rows",
+                    cond=cd.reshape(300, 16, 128)[keep])
