@@ -650,7 +650,6 @@ decode_kernel_persistent(const DecodeParams p, const __grid_constant__ CUtensorM
     const uint32_t bar_empty = bar_full + C::NST * 8;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int units = p.num_seqs * p.n_kv_heads;
     int* list = reinterpret_cast<int*>(smem + C::P_LIST_OFF);
     volatile int* flags = reinterpret_cast<volatile int*>(smem + C::P_FLAG_OFF);  // [0] units, [1] abort
 
@@ -671,33 +670,23 @@ decode_kernel_persistent(const DecodeParams p, const __grid_constant__ CUtensorM
     __syncthreads();
     const int n_units = flags[0];
 
-    // context length, clamped to what the table (and the split-K grid) can address; the unit's
-    // token range [t_begin, t_end) and 16-token chunk count
-    const int cap_table = table_row_tokens(p.max_blocks_per_seq, p.cpb_log2);
-    const int cap = (p.part_tokens > 0 && p.max_parts * p.part_tokens < cap_table) ? p.max_parts * p.part_tokens
-                                                                                    : cap_table;
+    // a unit: the whole context of (sequence s, KV head g), clamped to what the table addresses,
+    // in nblk 16-token chunks
+    const int cap = table_row_tokens(p.max_blocks_per_seq, p.cpb_log2);
     struct Unit {
-        int s, g, piece, L, t_begin, t_end, nblk, blk0;
-        bool direct, skip;
+        int s, g, L, nblk;
     };
     auto unit_at = [&](int k, bool report) {
         Unit u;
         u.s = list[3 * k];
         u.g = list[3 * k + 1];
-        u.piece = list[3 * k + 2];
         int L = __ldg(p.context_lens + u.s);
         if (L < 0 || L > cap) {
-            if (report && u.piece == 0 && u.g == 0 && threadIdx.x == 0) flag_error(p.err, PA_DEVERR_LENGTH);
+            if (report && u.g == 0 && threadIdx.x == 0) flag_error(p.err, PA_DEVERR_LENGTH);
             L = L < 0 ? 0 : cap;
         }
         u.L = L;
-        u.t_begin = p.part_tokens > 0 ? u.piece * p.part_tokens : 0;
-        u.t_end = p.part_tokens > 0 ? min(L, u.t_begin + p.part_tokens) : L;
-        const int n_parts = p.part_tokens > 0 ? (L + p.part_tokens - 1) / p.part_tokens : 1;
-        u.skip = (u.t_begin >= u.t_end && u.piece > 0);  // split-K piece past this sequence's context
-        u.nblk = u.skip ? 0 : (u.t_end - u.t_begin + C::BS - 1) / C::BS;
-        u.blk0 = u.t_begin / C::BS;
-        u.direct = (n_parts <= 1);
+        u.nblk = (L + C::BS - 1) / C::BS;
         return u;
     };
 
@@ -721,7 +710,7 @@ decode_kernel_persistent(const DecodeParams p, const __grid_constant__ CUtensorM
             for (int b0 = 0; b0 < u.nblk && ok; b0 += per_load) {
                 const int nb = min(per_load, u.nblk - b0);
                 int my = p.num_blocks;  // outside the tensor map: TMA fills zeros
-                const int e = half8 ? 2 * (u.blk0 + b0) + lane : (u.blk0 + b0 + lane) >> p.cpb_log2;
+                const int e = half8 ? 2 * b0 + lane : (b0 + lane) >> p.cpb_log2;
                 if (half8 ? (lane < 2 * nb && 8 * e < u.L) : (lane < nb)) {
                     my = __ldg(bt + e);
                     if (my < 0 || my >= p.num_blocks) {
@@ -737,7 +726,7 @@ decode_kernel_persistent(const DecodeParams p, const __grid_constant__ CUtensorM
                     const uint32_t ph = (gb / C::NST) & 1;
                     if (lane == 0) {
                         // chunk's first row in its block
-                        const int row0 = half8 ? 0 : ((u.blk0 + b0 + j) & ((1 << p.cpb_log2) - 1)) * C::BS;
+                        const int row0 = half8 ? 0 : ((b0 + j) & ((1 << p.cpb_log2) - 1)) * C::BS;
                         if (gb >= C::NST && !mbar_wait(bar_empty + 8 * st, ph ^ 1, p.err)) ok = false;
                         if (ok) {
                             const uint32_t dst = ring + st * C::STAGE_BYTES;
@@ -804,20 +793,15 @@ decode_kernel_persistent(const DecodeParams p, const __grid_constant__ CUtensorM
     bool ok = true;
     int base_blk = 0;  // ring index of the unit's first block
     for (int k = 0; k < n_units; ++k) {
-        int t_begin, t_end, nblk, s, g, piece;
-        bool direct;
+        int L, nblk, s, g;
         // q for the G heads of this group, this lane's CPL chunks, pre-scaled by scale*log2(e)
         float qf[G][C::CPL][8];
         {
             const Unit u = unit_at(k, true);
-            if (u.skip) continue;
-            t_begin = u.t_begin;
-            t_end = u.t_end;
+            L = u.L;
             nblk = u.nblk;
             s = u.s;
             g = u.g;
-            piece = u.piece;
-            direct = u.direct;
             const uint16_t* qrow =
                 static_cast<const uint16_t*>(p.q) + ((size_t)u.s * p.n_q_heads + (size_t)u.g * G) * p.hd;
 #pragma unroll
@@ -848,7 +832,7 @@ decode_kernel_persistent(const DecodeParams p, const __grid_constant__ CUtensorM
             const bool arrived = mbar_wait(bar_full + 8 * st, ph, p.err);
             if (!__all_sync(0xffffffffu, arrived)) { ok = false; break; }  // leave the loop warp-uniformly
             const uint32_t kt = ring + st * C::STAGE_BYTES;
-            const int nvalid = min(C::BS, t_end - (t_begin + b * C::BS));
+            const int nvalid = min(C::BS, L - b * C::BS);
             consume_chunk<D, G, BF16>(kt, nvalid, qf, chunk_col, lane, my_h, rep, pw, aw, m_run, l_run, o);
             __syncwarp();
             if (lane == 0) mbar_arrive(bar_empty + 8 * st);
@@ -909,17 +893,9 @@ decode_kernel_persistent(const DecodeParams p, const __grid_constant__ CUtensorM
             }
             const float inv = (Lsum > 0.f) ? 1.f / Lsum : 0.f;
             const size_t row = (size_t)s * p.n_q_heads + hq0 + h;
-            if (direct) {
-                uint32_t packed = F::pack_rn(o0 * inv, o1 * inv);
-                if (d < p.hd) *reinterpret_cast<uint32_t*>(static_cast<uint16_t*>(p.out) + row * p.hd + d) = packed;
-            } else {
-                const size_t pr = row * p.max_parts + piece;
-                *reinterpret_cast<float2*>(p.ws_o + pr * D + d) = make_float2(o0 * inv, o1 * inv);
-                if (d == 0) {
-                    p.ws_m[pr] = M * 0.69314718055994531f;  // back to natural-log units
-                    p.ws_l[pr] = Lsum;
-                }
-            }
+            if (d < p.hd)
+                *reinterpret_cast<uint32_t*>(static_cast<uint16_t*>(p.out) + row * p.hd + d) =
+                    F::pack_rn(o0 * inv, o1 * inv);
         }
         // the merge area is rewritten by the next unit; every warp has seen the abort flag
         asm volatile("bar.sync 1, %0;" ::"n"(C::NCW * 32) : "memory");
