@@ -179,10 +179,12 @@ int pa_decode_plan(int num_seqs, int n_q_heads, int n_kv_heads, int head_dim, in
                    int dtype, int* partition_tokens);
 
 /*
- * pa_decode_v1 -- the one-pass decode kernel: one CTA per (sequence, KV head)
- * streams the whole context, all G query heads of the group sharing each K/V
- * load (mini_engine, "Custom CUDA kernels", v1).  Arguments as pa_decode; no
- * workspace.
+ * pa_decode_v1 -- the one-pass decode kernel: each (sequence, KV head) unit is
+ * streamed whole by one CTA, all G query heads of the group sharing each K/V
+ * load (mini_engine, "Custom CUDA kernels", v1).  When the units outnumber the
+ * CTAs resident on the device, the CTAs take the longest sequences first, and
+ * from two waves on (G <= 2) one CTA per resident slot runs a list of units.
+ * Arguments as pa_decode; no workspace.
  */
 int pa_decode_v1(void* out, const void* q, const void* k_cache, const void* v_cache, const int32_t* block_tables,
                  int max_blocks_per_seq, const int32_t* context_lens, int num_seqs, int n_q_heads,
