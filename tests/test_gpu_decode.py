@@ -69,13 +69,13 @@ def test_decode_workloads_full_size(k, mode):
     w = wl.make_workload(k)
     pa.pa_device_errors(clear=True)
     got = Dev(w).run(mode)
-    err = check(got, oracle_decode(w), w.pool.dtype, f"config{k}/{mode}")
+    err = check(got, oracle_decode(w), w.pool.dtype, f"workload {k}/{mode}")
     assert err <= 2e-3
     assert pa.pa_device_errors(clear=True) == 0
 
 
 def test_full_decode_step_batch_256_write_then_decode():
-    """Config 4: the write lands, then every sequence decodes over its context including
+    """The batch-256 step: the write lands, then every sequence decodes over its context including
     the row just written (padded rows keep the slot's previous content)."""
     w = wl.make_workload(4)
     p, b, wr = w.pool, w.decode, w.write
@@ -86,15 +86,15 @@ def test_full_decode_step_batch_256_write_then_decode():
     k2, v2, _ = oracle.kv_write(p.k_cache, p.v_cache, wr.key, wr.value, wr.slot_mapping, 16)
     assert np.array_equal(bits_of(d.kc), k2) and np.array_equal(bits_of(d.vc), v2)
     ref = oracle_decode(w, k2, v2)
-    check(got, ref, p.dtype, "config4")
+    check(got, ref, p.dtype, "step256")
     for mode in ("v1", "splitk"):
-        check(d.run(mode), ref, p.dtype, f"config4/{mode}")
+        check(d.run(mode), ref, p.dtype, f"step256/{mode}")
 
 
 def test_mixed_batch_decode_rows_with_shared_prefix():
     w = wl.make_workload(5)
     got = Dev(w).run("auto")
-    check(got, oracle_decode(w), w.pool.dtype, "config5 decode rows")
+    check(got, oracle_decode(w), w.pool.dtype, "mixed batch decode rows")
 
 
 # ------------------------------------------------------------------ edge sweeps
@@ -260,7 +260,7 @@ def test_long_context_planned_pieces_match_oracle():
     assert which == 2 and part % 16 == 0
     pa.pa_device_errors(clear=True)
     got = Dev(w).run("splitk", part)
-    check(got, oracle_decode(w), w.pool.dtype, f"config3/splitk {part}")
+    check(got, oracle_decode(w), w.pool.dtype, f"long4/splitk {part}")
     assert pa.pa_device_errors(clear=True) == 0
 
 

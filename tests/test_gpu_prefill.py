@@ -98,7 +98,7 @@ def test_prefill_single_row_no_context_returns_v0():
 
 
 def test_prefill_mixed_batch_workload_sampled_rows():
-    """Config 5's eight 512-token chunks over 0..4096 cached tokens, full size; every
+    """The mixed batch's eight 512-token chunks over 0..4096 cached tokens, full size; every
     chunk's first 16 and last 16 rows plus 24 seeded random rows are checked."""
     w = wl.make_workload(5)
     got = bits_of(run_prefill(w)).reshape(w.prefill.q.shape)
@@ -108,7 +108,7 @@ def test_prefill_mixed_batch_workload_sampled_rows():
     for c in range(8):
         rows += list(range(qsl[c], qsl[c] + 16)) + list(range(qsl[c + 1] - 16, qsl[c + 1])) + list(qsl[c] + pick[c])
     rows = np.unique(np.asarray(rows))
-    check(got[rows], oracle_rows(w, rows), wl.BF16, "config5 prefill rows")
+    check(got[rows], oracle_rows(w, rows), wl.BF16, "mixed batch prefill rows")
 
 
 def test_mixed_batch_one_output_tensor():

@@ -86,7 +86,8 @@ def check_against_oracle(w, q_bits, positions, slot_mapping=None, with_q=True, m
 
 
 def test_rope_write_decode_step_batch_256():
-    """Config 4's write with the query rows and new keys at position context_len - 1."""
+    """The batch-256 decode step's write (256 rows, 26 padded) with the query rows and new keys at
+    position context_len - 1."""
     w = wl.make_workload(4)
     b = w.decode
     pos = (b.context_lens.astype(np.int64) - 1)

@@ -338,24 +338,24 @@ def workload_seed(k: int) -> int:
 def make_workload(k: int, *, nan_canaries: bool = True) -> Workload:
     seed = workload_seed(k)
     if k == 1:
-        return build_workload("config1", seed, dtype=F16, n_q_heads=2, n_kv_heads=2, head_dim=64,
+        return build_workload("single", seed, dtype=F16, n_q_heads=2, n_kv_heads=2, head_dim=64,
                               decode_lens=[128], pool_blocks=64, nan_canaries=nan_canaries, scale=1.0 / 8.0)
     if k == 2:
         lens = uniform_ints(derive_seed(seed, TAG_LENS), 64, 100, 2048)
-        return build_workload("config2", seed, dtype=BF16, n_q_heads=16, n_kv_heads=8, head_dim=128,
+        return build_workload("decode64", seed, dtype=BF16, n_q_heads=16, n_kv_heads=8, head_dim=128,
                               decode_lens=lens, max_blocks_per_seq=128, nan_canaries=nan_canaries)
     if k == 3:
-        return build_workload("config3", seed, dtype=BF16, n_q_heads=32, n_kv_heads=8, head_dim=128,
+        return build_workload("long4", seed, dtype=BF16, n_q_heads=32, n_kv_heads=8, head_dim=128,
                               decode_lens=[32768] * 4, max_blocks_per_seq=2048, nan_canaries=nan_canaries)
     if k == 4:
         lens = uniform_ints(derive_seed(seed, TAG_LENS), 256, 100, 2048)
-        return build_workload("config4", seed, dtype=BF16, n_q_heads=16, n_kv_heads=8, head_dim=128,
+        return build_workload("step256", seed, dtype=BF16, n_q_heads=16, n_kv_heads=8, head_dim=128,
                               decode_lens=lens, max_blocks_per_seq=128, write_rows=True,
                               n_padded=int(round(0.1 * 256)), nan_canaries=nan_canaries)
     if k == 5:
         suffix = uniform_ints(derive_seed(seed, TAG_LENS), 128, 1, 1024)
         ctx = [0] + [int(x) for x in uniform_ints(derive_seed(seed, TAG_CTX), 6, 0, 4096)] + [4096]
-        return build_workload("config5", seed, dtype=BF16, n_q_heads=16, n_kv_heads=8, head_dim=128,
+        return build_workload("mixed", seed, dtype=BF16, n_q_heads=16, n_kv_heads=8, head_dim=128,
                               decode_lens=1024 + suffix, shared_prefix_blocks=64, max_blocks_per_seq=128,
                               prefill_q_lens=[512] * 8, prefill_ctx_lens=ctx, nan_canaries=nan_canaries)
     raise ValueError(f"no workload {k}")
