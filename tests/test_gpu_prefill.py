@@ -192,7 +192,7 @@ def test_unified_mixed_batch_single_launch():
     check(got[S:][rows], oracle_rows(w, rows), p.dtype, "unified: prefill rows")
 
 
-@pytest.mark.parametrize("bs", [8, 32, 64])
+@pytest.mark.parametrize("bs", [8, 32, 64, 128])
 @pytest.mark.parametrize("d", [128, 64, 256])
 def test_prefill_block_sizes(bs, d):
     w = wl.build_workload("pfbs", 950 + bs + d, dtype=wl.BF16, n_q_heads=16, n_kv_heads=8, head_dim=d, block_size=bs,
