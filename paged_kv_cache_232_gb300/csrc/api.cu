@@ -210,8 +210,8 @@ int decode_impl(void* out, const void* q, const void* k_cache, const void* v_cac
 // Dispatcher (mini_engine, "Custom CUDA kernels": split-K when few sequences or long
 // contexts cannot fill the GPU, the one-pass kernel when there is enough parallelism).
 // The thresholds are this library's, set from GB300 measurements: the one-pass kernel wins
-// as soon as there is a (sequence, KV head) unit per SM and contexts are at most 8192 tokens;
-// otherwise split-K.  The piece length sizes the grid in whole waves of resident CTAs: taking
+// from two waves of (sequence, KV head) units on (and for contexts under 1024 tokens) once
+// there is a unit per SM and contexts are at most 8192 tokens; otherwise split-K.  The piece length sizes the grid in whole waves of resident CTAs: taking
 // every context at the maximum, n equal pieces per unit cost waves(n) x (piece(n) + 64), the
 // 64 tokens standing for a CTA's pipeline start and its share of the merge (fitted to GB300
 // timings of 32 units of 32K tokens: one full wave of 2352-token pieces beats two of 1184 by
@@ -222,10 +222,18 @@ int plan(int64_t units, int max_context_len, int sm_count, int resident, int blo
     const int min_piece = PA_DEFAULT_PARTITION_TOKENS;
     if (part_tokens) *part_tokens = min_piece;
     if (max_context_len <= min_piece) return 1;
-    if (units >= sm_count && max_context_len <= 8192) return 1;
     const int64_t slots = (int64_t)sm_count * (resident > 0 ? resident : 1);
     const int64_t L = max_context_len;
     const int64_t align = block_size < 16 ? 16 : block_size;  // pieces hold whole chunks and blocks
+    if (units >= sm_count && max_context_len <= 8192) {
+        // between one and two waves of units the one-pass grid ends on a few long contexts
+        // streaming alone; quarter-context pieces keep every SM busy to the end (GB300, 64
+        // sequences of 100..2048 tokens: 62.2 us against 65.0 one-pass)
+        if (units >= 2 * slots || max_context_len < 1024) return 1;
+        const int64_t piece = std::max<int64_t>(min_piece, ((L + 3) / 4 + align - 1) / align * align);
+        if (part_tokens) *part_tokens = (int)piece;
+        return 2;
+    }
     const int n_max = (int)std::min<int64_t>((L + min_piece - 1) / min_piece, 1024);
     int64_t best = INT64_MAX;
     for (int n = 2; n <= n_max; ++n) {
