@@ -141,6 +141,18 @@ def test_decode_matches_torch_sdpa_fp64(dtype, hq, hkv, d):
     np.testing.assert_allclose(got, ref, rtol=0, atol=1e-12)
 
 
+@pytest.mark.parametrize("bs,d", [(8, 96), (32, 24), (128, 8)])
+def test_decode_matches_torch_sdpa_other_block_sizes_and_widths(bs, d):
+    """The oracle's block addressing at 8-, 32- and 128-token blocks (lengths straddling block
+    boundaries) and head widths that are not powers of two, against SDPA over gathered K/V."""
+    w = small_decode(31 + bs, [1, bs - 1, bs, bs + 1, 3 * bs + 2], hq=6, hkv=3, d=d, block_size=bs)
+    p, b = w.pool, w.decode
+    got = oracle.decode(b.q, p.k_cache, p.v_cache, b.block_tables, b.context_lens, b.scale, BF16)
+    ref = sdpa_decode(b.q, p.k_cache, p.v_cache, b.block_tables, b.context_lens, b.scale, BF16, 3)
+    np.testing.assert_allclose(got, ref, rtol=0, atol=1e-12)
+    assert np.isfinite(got).all()
+
+
 def test_paged_equals_materialised_contiguous():
     w = small_decode(21, [3, 16, 33, 64, 129], hq=6, hkv=3, d=32)
     p, b = w.pool, w.decode
