@@ -170,8 +170,10 @@ int pa_decode(void* out, const void* q, const void* k_cache, const void* v_cache
  * launching: returns 1 for the one-pass kernel, 2 for split-K, or a negative
  * status (PA_ERR_SHAPE / PA_ERR_UNSUPPORTED as pa_decode, PA_ERR_CUDA).
  * *partition_tokens (if not NULL) receives the split-K piece length: a
- * multiple of block_size and of 16, at least PA_DEFAULT_PARTITION_TOKENS, chosen so the
- * grid fills whole waves of the CTAs resident on the device's SMs.  The first
+ * multiple of block_size and of 16, at least PA_DEFAULT_PARTITION_TOKENS: a
+ * quarter of max_context_len when the (sequence, KV head) units fill between one
+ * and two waves of the CTAs resident on the device's SMs, else the length whose
+ * grid fills whole waves.  The first
  * call for a (dtype, head_dim, group) on a device queries the kernel's
  * occupancy; later calls make no CUDA call (safe inside a stream capture).
  */

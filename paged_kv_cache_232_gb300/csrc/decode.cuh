@@ -3,7 +3,7 @@
 // What is computed (mini_engine, "Custom CUDA kernels", paged decode attention v1/v2;
 // MiniLLM Runtime, "Core class relationships"): for sequence s, query head h and KV head
 // g = h / G, over tokens t of the work unit's range, each token translated through the
-// block table (physical block block_tables[s][t / 16], offset t % 16),
+// block table (physical block block_tables[s][t / block_size], offset t % block_size),
 //     out[s, h] = sum_t exp(s_t - m) V_t / sum_t exp(s_t - m),  s_t = scale * q[s, h] . K_t.
 //
 // GB300 design (not the pages' sm_80 one):
@@ -24,6 +24,10 @@
 //  * At the end the four warps' (m, l, o) are merged in shared memory and the CTA
 //    writes either the final row (rounded to nearest even) or its piece's (m, l, o) for
 //    the reduce kernel.
+//  * When the one-pass grid is longer than a wave of resident CTAs, CTAs take sequences
+//    longest first (a counting sort of the lengths in every CTA); from two waves on, at
+//    G <= 2, decode_kernel_persistent runs one CTA per resident slot over a unit list, the
+//    producer streaming the next unit while the consumers merge this one.
 #pragma once
 
 #include "pa_device.cuh"
