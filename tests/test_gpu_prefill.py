@@ -231,3 +231,14 @@ def test_prefill_head_dim_256_long_context_sampled_rows():
     rows = np.arange(0, w.prefill.q.shape[0], 7)
     check(got[rows], oracle_rows(w, rows), wl.BF16, "prefill hd 256 long")
     assert pa.pa_device_errors(clear=True) == 0
+
+
+def test_prefill_empty_chunks_between_others():
+    """Chunks with no query rows (a sequence with nothing new this step) between real ones:
+    nothing is written for them and the others are unaffected."""
+    w = wl.build_workload("pfz", 4141, dtype=wl.BF16, n_q_heads=16, n_kv_heads=8, head_dim=128,
+                          prefill_q_lens=[0, 70, 0, 5, 0], prefill_ctx_lens=[40, 300, 16, 1000, 0], extra_blocks=3)
+    pa.pa_device_errors(clear=True)
+    got = bits_of(run_prefill(w))
+    check(got, oracle_rows(w), wl.BF16, "prefill with empty chunks")
+    assert pa.pa_device_errors(clear=True) == 0
