@@ -228,7 +228,7 @@ def test_decode_block_sizes(bs, mode, part):
     if part % max(bs, 16):
         pytest.skip("split-K pieces hold whole blocks")
     lens = [1, 15, 16, 17, bs - 1, bs, bs + 1, 3 * bs + 5, 2000]
-    for dt, hq, hkv, d in [(wl.BF16, 16, 8, 128), (wl.F16, 8, 2, 64)]:
+    for dt, hq, hkv, d in [(wl.BF16, 16, 8, 128), (wl.F16, 8, 2, 64), (wl.BF16, 8, 4, 256)]:
         w = wl.build_workload("bs", 900 + bs + d, dtype=dt, n_q_heads=hq, n_kv_heads=hkv, head_dim=d, block_size=bs,
                               decode_lens=lens, extra_blocks=3)
         pa.pa_device_errors(clear=True)
