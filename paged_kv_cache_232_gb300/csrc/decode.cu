@@ -62,8 +62,19 @@ static cudaError_t launch_decode_t(const DecodeParams& p, const CUtensorMap& tmK
         e = smem_limit_once(reinterpret_cast<const void*>(rk), 227 * 1024, s_red_done);
         if (e != cudaSuccess) return e;
     }
-    rk<<<p.num_seqs * p.n_q_heads, 256, red_smem, st>>>(p);
-    return cudaGetLastError();
+    // a programmatic dependent launch: the merge grid is set up while the piece kernel drains and
+    // waits for it (griddepcontrol.wait) before reading the partials
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(p.num_seqs * p.n_q_heads));
+    cfg.blockDim = dim3(256);
+    cfg.dynamicSmemBytes = red_smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, rk, p);
 }
 
 template <int D, bool BF16>

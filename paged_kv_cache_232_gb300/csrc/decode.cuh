@@ -924,6 +924,9 @@ __global__ void __launch_bounds__(256) splitk_reduce_kernel(const DecodeParams p
     L = L < 0 ? 0 : (L > cap ? cap : L);
     const int n_parts = (L + p.part_tokens - 1) / p.part_tokens;
     if (n_parts <= 1) return;  // written directly by the piece kernel
+    // launched as a programmatic dependent of the piece kernel: its partials are complete and
+    // visible past this point
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     float* wsh = red_smem;
     float* acc = red_smem + ((p.max_parts + 3) & ~3);  // 16-byte aligned for the float4 stores
     const float* m = p.ws_m + (size_t)row * p.max_parts;
