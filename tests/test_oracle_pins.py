@@ -346,6 +346,22 @@ def test_prefill_matches_torch_sdpa_bottom_right_mask():
     np.testing.assert_allclose(got, ref, rtol=0, atol=1e-12)
 
 
+@pytest.mark.parametrize("bs,d,dt", [(8, 96, BF16), (32, 24, F16), (128, 8, BF16)])
+def test_prefill_matches_torch_sdpa_other_block_sizes_and_widths(bs, d, dt):
+    """The prefill oracle's block addressing at 8-, 32- and 128-token blocks (chunks and cached
+    contexts straddling block boundaries) and widths that are not powers of two, against SDPA
+    with the bottom-right mask over gathered K/V."""
+    w = wl.build_workload("pb", 43 + bs, dtype=dt, n_q_heads=6, n_kv_heads=3, head_dim=d, block_size=bs,
+                          prefill_q_lens=[1, bs + 1, 2 * bs - 1, 5],
+                          prefill_ctx_lens=[bs - 1, 0, bs + 3, 3 * bs])
+    pre, p = w.prefill, w.pool
+    got = oracle.prefill_chunk(pre.q, p.k_cache, p.v_cache, pre.block_tables, pre.query_start_loc, pre.seq_lens,
+                               pre.scale, dt)
+    ref = sdpa_prefill(pre, p, 3, dt)
+    np.testing.assert_allclose(got, ref, rtol=0, atol=1e-12)
+    assert np.isfinite(got).all()
+
+
 def test_prefill_row_is_a_decode_row_with_shorter_context():
     w = wl.build_workload("p", 42, dtype=BF16, n_q_heads=4, n_kv_heads=2, head_dim=16,
                           prefill_q_lens=[9, 1], prefill_ctx_lens=[23, 0])
