@@ -100,16 +100,17 @@ def test_bf16_rounding_matches_torch():
 # --------------------------------------------------------------- KV-cache write
 
 
-def test_kv_write_lands_at_block_and_offset():
-    w = wl.write_rows_case(7, 300, n_kv_heads=2, head_dim=16, block_size=16, pad_frac=0.1)
+@pytest.mark.parametrize("bs", [8, 16, 32, 128])
+def test_kv_write_lands_at_block_and_offset(bs):
+    w = wl.write_rows_case(7, 300, n_kv_heads=2, head_dim=16, block_size=bs, pad_frac=0.1)
     p, wr = w.pool, w.write
-    k, v, st = oracle.kv_write(p.k_cache, p.v_cache, wr.key, wr.value, wr.slot_mapping, 16)
+    k, v, st = oracle.kv_write(p.k_cache, p.v_cache, wr.key, wr.value, wr.slot_mapping, bs)
     assert st == oracle.OK
-    touched = np.zeros((p.num_blocks, 16), dtype=bool)
+    touched = np.zeros((p.num_blocks, bs), dtype=bool)
     for i, slot in enumerate(wr.slot_mapping):
         if slot < 0:
             continue
-        b, o = divmod(int(slot), 16)          # slot = block_id * block_size + offset
+        b, o = divmod(int(slot), bs)          # slot = block_id * block_size + offset
         assert np.array_equal(k[b, o], wr.key[i]) and np.array_equal(v[b, o], wr.value[i])
         touched[b, o] = True
     assert (wr.slot_mapping == -1).sum() == 30
