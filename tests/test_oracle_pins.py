@@ -459,3 +459,50 @@ def test_rope_kv_write_position_zero_and_row_handling(dt):
     assert np.array_equal(q2[:5], q[:5])           # position 0: identity, padded row 3 included
     assert np.array_equal(q2[7], q[7])             # out of range: untouched
     assert not np.array_equal(q2[6], q[6])
+
+
+def _rope_complex(x, m, theta):
+    """The rotation written as complex multiplication with numpy: pair i is the complex number
+    x[i] + i x[i + D/2], turned by e^{i m theta^(-2i/D)} -- independent of the oracle's code."""
+    h = x.size // 2
+    f = theta ** (-2.0 * np.arange(h) / x.size)
+    z = (x[:h] + 1j * x[h:]) * np.exp(1j * m * f)
+    return np.concatenate([z.real, z.imag])
+
+
+@pytest.mark.parametrize("dt", [BF16, F16])
+@pytest.mark.parametrize("hq,hkv,d", [(4, 2, 64), (8, 2, 128), (2, 2, 96)])
+def test_rope_kv_write_query_rows_every_head(dt, hq, hkv, d):
+    """Every head of every query row at a non-zero position equals the rounded rotation of that
+    head alone, as numpy's complex multiplication gives it (and as the oracle's exact rotation
+    gives it); a padded (-1) row still rotates its query at its own position.  Query heads and KV
+    heads differ in number, so a query branch that used the key-head count as its stride, or
+    rotated a padded row at another row's position, fails here (mini_engine, "Roadmap": RoPE
+    folded into the KV-cache write; "Features": GQA)."""
+    theta, maxpos = 1.0e6, 1 << 20
+    w = wl.write_rows_case(93 + hq + d, 10, n_kv_heads=hkv, head_dim=d, dtype=dt, pad_frac=0.0)
+    p, wr = w.pool, w.write
+    n = wr.key.shape[0]
+    q = wl.normal_bits(wl.derive_seed(93, hq + d), n * hq * d, dt).reshape(n, hq, d)
+    sm = wr.slot_mapping.copy()
+    sm[[2, 7]] = -1                                   # padded rows, non-zero positions below
+    pos = (np.arange(n, dtype=np.int64) * 7919 + 13) % maxpos
+    pos[4] = maxpos - 1
+    q2, k2, _, st = oracle.rope_kv_write(q, p.k_cache, p.v_cache, wr.key, wr.value, sm, pos, maxpos, theta, dt)
+    assert st == oracle.OK and (pos > 0).all()
+    for i in range(n):
+        for h in range(hq):
+            x = f64(q[i, h], dt)
+            want = oracle.round_to(_rope_complex(x, float(pos[i]), theta), dt)
+            assert np.array_equal(q2[i, h], oracle.round_to(oracle.rope_exact(x, pos[i], theta), dt)), (i, h)
+            # the numpy rotation rounds the same except where an exact value sits within a few
+            # ulps of 1e-16 of a rounding boundary
+            diff = np.abs(f64(q2[i, h], dt) - f64(want, dt))
+            assert (diff <= 2.0 ** -6 * np.maximum(np.abs(f64(want, dt)), 1e-30) + 1e-300).all(), (i, h)
+            assert (q2[i, h] == want).mean() > 0.98, (i, h)
+    # keys of the padded rows were not written anywhere new: the cache equals the write of the
+    # other rows
+    keep = sm >= 0
+    _, k_ref, _, _ = oracle.rope_kv_write(None, p.k_cache, p.v_cache, wr.key[keep], wr.value[keep], sm[keep],
+                                          pos[keep], maxpos, theta, dt)
+    assert np.array_equal(k2, k_ref)
