@@ -73,6 +73,8 @@ extern "C" {
  *  slot_mapping    [num_tokens] int64; row i is copied to flat slot slot_mapping[i]
  *                  of the cache viewed as [num_blocks*block_size, n_kv_heads, head_dim];
  *                  -1 marks a padded row, which is skipped.  Slots must be distinct.
+ *  Any n_kv_heads x head_dim whose row (n_kv_heads * head_dim * 2 bytes) is a whole number of
+ *  16-byte chunks (PA_ERR_UNSUPPORTED otherwise); no upper limit on the row width.
  *  The copy is bit-exact.  num_tokens == 0 launches nothing and returns PA_OK.
  */
 int pa_reshape_and_cache(const void* key, const void* value, void* k_cache, void* v_cache,

@@ -295,7 +295,8 @@ int pa_reshape_and_cache(const void* key, const void* value, void* k_cache, void
         return PA_ERR_SHAPE;
     if (dtype != PA_F16 && dtype != PA_BF16) return PA_ERR_UNSUPPORTED;
     const int64_t row_bytes = (int64_t)n_kv_heads * head_dim * 2;
-    if (row_bytes % 16 || row_bytes / 16 > 512) return PA_ERR_UNSUPPORTED;  // one thread per 16-byte chunk, K and V
+    if (row_bytes % 16) return PA_ERR_UNSUPPORTED;  // 16-byte chunks
+    if (row_bytes / 16 > INT32_MAX / 2) return PA_ERR_SHAPE;
     if (num_tokens == 0) return PA_OK;
     if (!key || !value || !k_cache || !v_cache || !slot_mapping) return PA_ERR_NULL;
     if (!aligned16(key) || !aligned16(value) || !aligned16(k_cache) || !aligned16(v_cache)) return PA_ERR_ALIGN;
@@ -303,7 +304,8 @@ int pa_reshape_and_cache(const void* key, const void* value, void* k_cache, void
     int st = device_state(&dev);
     if (st != PA_OK) return st;
     const int row_vecs = (int)(row_bytes / 16);
-    const int threads = 2 * row_vecs;
+    // one thread per 16-byte chunk of the (K row ++ V row) pair, at most 512 (then each loops)
+    const int threads = 2 * row_vecs < 512 ? 2 * row_vecs : 512;
     const int64_t iters = (num_tokens + pa::kKvWriteRowsPerIter - 1) / pa::kKvWriteRowsPerIter;
     const int64_t max_grid = (int64_t)dev->sm_count * (2048 / threads);
     const int grid = (int)(iters < max_grid ? iters : max_grid);
@@ -469,6 +471,7 @@ int pa_prefill_chunk(void* out, const void* q, const void* k_cache, const void* 
     p.num_blocks = (int)num_blocks;
     p.cpb_log2 = cpb_log2_of(block_size);
     p.tiles_per_chunk = (int)(((int64_t)max_q_len * G + 127) / 128);
+    p.max_q_len = max_q_len;
     p.qk_scale_log2 = scale * 1.4426950408889634f;
     p.hd = head_dim;
     if ((int64_t)p.tiles_per_chunk * num_chunks * n_kv_heads > INT32_MAX) return PA_ERR_UNSUPPORTED;

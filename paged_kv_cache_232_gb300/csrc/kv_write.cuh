@@ -4,7 +4,8 @@
 //
 // A cache row for one slot, [n_kv_heads, head_dim], is contiguous in the
 // [num_blocks, block_size, n_kv_heads, head_dim] layout, so the write is a row scatter:
-// thread t of a CTA owns 16-byte chunk t of the (K row ++ V row) pair, and each CTA walks
+// thread t of a CTA owns 16-byte chunks t, t + blockDim.x, ... of the (K row ++ V row) pair
+// (one chunk when the pair has at most 512 of them, as at 8 KV heads x 128), and each CTA walks
 // U rows at a time so every thread has U independent 16-byte loads in flight before its
 // stores.  Bit-exact: no arithmetic touches the data.
 #pragma once
@@ -20,12 +21,7 @@ __global__ void kv_write_kernel(const uint4* __restrict__ key, const uint4* __re
                                 int row_vecs, int64_t num_slots, unsigned* err) {
     constexpr int U = kKvWriteRowsPerIter;
     const int t = threadIdx.x;
-    const bool is_v = t >= row_vecs;
-    const int c = is_v ? t - row_vecs : t;
-    const uint4* src = (is_v ? value : key) + c;
-    uint4* dst = (is_v ? v_cache : k_cache) + c;
     for (int64_t r0 = (int64_t)blockIdx.x * U; r0 < num_tokens; r0 += (int64_t)gridDim.x * U) {
-        uint4 v[U];
         int64_t slot[U];
 #pragma unroll
         for (int u = 0; u < U; ++u) {
@@ -35,11 +31,20 @@ __global__ void kv_write_kernel(const uint4* __restrict__ key, const uint4* __re
                 if (t == 0) flag_error(err, PA_DEVERR_SLOT);
                 slot[u] = -1;
             }
-            if (slot[u] >= 0) v[u] = ldg_nc_128(src + r * row_vecs);
         }
+        for (int k = t; k < 2 * row_vecs; k += blockDim.x) {
+            const bool is_v = k >= row_vecs;
+            const int c = is_v ? k - row_vecs : k;
+            const uint4* src = (is_v ? value : key) + c;
+            uint4* dst = (is_v ? v_cache : k_cache) + c;
+            uint4 v[U];
 #pragma unroll
-        for (int u = 0; u < U; ++u)
-            if (slot[u] >= 0) dst[slot[u] * row_vecs] = v[u];
+            for (int u = 0; u < U; ++u)
+                if (slot[u] >= 0) v[u] = ldg_nc_128(src + (r0 + u) * row_vecs);
+#pragma unroll
+            for (int u = 0; u < U; ++u)
+                if (slot[u] >= 0) dst[slot[u] * row_vecs] = v[u];
+        }
     }
 }
 

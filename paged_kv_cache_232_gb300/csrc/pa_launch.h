@@ -55,6 +55,7 @@ struct PrefillParams {
     unsigned* err;
     int num_chunks, n_q_heads, n_kv_heads, max_blocks_per_seq, num_blocks;
     int tiles_per_chunk;        // query tiles (or CTA units) per (chunk, kv head)
+    int max_q_len;              // host-side bound of the chunks' query lengths (sizes the grid)
     int cpb_log2;               // log2 of the 16-token chunks per cache block; -1: blocks of 8 tokens
     int lpt;                    // 1: CTAs take units longest-first (schedule fits in shared memory)
     float qk_scale_log2;

@@ -100,10 +100,11 @@ __device__ __forceinline__ void sts128(uint32_t addr, uint4 v) {
 }
 
 // Key tiles a unit (a pair of query tiles: tokens [j0, j0 + span) of chunk c) streams.
-__device__ __forceinline__ int unit_cost(const int* qsl, const int* kvl, int c, int pair, int span, int cap) {
+__device__ __forceinline__ int unit_cost(const int* qsl, const int* kvl, int c, int pair, int span, int cap,
+                                         int max_q_len) {
     const int q_len = qsl[c + 1] - qsl[c], kv_len = kvl[c];
     const int j0 = pair * span;
-    if (q_len < 0 || kv_len < q_len || kv_len > cap || j0 >= q_len) return 0;
+    if (q_len < 0 || q_len > max_q_len || kv_len < q_len || kv_len > cap || j0 >= q_len) return 0;
     return (kv_len - q_len + min(j0 + span, q_len) + pf::BN - 1) / pf::BN;
 }
 
@@ -126,7 +127,7 @@ __device__ __forceinline__ int lpt_unit(const PrefillParams& p, unsigned char* s
     for (int i = tid; i < ncost; i += nt) hist[i] = 0;
     __syncthreads();
     for (int u = tid; u < U; u += nt) {
-        const int cst = min(unit_cost(qsl, kvl, (u / p.n_kv_heads) % C, u / per_unit, SPAN, cap), ncost - 1);
+        const int cst = min(unit_cost(qsl, kvl, (u / p.n_kv_heads) % C, u / per_unit, SPAN, cap, p.max_q_len), ncost - 1);
         atomicAdd(&hist[cst], 1);
     }
     __syncthreads();
@@ -157,7 +158,7 @@ __device__ __forceinline__ int lpt_unit(const PrefillParams& p, unsigned char* s
     int seen = 0;
     for (int base = 0; base < U; base += nt) {
         const int u = base + tid;
-        const bool hit = u < U && min(unit_cost(qsl, kvl, (u / p.n_kv_heads) % C, u / per_unit, SPAN, cap),
+        const bool hit = u < U && min(unit_cost(qsl, kvl, (u / p.n_kv_heads) % C, u / per_unit, SPAN, cap, p.max_q_len),
                                       ncost - 1) == want;
         const unsigned bal = __ballot_sync(0xffffffffu, hit);
         if ((tid & 31) == 0) sel[3 + (tid >> 5)] = __popc(bal);
@@ -310,7 +311,10 @@ prefill_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmK, c
     const int q0 = p.lpt ? sched[c] : __ldg(p.query_start_loc + c);
     const int q_len = (p.lpt ? sched[c + 1] : __ldg(p.query_start_loc + c + 1)) - q0;
     const int kv_len = p.lpt ? sched[p.num_chunks + 1 + c] : __ldg(p.seq_lens + c);
-    if (q_len < 0 || kv_len < q_len || kv_len > table_row_tokens(p.max_blocks_per_seq, p.cpb_log2)) {
+    // a chunk longer than max_q_len (which sized the grid) would leave rows past the grid unwritten:
+    // it is flagged and skipped like the other bad lengths
+    if (q_len < 0 || q_len > p.max_q_len || kv_len < q_len ||
+        kv_len > table_row_tokens(p.max_blocks_per_seq, p.cpb_log2)) {
         if (unit == 0 && g == 0 && threadIdx.x == 0) flag_error(p.err, PA_DEVERR_LENGTH);
         return;
     }

@@ -97,22 +97,29 @@ def test_prefill_single_row_no_context_returns_v0():
         assert np.array_equal(got[c], np.repeat(v0, 2, axis=0))
 
 
-def test_prefill_mixed_batch_workload_sampled_rows():
-    """The mixed batch's eight 512-token chunks over 0..4096 cached tokens, full size; every
-    chunk's first 16 and last 16 rows plus 24 seeded random rows are checked."""
+_MIXED = {}
+
+
+def mixed_prefill_oracle(w):
+    """The fp64 oracle over every prefill row of the mixed batch (about 71 GFLOP of visible
+    pairs, twice with the condition scales), computed once for the tests that need it."""
+    if "ref" not in _MIXED:
+        _MIXED["ref"] = oracle_rows(w)
+    return _MIXED["ref"]
+
+
+def test_prefill_mixed_batch_workload_every_row():
+    """The mixed batch's eight 512-token chunks over 0..4096 cached tokens, full size: every
+    row of every chunk against the oracle."""
     w = wl.make_workload(5)
     got = bits_of(run_prefill(w)).reshape(w.prefill.q.shape)
-    qsl = w.prefill.query_start_loc
-    pick = wl.uniform_ints(wl.derive_seed(5, 99), 8 * 24, 0, 511).reshape(8, 24)
-    rows = []
-    for c in range(8):
-        rows += list(range(qsl[c], qsl[c] + 16)) + list(range(qsl[c + 1] - 16, qsl[c + 1])) + list(qsl[c] + pick[c])
-    rows = np.unique(np.asarray(rows))
-    check(got[rows], oracle_rows(w, rows), wl.BF16, "mixed batch prefill rows")
+    check(got, mixed_prefill_oracle(w), wl.BF16, "mixed batch prefill, every row")
+    assert pa.pa_device_errors(clear=True) == 0
 
 
 def test_mixed_batch_one_output_tensor():
-    """Decode rows and prefill rows of one batch write disjoint rows of one output."""
+    """Decode rows and prefill rows of one batch write disjoint rows of one output; every row
+    of both is checked."""
     w = wl.make_workload(5)
     p, b, pre = w.pool, w.decode, w.prefill
     kc, vc = to_dev(p.k_cache, p.dtype), to_dev(p.v_cache, p.dtype)
@@ -128,8 +135,8 @@ def test_mixed_batch_one_output_tensor():
     ex = oracle.decode(b.q, p.k_cache, p.v_cache, b.block_tables, b.context_lens, b.scale, p.dtype)
     cd = oracle.decode(b.q, p.k_cache, abs_bits(p.v_cache), b.block_tables, b.context_lens, b.scale, p.dtype)
     check_attention(got[:S], ex, p.dtype, "mixed: decode rows", cond=cd)
-    rows = np.arange(0, pre.q.shape[0], 61)
-    check(got[S:][rows], oracle_rows(w, rows), p.dtype, "mixed: prefill rows")
+    check(got[S:], mixed_prefill_oracle(w), p.dtype, "mixed: prefill rows")
+    assert pa.pa_device_errors(clear=True) == 0
 
 
 def test_prefill_out_of_pool_block_is_flagged_not_faulted():
@@ -144,6 +151,27 @@ def test_prefill_out_of_pool_block_is_flagged_not_faulted():
     got = bits_of(out).reshape(w.prefill.q.shape)
     rows = np.arange(40, 70)                      # the second chunk does not touch the bad entry
     check(got[rows], oracle_rows(w, rows), wl.BF16, "good chunk")
+
+
+def test_prefill_chunk_longer_than_max_q_len_is_flagged():
+    """max_q_len sizes the grid; a chunk longer than it is skipped and flagged
+    (PA_DEVERR_LENGTH) instead of leaving its later rows silently unwritten, and the other
+    chunks are still computed."""
+    w = wl.build_workload("pfq", 9, dtype=wl.BF16, n_q_heads=16, n_kv_heads=8, head_dim=128,
+                          prefill_q_lens=[40, 300], prefill_ctx_lens=[100, 10])
+    p, pre = w.pool, w.prefill
+    q = to_dev(pre.q, p.dtype)
+    out = torch.full_like(q, float("nan"))
+    pa.pa_device_errors(clear=True)
+    pa.pa_prefill_chunk(out, q, to_dev(p.k_cache, p.dtype), to_dev(p.v_cache, p.dtype),
+                        to_dev_i(pre.block_tables, torch.int32), to_dev_i(pre.query_start_loc, torch.int32),
+                        to_dev_i(pre.seq_lens, torch.int32), 100, pre.scale)
+    torch.cuda.synchronize()
+    assert pa.pa_device_errors(clear=True) & pa.PA_DEVERR_LENGTH
+    got = bits_of(out).reshape(pre.q.shape)
+    rows = np.arange(0, 40)
+    check(got[rows], oracle_rows(w, rows), wl.BF16, "chunk within max_q_len")
+    assert np.isnan(wl.bits_to_float(got[40:], wl.BF16)).all()   # the long chunk was not written
 
 
 @pytest.mark.parametrize("cfg", ["mixed", "short"])
