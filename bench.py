@@ -304,7 +304,20 @@ def run_ours(args, rank, world, local_rank):
             which, part = 2, (args.partition or part)
         dec_logical = decode_bytes(b, p)
         dec_unique = unique_decode_bytes(b, p)
-        if args.decode_path == "auto":
+        prefix = int(w.meta.get("shared_prefix_tokens", 0))
+        dec_launches = 1 if which == 1 else 2
+        if args.decode_path == "auto" and prefix > 0:
+            # the caller knows the blocks its sequences share (its prefix cache): the prefix part
+            # once per KV head on the tensor cores, the rest per sequence
+            which = 3
+            ws = torch.empty(max(pa.pa_decode_shared_prefix_workspace_size(S, hq, D, maxL, prefix), 16),
+                             dtype=torch.uint8, device=dev)
+            sw, _ = pa.pa_decode_plan(S, hq, p.n_kv_heads, D, p.block_size, maxL - prefix,
+                                      pa.PA_BF16 if p.dtype == wl.BF16 else pa.PA_F16)
+            dec_launches = 2 if sw == 1 else 3
+            dec_fn = lambda: pa.pa_decode_shared_prefix(out[:S], q[:S], kc, vc, bt, cl, maxL, b.scale, prefix, ws,
+                                                        prefix_piece_tokens=args.prefix_piece)
+        elif args.decode_path in ("auto", "plain"):
             dec_fn = lambda: pa.pa_decode(out[:S], q[:S], kc, vc, bt, cl, maxL, b.scale, ws)
         elif which == 1:
             dec_fn = lambda: pa.pa_decode_v1(out[:S], q[:S], kc, vc, bt, cl, b.scale)
@@ -345,7 +358,7 @@ def run_ours(args, rank, world, local_rank):
         if ev:
             ev[ns].record(stream)
 
-    launches_per_step = ((1 if wr is not None else 0) + (0 if (b is None or which == 0) else (1 if which == 1 else 2))
+    launches_per_step = ((1 if wr is not None else 0) + (0 if (b is None or which == 0) else dec_launches)
                          + (1 if pre is not None else 0))
     for _ in range(args.warmup):
         step()
@@ -458,8 +471,9 @@ def run_ours(args, rank, world, local_rank):
     if b is not None:
         cfg.update({"num_seqs": int(S), "n_q_heads": int(hq), "total_context_tokens": int(b.context_lens.sum()),
                     "decode_path": ("unified: decode rows as one-row chunks of the prefill launch" if which == 0
-                                    else ("one-pass" if which == 1 else f"split-K/{part}")
-                                    + ("" if args.decode_path == "auto" else " (forced)"))})
+                                    else (f"shared prefix of {prefix} tokens on the tensor cores + suffix decode"
+                                          if which == 3 else ("one-pass" if which == 1 else f"split-K/{part}"))
+                                    + ("" if args.decode_path in ("auto", "plain") else " (forced)"))})
     cfg.update({"l2": "512 MiB memset between timed steps (outside the events)",
                 "parallelism": f"replicas x{world} (independent batches, no collective)"})
     if wr is not None:
@@ -630,8 +644,11 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--unified", action="store_true",
                     help="mixed batch: decode rows through the prefill kernel in the same launch (one-row chunks)")
-    ap.add_argument("--decode-path", choices=["auto", "v1", "splitk"], default="auto",
-                    help="force the one-pass or split-K decode kernel instead of the library's dispatcher")
+    ap.add_argument("--decode-path", choices=["auto", "plain", "v1", "splitk"], default="auto",
+                    help="force the one-pass or split-K decode kernel instead of the library's dispatcher "
+                         "(plain: the dispatcher without the shared-prefix pass)")
+    ap.add_argument("--prefix-piece", type=int, default=0,
+                    help="shared-prefix pass: keys per CTA (multiple of 128; 0 = the library's choice)")
     ap.add_argument("--partition", type=int, default=0, help="split-K piece length in tokens (with --decode-path splitk)")
     ap.add_argument("--traffic", type=float, default=None,
                     help="dram bytes per decode launch from an ncu capture of this workload (reported as-is)")

@@ -239,6 +239,47 @@ int pa_decode_splitk_static(void* out, const void* q, const void* k_cache, const
                             void* stream);
 
 /*
+ * pa_decode_shared_prefix -- decode attention for a batch whose sequences share a prefix: the
+ * same physical blocks hold the first prefix_tokens tokens of every sequence.
+ * Source: mini_engine, "Features" (hash-based prefix caching: requests with a common prompt
+ * prefix share its KV blocks) and "Custom CUDA kernels" (paged decode attention; the kernels
+ * read K/V straight from the pool, prefix hits included).  The result is that of pa_decode on
+ * the same inputs (out[s, h] = softmax-weighted sum over every token t < context_lens[s]); only
+ * the order of the arithmetic differs.
+ *
+ * The prefix part is one dense contraction per KV head -- rows: the sequences' query heads of
+ * the group; keys: the prefix tokens -- run once on the tcgen05 tensor cores (the prefill
+ * kernel's tiles, in pieces of prefix_piece_tokens), which leaves per-row partials (max,
+ * exp-sum, normalised output) in the workspace; the tokens past the prefix are streamed per
+ * sequence by the decode kernels (pa_decode's dispatcher picks one-pass or split-K for them),
+ * which fold the partials into their final merge.  The decode is launched as a programmatic
+ * dependent of the prefix pass, so the two overlap.
+ *
+ *  Arguments as pa_decode, plus:
+ *  prefix_tokens  tokens every sequence shares: table entries [0, ceil(prefix_tokens /
+ *                 block_size)) are the same blocks in every row the prefix reaches, and the
+ *                 prefix pass reads them from row 0 (which must hold them).  Only whole 16-token
+ *                 chunks of min(prefix_tokens, max_context_len) go through the prefix pass; the
+ *                 remainder is streamed per sequence.  A sequence shorter than the prefix
+ *                 attends to its own context_lens[s] tokens only.  0 (or fewer than 16 shared
+ *                 tokens) runs plain pa_decode.  Must be <= max_blocks_per_seq * block_size.
+ *  prefix_piece_tokens  keys per CTA of the prefix pass, a multiple of 128; 0 = the library's
+ *                 choice (about a quarter of the SMs busy with the prefix pass).
+ *  workspace  at least pa_decode_shared_prefix_workspace_size(...) bytes, caller-owned.
+ *  Returns PA_ERR_BOUNDS for max_context_len or prefix_tokens beyond the table's capacity,
+ *  PA_ERR_UNSUPPORTED for a piece that is not a multiple of 128, PA_ERR_WORKSPACE for a missing
+ *  or small workspace; otherwise as pa_decode.
+ */
+size_t pa_decode_shared_prefix_workspace_size(int num_seqs, int n_q_heads, int head_dim, int max_context_len,
+                                              int prefix_tokens);
+
+int pa_decode_shared_prefix(void* out, const void* q, const void* k_cache, const void* v_cache,
+                            const int32_t* block_tables, int max_blocks_per_seq, const int32_t* context_lens,
+                            int max_context_len, int num_seqs, int n_q_heads, int n_kv_heads, int head_dim,
+                            int block_size, int64_t num_blocks, float scale, int dtype, int prefix_tokens,
+                            int prefix_piece_tokens, void* workspace, size_t workspace_bytes, void* stream);
+
+/*
  * pa_prefill_chunk -- attention for ragged prefill chunks that attend to their
  * earlier cached context, on the tcgen05 tensor cores (head_dim 64, 96, 128 or 256).
  * Source: mini_engine, "Custom CUDA kernels" (paged prefill attention: tiled,

@@ -23,7 +23,8 @@ DEFAULT_PARTITION_TOKENS = 256
 EXPORTED = (
     "pa_reshape_and_cache", "pa_decode_workspace_size", "pa_decode", "pa_decode_plan", "pa_decode_v1",
     "pa_decode_splitk", "pa_prefill_chunk", "pa_device_errors", "pa_status_string", "pa_version",
-    "pa_decode_splitk_static", "pa_rope_table", "pa_rope_reshape_and_cache",
+    "pa_decode_splitk_static", "pa_rope_table", "pa_rope_reshape_and_cache", "pa_decode_shared_prefix",
+    "pa_decode_shared_prefix_workspace_size",
 )
 STATIC_SCRATCH_BYTES = 16 << 20
 
@@ -73,6 +74,11 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
     L.pa_decode_splitk_static.argtypes = [vp, vp, vp, vp, vp, i32, vp, i32, i32, i32, i32, i32, i32, i64, f32, i32,
                                           i32, vp]
     L.pa_decode_splitk_static.restype = i32
+    L.pa_decode_shared_prefix.argtypes = [vp, vp, vp, vp, vp, i32, vp, i32, i32, i32, i32, i32, i32, i64, f32, i32,
+                                          i32, i32, vp, sz, vp]
+    L.pa_decode_shared_prefix.restype = i32
+    L.pa_decode_shared_prefix_workspace_size.argtypes = [i32, i32, i32, i32, i32]
+    L.pa_decode_shared_prefix_workspace_size.restype = sz
     L.pa_prefill_chunk.argtypes = [vp, vp, vp, vp, vp, i32, vp, vp, i32, i32, i32, i32, i32, i32, i64, f32, i32, vp]
     L.pa_prefill_chunk.restype = i32
     L.pa_device_errors.argtypes = [i32]
@@ -250,6 +256,25 @@ def pa_decode_splitk_static(out, q, k_cache, v_cache, block_tables, context_lens
     st = load().pa_decode_splitk_static(po, pq, pk, pv, pbt, mb, pcl, int(max_context_len), S, hq, hkv, d, bs, nb,
                                         float(scale), dt, int(partition_tokens), _stream(stream, q.device))
     _check(st, "pa_decode_splitk_static")
+
+
+def pa_decode_shared_prefix_workspace_size(num_seqs: int, n_q_heads: int, head_dim: int, max_context_len: int,
+                                           prefix_tokens: int) -> int:
+    return int(load().pa_decode_shared_prefix_workspace_size(num_seqs, n_q_heads, head_dim, max_context_len,
+                                                             prefix_tokens))
+
+
+def pa_decode_shared_prefix(out, q, k_cache, v_cache, block_tables, context_lens, max_context_len: int, scale: float,
+                            prefix_tokens: int, workspace, prefix_piece_tokens: int = 0, stream=None) -> None:
+    """Decode for sequences whose first prefix_tokens tokens are the same cache blocks: the prefix
+    part once per KV head on the tensor cores, the rest per sequence, merged."""
+    dt, nb, bs, hkv, d, S, hq, mb, (po, pq, pk, pv, pbt, pcl) = _decode_common(out, q, k_cache, v_cache, block_tables,
+                                                                             context_lens)
+    wp, wb = (workspace.data_ptr(), workspace.numel() * workspace.element_size()) if workspace is not None else (None, 0)
+    st = load().pa_decode_shared_prefix(po, pq, pk, pv, pbt, mb, pcl, int(max_context_len), S, hq, hkv, d, bs, nb,
+                                        float(scale), dt, int(prefix_tokens), int(prefix_piece_tokens), wp, wb,
+                                        _stream(stream, q.device))
+    _check(st, "pa_decode_shared_prefix")
 
 
 def pa_prefill_chunk(out, q, k_cache, v_cache, block_tables, query_start_loc, seq_lens, max_q_len: int, scale: float,

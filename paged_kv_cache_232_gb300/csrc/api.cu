@@ -134,10 +134,18 @@ int check_decode(const void* out, const void* q, const void* k_cache, const void
     return PA_OK;
 }
 
+// Partials of a shared-prefix pass that the decode folds into its merge (see pa_decode_shared_prefix).
+struct PrefixPartials {
+    int tokens;  // the decode streams tokens [tokens, L) of each sequence
+    int parts;
+    const float *m, *l, *o;
+};
+
 int decode_impl(void* out, const void* q, const void* k_cache, const void* v_cache, const int32_t* block_tables,
                 int max_blocks_per_seq, const int32_t* context_lens, int max_context_len, int num_seqs,
                 int n_q_heads, int n_kv_heads, int head_dim, int block_size, int64_t num_blocks, float scale,
-                int dtype, int part_tokens, void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+                int dtype, int part_tokens, void* workspace, size_t workspace_bytes, cudaStream_t stream,
+                const PrefixPartials* pf = nullptr) {
     int st = check_decode(out, q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens, num_seqs,
                           n_q_heads, n_kv_heads, head_dim, block_size, num_blocks, dtype);
     if (st != PA_OK || num_seqs == 0) return st;
@@ -159,6 +167,13 @@ int decode_impl(void* out, const void* q, const void* k_cache, const void* v_cac
     p.cpb_log2 = cpb_log2_of(block_size);
     p.qk_scale_log2 = scale * 1.4426950408889634f;
     p.hd = head_dim;
+    if (pf) {
+        p.prefix_tokens = pf->tokens;
+        p.pf_parts = pf->parts;
+        p.pf_m = pf->m;
+        p.pf_l = pf->l;
+        p.pf_o = pf->o;
+    }
     const int units = num_seqs * n_kv_heads;
     int grid = units;
     bool reduce = false;
@@ -166,7 +181,9 @@ int decode_impl(void* out, const void* q, const void* k_cache, const void* v_cac
         if (part_tokens % (block_size < 16 ? 16 : block_size)) return PA_ERR_UNSUPPORTED;  // whole chunks and blocks
         if (max_context_len < 0 || (int64_t)max_context_len > (int64_t)max_blocks_per_seq * block_size)
             return PA_ERR_BOUNDS;
-        const int max_parts = max_context_len > 0 ? (max_context_len + part_tokens - 1) / part_tokens : 1;
+        // pieces cover the tokens past the shared prefix, if any
+        const int streamed = max_context_len - std::min(max_context_len, p.prefix_tokens);
+        const int max_parts = streamed > 0 ? (streamed + part_tokens - 1) / part_tokens : 1;
         if ((int64_t)units * max_parts > INT32_MAX) return PA_ERR_UNSUPPORTED;
         const WsLayout w = ws_layout(num_seqs, n_q_heads, kernel_dim(head_dim), max_parts);
         if (max_parts > 1) {
@@ -481,6 +498,124 @@ int pa_prefill_chunk(void* out, const void* q, const void* k_cache, const void* 
     cudaError_t e = pa::launch_prefill(dtype == PA_BF16, kernel_dim(head_dim), G, p, tk, tv, static_cast<cudaStream_t>(stream));
     if (e == cudaErrorNotSupported) return PA_ERR_UNSUPPORTED;
     return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
+// ---- shared prefix --------------------------------------------------------------------------
+
+// Layout of pa_decode_shared_prefix's workspace: the prefix pass's partials (m, l: [S * Hq][KP];
+// o: [S * Hq][KP][kernel head_dim]; KP sized for the smallest piece), then the suffix's split-K
+// region (pa_decode_workspace_size over the tokens past the prefix), each 256-byte aligned.
+static constexpr int kMinPrefixPiece = 128;
+
+static int prefix_tokens_used(int prefix_tokens, int max_context_len) {
+    // whole 16-token chunks of the prefix within the longest context; the rest of a shared
+    // prefix is streamed by each sequence's decode like its own tokens
+    const int p = prefix_tokens < max_context_len ? prefix_tokens : max_context_len;
+    return p > 0 ? (p / 16) * 16 : 0;
+}
+
+static WsLayout pf_layout(int num_seqs, int n_q_heads, int kdim, int parts) {
+    return ws_layout(num_seqs, n_q_heads, kdim, parts);  // same three regions, one column per piece
+}
+
+size_t pa_decode_shared_prefix_workspace_size(int num_seqs, int n_q_heads, int head_dim, int max_context_len,
+                                              int prefix_tokens) {
+    if (num_seqs <= 0 || n_q_heads <= 0 || head_dim <= 0 || max_context_len < 0 || prefix_tokens < 0) return 0;
+    const int P = prefix_tokens_used(prefix_tokens, max_context_len);
+    if (P == 0) return pa_decode_workspace_size(num_seqs, n_q_heads, head_dim, max_context_len, 0);
+    const int kp = (P + kMinPrefixPiece - 1) / kMinPrefixPiece;
+    return pf_layout(num_seqs, n_q_heads, kernel_dim(head_dim), kp).total +
+           pa_decode_workspace_size(num_seqs, n_q_heads, head_dim, max_context_len - P, 0);
+}
+
+int pa_decode_shared_prefix(void* out, const void* q, const void* k_cache, const void* v_cache,
+                            const int32_t* block_tables, int max_blocks_per_seq, const int32_t* context_lens,
+                            int max_context_len, int num_seqs, int n_q_heads, int n_kv_heads, int head_dim,
+                            int block_size, int64_t num_blocks, float scale, int dtype, int prefix_tokens,
+                            int prefix_piece_tokens, void* workspace, size_t workspace_bytes, void* stream) {
+    int st = check_decode(out, q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens, num_seqs,
+                          n_q_heads, n_kv_heads, head_dim, block_size, num_blocks, dtype);
+    if (st != PA_OK || num_seqs == 0) return st;
+    const int64_t row_tokens = (int64_t)max_blocks_per_seq * block_size;
+    if (max_context_len < 0 || max_context_len > row_tokens || prefix_tokens < 0 || prefix_tokens > row_tokens)
+        return PA_ERR_BOUNDS;
+    if (prefix_piece_tokens < 0 || prefix_piece_tokens % kMinPrefixPiece) return PA_ERR_UNSUPPORTED;
+    if (!std::isfinite(scale)) return PA_ERR_SHAPE;
+    const int P = prefix_tokens_used(prefix_tokens, max_context_len);
+    if (P == 0)  // nothing shared: the plain dispatcher, same workspace
+        return pa_decode(out, q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens, max_context_len,
+                         num_seqs, n_q_heads, n_kv_heads, head_dim, block_size, num_blocks, scale, dtype, workspace,
+                         workspace_bytes, stream);
+    DeviceState* dev = nullptr;
+    if ((st = device_state(&dev)) != PA_OK) return st;
+    const int G = n_q_heads / n_kv_heads;
+    const int kdim = kernel_dim(head_dim);
+    if (workspace_bytes < pa_decode_shared_prefix_workspace_size(num_seqs, n_q_heads, head_dim, max_context_len,
+                                                                 prefix_tokens) ||
+        !workspace)
+        return PA_ERR_WORKSPACE;
+    if (!aligned16(workspace)) return PA_ERR_ALIGN;
+
+    // the prefix pass: CTAs of (query-tile pair, KV head, piece); the default piece keeps about a
+    // quarter of the SMs on it (its CTAs run beside the suffix decode, which starts at once)
+    const int tiles = (int)(((int64_t)num_seqs * G + 127) / 128);
+    const int pairs = (tiles + 1) / 2;
+    int piece = prefix_piece_tokens;
+    if (piece == 0) {
+        const int64_t per_piece = (int64_t)pairs * n_kv_heads;
+        const int64_t kp = std::max<int64_t>(1, (dev->sm_count / 4 + per_piece - 1) / per_piece);
+        piece = (int)((((int64_t)P + kp - 1) / kp + 127) / 128 * 128);
+        piece = std::max(piece, 256);
+    }
+    const int kp = (P + piece - 1) / piece;
+    if ((int64_t)tiles * n_kv_heads * kp > INT32_MAX) return PA_ERR_UNSUPPORTED;
+    const WsLayout pw = pf_layout(num_seqs, n_q_heads, kdim, (P + kMinPrefixPiece - 1) / kMinPrefixPiece);
+    // the partials are laid out for kp pieces inside the region sized for the smallest piece
+    const WsLayout pk = pf_layout(num_seqs, n_q_heads, kdim, kp);
+    char* base = static_cast<char*>(workspace);
+    float* pf_m = reinterpret_cast<float*>(base + pk.m_off);
+    float* pf_l = reinterpret_cast<float*>(base + pk.l_off);
+    float* pf_o = reinterpret_cast<float*>(base + pk.o_off);
+
+    CUtensorMap tk, tv;
+    if ((st = encode_cache_map(&tk, k_cache, dtype, num_blocks, block_size, n_kv_heads, head_dim)) != PA_OK) return st;
+    if ((st = encode_cache_map(&tv, v_cache, dtype, num_blocks, block_size, n_kv_heads, head_dim)) != PA_OK) return st;
+    pa::PrefillParams pp{};
+    pp.q = q;
+    pp.block_tables = block_tables;
+    pp.err = dev->err;
+    pp.n_q_heads = n_q_heads;
+    pp.n_kv_heads = n_kv_heads;
+    pp.max_blocks_per_seq = max_blocks_per_seq;
+    pp.num_blocks = (int)num_blocks;
+    pp.cpb_log2 = cpb_log2_of(block_size);
+    pp.tiles_per_chunk = tiles;
+    pp.qk_scale_log2 = scale * 1.4426950408889634f;
+    pp.hd = head_dim;
+    pp.context_lens = context_lens;
+    pp.pf_m = pf_m;
+    pp.pf_l = pf_l;
+    pp.pf_o = pf_o;
+    pp.num_seqs = num_seqs;
+    pp.prefix_tokens = P;
+    pp.piece_tokens = piece;
+    pp.pf_parts = kp;
+    cudaError_t e = pa::launch_prefix(dtype == PA_BF16, kdim, G, pp, tk, tv, static_cast<cudaStream_t>(stream));
+    if (e == cudaErrorNotSupported) return PA_ERR_UNSUPPORTED;
+    if (e != cudaSuccess) return PA_ERR_CUDA;
+
+    // the suffix: the dispatcher's plan over the tokens past the prefix
+    const int resident = pa::decode_resident_ctas(dtype == PA_BF16, kdim, G);
+    if (resident <= 0) return PA_ERR_CUDA;
+    int part = 0;
+    const int which = plan((int64_t)num_seqs * n_kv_heads, max_context_len - P, dev->sm_count, resident, block_size,
+                           &part);
+    const PrefixPartials pin{P, kp, pf_m, pf_l, pf_o};
+    void* ws2 = base + pw.total;
+    const size_t ws2_bytes = workspace_bytes - pw.total;
+    return decode_impl(out, q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens, max_context_len,
+                       num_seqs, n_q_heads, n_kv_heads, head_dim, block_size, num_blocks, scale, dtype,
+                       which == 2 ? part : 0, ws2, ws2_bytes, static_cast<cudaStream_t>(stream), &pin);
 }
 
 }  // extern "C"

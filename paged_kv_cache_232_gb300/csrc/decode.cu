@@ -35,13 +35,32 @@ static cudaError_t launch_decode_t(const DecodeParams& p, const CUtensorMap& tmK
                                    bool with_reduce, cudaStream_t st) {
     using C = DecodeCfg<D, G, BF16>;
     cudaError_t e;
+    // after a shared-prefix pass the decode is its programmatic dependent: its CTAs start while
+    // that pass runs and wait for its partials (griddepcontrol.wait) only at their merge
+    auto launch = [&](auto kern, int smem) -> cudaError_t {
+        if (p.pf_parts <= 0) {
+            kern<<<grid, C::THREADS, smem, st>>>(p, tmK, tmV);
+            return cudaGetLastError();
+        }
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3((unsigned)grid);
+        cfg.blockDim = dim3(C::THREADS);
+        cfg.dynamicSmemBytes = (size_t)smem;
+        cfg.stream = st;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        return cudaLaunchKernelEx(&cfg, kern, p, tmK, tmV);
+    };
     if (p.persist) {
         // group sizes 1 and 2 only: larger groups run out of registers in the unit loop
         if constexpr (G <= 2) {
             auto kern = decode_kernel_persistent<D, G, BF16>;
             e = smem_limit_once(reinterpret_cast<const void*>(kern), C::P_SMEM_BYTES, smem_flag<D, G, BF16, true>());
             if (e != cudaSuccess) return e;
-            kern<<<grid, C::THREADS, C::P_SMEM_BYTES, st>>>(p, tmK, tmV);
+            e = launch(kern, C::P_SMEM_BYTES);
         } else {
             return cudaErrorInvalidValue;
         }
@@ -49,11 +68,10 @@ static cudaError_t launch_decode_t(const DecodeParams& p, const CUtensorMap& tmK
         auto kern = decode_kernel<D, G, BF16>;
         e = smem_limit_once(reinterpret_cast<const void*>(kern), C::SMEM_BYTES, smem_flag<D, G, BF16, false>());
         if (e != cudaSuccess) return e;
-        kern<<<grid, C::THREADS, C::SMEM_BYTES, st>>>(p, tmK, tmV);
+        e = launch(kern, C::SMEM_BYTES);
     }
-    e = cudaGetLastError();
     if (e != cudaSuccess || !with_reduce) return e;
-    const size_t red_smem = (size_t)(((p.max_parts + 3) & ~3) + 8 * D) * sizeof(float);
+    const size_t red_smem = (size_t)(((p.max_parts + 3) & ~3) + ((p.pf_parts + 3) & ~3) + 8 * D) * sizeof(float);
     auto rk = splitk_reduce_kernel<D, BF16>;
     if (red_smem > 227 * 1024) return cudaErrorInvalidValue;
     if (red_smem > 48 * 1024) {

@@ -52,7 +52,44 @@ struct DecodeParams {
     int hd;                    // head_dim of q, out and the cache (<= D; columns hd .. D-1 are zero)
     int lpt;                   // one-pass grid only: CTAs take sequences longest first
     int persist;               // one-pass grid only: decode_kernel_persistent, gridDim.x CTAs run unit lists
+    // Shared prefix: tokens [0, prefix_tokens) of every sequence were attended by the shared-prefix
+    // pass (prefill kernel in shared-prefix mode), which left pf_parts partials per (s, h): pf_m (base-2
+    // log of the weights' reference), pf_l (their sum), pf_o (normalised output, D columns).  The
+    // kernels here cover tokens [prefix_tokens, L) and fold those partials into their merge, after
+    // griddepcontrol.wait (they are launched as programmatic dependents of that pass).
+    int prefix_tokens;
+    int pf_parts;              // 0: no shared prefix
+    const float* pf_m;         // [S * Hq][pf_parts]
+    const float* pf_l;
+    const float* pf_o;         // [S * Hq][pf_parts][D]
 };
+
+// Tokens of a sequence of context L the decode kernels stream: the part past the shared prefix.
+__device__ __forceinline__ int streamed_tokens(const DecodeParams& p, int L) { return max(L - p.prefix_tokens, 0); }
+
+// Folds the shared-prefix partials of output row `row` into a merge in progress: raises the
+// running maximum M (base 2) first (pass 0), then adds each partial's weight l_k 2^(m_k - M) to
+// the sum and its output (normalised) times that weight (pass 1).  Partials with l = 0 (no key
+// of the piece visible) are skipped.
+__device__ __forceinline__ float prefix_max(const DecodeParams& p, size_t row, float M) {
+    for (int k = 0; k < p.pf_parts; ++k)
+        if (p.pf_l[row * p.pf_parts + k] > 0.f) M = fmaxf(M, p.pf_m[row * p.pf_parts + k]);
+    return M;
+}
+__device__ __forceinline__ void prefix_add(const DecodeParams& p, size_t row, int d, int D, float M, float& Lsum,
+                                           float& o0, float& o1) {
+    for (int k = 0; k < p.pf_parts; ++k) {
+        const size_t i = row * p.pf_parts + k;
+        const float lk = p.pf_l[i];
+        if (lk > 0.f) {
+            const float wt = lk * ex2(p.pf_m[i] - M);
+            Lsum += wt;
+            const float2 v = *reinterpret_cast<const float2*>(p.pf_o + i * D + d);
+            o0 = fmaf(v.x, wt, o0);
+            o1 = fmaf(v.y, wt, o1);
+        }
+    }
+}
 
 // Longest-first order of the one-pass grid: sequences ranked by 16-token chunk count
 // (descending, ties by index); CTA b takes KV head b mod Hkv of the sequence at rank b / Hkv,
@@ -70,7 +107,7 @@ __device__ __forceinline__ int seq_at_rank(const DecodeParams& p, int r, int* sc
     for (int i = tid; i < S; i += blockDim.x) {
         int L = __ldg(p.context_lens + i);
         L = L < 0 ? 0 : min(L, cap);
-        len[i] = (L + 15) >> 4;
+        len[i] = (streamed_tokens(p, L) + 15) >> 4;
     }
     __syncthreads();
     for (int i = tid; i < S; i += blockDim.x) atomicAdd(&hist[len[i]], 1);
@@ -131,7 +168,7 @@ __device__ __forceinline__ int lpt_units(const DecodeParams& p, int* scratch, in
     for (int i = tid; i < S; i += blockDim.x) {
         int L = __ldg(p.context_lens + i);
         L = L < 0 ? 0 : min(L, cap);
-        len[i] = (L + 15) >> 4;
+        len[i] = (streamed_tokens(p, L) + 15) >> 4;
     }
     __syncthreads();
     for (int i = tid; i < S; i += blockDim.x) atomicAdd(&hist[len[i]], 1);
@@ -412,14 +449,17 @@ decode_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmK, con
     // context length, clamped to what the table (and the split-K grid) can address
     int L = __ldg(p.context_lens + s);
     int cap = table_row_tokens(p.max_blocks_per_seq, p.cpb_log2);  // tokens the table row addresses
-    if (p.part_tokens > 0 && p.max_parts * p.part_tokens < cap) cap = p.max_parts * p.part_tokens;
+    if (p.part_tokens > 0 && p.prefix_tokens + p.max_parts * p.part_tokens < cap)
+        cap = p.prefix_tokens + p.max_parts * p.part_tokens;
     if (L < 0 || L > cap) {
         if (piece == 0 && g == 0 && threadIdx.x == 0) flag_error(p.err, PA_DEVERR_LENGTH);
         L = L < 0 ? 0 : cap;
     }
-    const int t_begin = p.part_tokens > 0 ? piece * p.part_tokens : 0;
+    // tokens [base, L) are streamed here (base > 0 past a shared prefix), in pieces for split-K
+    const int base = min(L, p.prefix_tokens);
+    const int t_begin = p.part_tokens > 0 ? min(L, base + piece * p.part_tokens) : base;
     const int t_end = p.part_tokens > 0 ? min(L, t_begin + p.part_tokens) : L;
-    const int n_parts = p.part_tokens > 0 ? (L + p.part_tokens - 1) / p.part_tokens : 1;
+    const int n_parts = p.part_tokens > 0 ? (L - base + p.part_tokens - 1) / p.part_tokens : 1;
     if (t_begin >= t_end && piece > 0) return;  // split-K piece past this sequence's context
     const int nblk = (t_end - t_begin + C::BS - 1) / C::BS;
     const int blk0 = t_begin / C::BS;
@@ -599,14 +639,20 @@ decode_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmK, con
         ml[warp * G + my_h] = l_run;
     }
     asm volatile("bar.sync 1, %0;" ::"n"(C::NCW * 32) : "memory");
+    // the shared-prefix partials are complete and visible past this point (and this grid completes
+    // only after that pass has: the split-K merge relies on it)
+    if (p.pf_parts > 0) asm volatile("griddepcontrol.wait;" ::: "memory");
 
     const int tid = threadIdx.x;  // 0 .. 127
     const int hq0 = g * G;
     for (int idx = 2 * tid; idx < G * D; idx += 2 * C::NCW * 32) {
         const int h = idx / D, d = idx - h * D;
+        const size_t row = (size_t)s * p.n_q_heads + hq0 + h;
+        const bool fold = direct && p.pf_parts > 0;  // split-K pieces leave the prefix to the reduce
         float M = -INFINITY;
 #pragma unroll
         for (int w = 0; w < C::NCW; ++w) M = fmaxf(M, mm[w * G + h]);
+        if (fold) M = prefix_max(p, row, M);
         float Lsum = 0.f, o0 = 0.f, o1 = 0.f;
         if (M != -INFINITY) {
 #pragma unroll
@@ -616,9 +662,9 @@ decode_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmK, con
                 o0 = fmaf(mo[(w * G + h) * D + d], wt, o0);
                 o1 = fmaf(mo[(w * G + h) * D + d + 1], wt, o1);
             }
+            if (fold) prefix_add(p, row, d, D, M, Lsum, o0, o1);
         }
         const float inv = (Lsum > 0.f) ? 1.f / Lsum : 0.f;
-        const size_t row = (size_t)s * p.n_q_heads + hq0 + h;
         if (direct) {
             uint32_t packed = F::pack_rn(o0 * inv, o1 * inv);
             if (d < p.hd) *reinterpret_cast<uint32_t*>(static_cast<uint16_t*>(p.out) + row * p.hd + d) = packed;
@@ -678,7 +724,7 @@ decode_kernel_persistent(const DecodeParams p, const __grid_constant__ CUtensorM
     // in nblk 16-token chunks
     const int cap = table_row_tokens(p.max_blocks_per_seq, p.cpb_log2);
     struct Unit {
-        int s, g, L, nblk;
+        int s, g, L, t0, nblk;  // tokens [t0, L) are streamed (t0 > 0 past a shared prefix)
     };
     auto unit_at = [&](int k, bool report) {
         Unit u;
@@ -690,7 +736,8 @@ decode_kernel_persistent(const DecodeParams p, const __grid_constant__ CUtensorM
             L = L < 0 ? 0 : cap;
         }
         u.L = L;
-        u.nblk = (L + C::BS - 1) / C::BS;
+        u.t0 = min(L, p.prefix_tokens);
+        u.nblk = (L - u.t0 + C::BS - 1) / C::BS;
         return u;
     };
 
@@ -711,10 +758,11 @@ decode_kernel_persistent(const DecodeParams p, const __grid_constant__ CUtensorM
             // with blocks of 8 tokens, entries 2c and 2c + 1 (the second only if the context reaches
             // it), each an 8-row box, the second landing 8 rows (1 KB) further
             const int32_t* bt = p.block_tables + (size_t)u.s * p.max_blocks_per_seq;
+            const int c0 = u.t0 / C::BS;  // the unit's first chunk (t0 is a multiple of 16)
             for (int b0 = 0; b0 < u.nblk && ok; b0 += per_load) {
                 const int nb = min(per_load, u.nblk - b0);
                 int my = p.num_blocks;  // outside the tensor map: TMA fills zeros
-                const int e = half8 ? 2 * b0 + lane : (b0 + lane) >> p.cpb_log2;
+                const int e = half8 ? 2 * (c0 + b0) + lane : (c0 + b0 + lane) >> p.cpb_log2;
                 if (half8 ? (lane < 2 * nb && 8 * e < u.L) : (lane < nb)) {
                     my = __ldg(bt + e);
                     if (my < 0 || my >= p.num_blocks) {
@@ -730,7 +778,7 @@ decode_kernel_persistent(const DecodeParams p, const __grid_constant__ CUtensorM
                     const uint32_t ph = (gb / C::NST) & 1;
                     if (lane == 0) {
                         // chunk's first row in its block
-                        const int row0 = half8 ? 0 : ((b0 + j) & ((1 << p.cpb_log2) - 1)) * C::BS;
+                        const int row0 = half8 ? 0 : ((c0 + b0 + j) & ((1 << p.cpb_log2) - 1)) * C::BS;
                         if (gb >= C::NST && !mbar_wait(bar_empty + 8 * st, ph ^ 1, p.err)) ok = false;
                         if (ok) {
                             const uint32_t dst = ring + st * C::STAGE_BYTES;
@@ -797,12 +845,13 @@ decode_kernel_persistent(const DecodeParams p, const __grid_constant__ CUtensorM
     bool ok = true;
     int base_blk = 0;  // ring index of the unit's first block
     for (int k = 0; k < n_units; ++k) {
-        int L, nblk, s, g;
+        int L, t0, nblk, s, g;
         // q for the G heads of this group, this lane's CPL chunks, pre-scaled by scale*log2(e)
         float qf[G][C::CPL][8];
         {
             const Unit u = unit_at(k, true);
             L = u.L;
+            t0 = u.t0;
             nblk = u.nblk;
             s = u.s;
             g = u.g;
@@ -836,7 +885,7 @@ decode_kernel_persistent(const DecodeParams p, const __grid_constant__ CUtensorM
             const bool arrived = mbar_wait(bar_full + 8 * st, ph, p.err);
             if (!__all_sync(0xffffffffu, arrived)) { ok = false; break; }  // leave the loop warp-uniformly
             const uint32_t kt = ring + st * C::STAGE_BYTES;
-            const int nvalid = min(C::BS, L - b * C::BS);
+            const int nvalid = min(C::BS, L - t0 - b * C::BS);
             consume_chunk<D, G, BF16>(kt, nvalid, qf, chunk_col, lane, my_h, rep, pw, aw, m_run, l_run, o);
             __syncwarp();
             if (lane == 0) mbar_arrive(bar_empty + 8 * st);
@@ -877,14 +926,18 @@ decode_kernel_persistent(const DecodeParams p, const __grid_constant__ CUtensorM
             ml[warp * G + my_h] = l_run;
         }
         asm volatile("bar.sync 1, %0;" ::"n"(C::NCW * 32) : "memory");
+        // the shared-prefix partials are complete and visible past this point
+        if (k == 0 && p.pf_parts > 0) asm volatile("griddepcontrol.wait;" ::: "memory");
 
         const int tid = threadIdx.x;  // 0 .. 127
         const int hq0 = g * G;
         for (int idx = 2 * tid; idx < G * D; idx += 2 * C::NCW * 32) {
             const int h = idx / D, d = idx - h * D;
+            const size_t row = (size_t)s * p.n_q_heads + hq0 + h;
             float M = -INFINITY;
 #pragma unroll
             for (int w = 0; w < C::NCW; ++w) M = fmaxf(M, mm[w * G + h]);
+            if (p.pf_parts > 0) M = prefix_max(p, row, M);
             float Lsum = 0.f, o0 = 0.f, o1 = 0.f;
             if (M != -INFINITY) {
 #pragma unroll
@@ -894,9 +947,9 @@ decode_kernel_persistent(const DecodeParams p, const __grid_constant__ CUtensorM
                     o0 = fmaf(mo[(w * G + h) * D + d], wt, o0);
                     o1 = fmaf(mo[(w * G + h) * D + d + 1], wt, o1);
                 }
+                if (p.pf_parts > 0) prefix_add(p, row, d, D, M, Lsum, o0, o1);
             }
             const float inv = (Lsum > 0.f) ? 1.f / Lsum : 0.f;
-            const size_t row = (size_t)s * p.n_q_heads + hq0 + h;
             if (d < p.hd)
                 *reinterpret_cast<uint32_t*>(static_cast<uint16_t*>(p.out) + row * p.hd + d) =
                     F::pack_rn(o0 * inv, o1 * inv);
@@ -911,24 +964,29 @@ decode_kernel_persistent(const DecodeParams p, const __grid_constant__ CUtensorM
 
 // Split-K merge (mini_engine, "Custom CUDA kernels", v2 reduce): for each (s, h) with more
 // than one piece, M = max_p m_p, w_p = l_p exp(m_p - M), out = sum_p w_p o_p / sum_p w_p.
+// The shared-prefix partials (if any) take part as further pieces.
 // One CTA of 256 threads per (s, h): 8 warps take pieces round-robin, each lane 4 columns.
 template <int D, bool BF16>
 __global__ void __launch_bounds__(256) splitk_reduce_kernel(const DecodeParams p) {
     using F = F16x2<BF16>;
-    extern __shared__ float4 red_smem4[];  // w[max_parts rounded up to 4] | acc[8][D]
+    // w[max_parts rounded up to 4] | prefix weights [pf_parts rounded up to 4] | acc[8][D]
+    extern __shared__ float4 red_smem4[];
     float* red_smem = reinterpret_cast<float*>(red_smem4);
     const int row = blockIdx.x;          // s * Hq + h
     const int s = row / p.n_q_heads;
     int L = __ldg(p.context_lens + s);
-    const int cap = min(table_row_tokens(p.max_blocks_per_seq, p.cpb_log2), p.max_parts * p.part_tokens);
+    const int cap = min(table_row_tokens(p.max_blocks_per_seq, p.cpb_log2), p.prefix_tokens + p.max_parts * p.part_tokens);
     L = L < 0 ? 0 : (L > cap ? cap : L);
-    const int n_parts = (L + p.part_tokens - 1) / p.part_tokens;
+    const int n_parts = (streamed_tokens(p, L) + p.part_tokens - 1) / p.part_tokens;
     if (n_parts <= 1) return;  // written directly by the piece kernel
-    // launched as a programmatic dependent of the piece kernel: its partials are complete and
-    // visible past this point
+    // launched as a programmatic dependent of the piece kernel: its partials (and, through it, the
+    // shared-prefix pass's) are complete and visible past this point
     asm volatile("griddepcontrol.wait;" ::: "memory");
     float* wsh = red_smem;
-    float* acc = red_smem + ((p.max_parts + 3) & ~3);  // 16-byte aligned for the float4 stores
+    float* wpf = red_smem + ((p.max_parts + 3) & ~3);
+    float* acc = wpf + ((p.pf_parts + 3) & ~3);  // 16-byte aligned for the float4 stores
+    const int KP = p.pf_parts;
+    constexpr float kLn2 = 0.69314718055994531f;  // the prefix partials' m is base 2
     const float* m = p.ws_m + (size_t)row * p.max_parts;
     const float* l = p.ws_l + (size_t)row * p.max_parts;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -937,6 +995,8 @@ __global__ void __launch_bounds__(256) splitk_reduce_kernel(const DecodeParams p
 
     float mx = -INFINITY;
     for (int i = tid; i < n_parts; i += 256) mx = fmaxf(mx, m[i]);
+    for (int k = tid; k < KP; k += 256)
+        if (p.pf_l[(size_t)row * KP + k] > 0.f) mx = fmaxf(mx, p.pf_m[(size_t)row * KP + k] * kLn2);
 #pragma unroll
     for (int o = 16; o; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
     if (lane == 0) red[warp] = mx;
@@ -952,6 +1012,12 @@ __global__ void __launch_bounds__(256) splitk_reduce_kernel(const DecodeParams p
     for (int i = tid; i < n_parts; i += 256) {
         const float w = (l[i] > 0.f) ? l[i] * __expf(m[i] - M) : 0.f;
         wsh[i] = w;
+        wsum += w;
+    }
+    for (int k = tid; k < KP; k += 256) {
+        const float lk = p.pf_l[(size_t)row * KP + k];
+        const float w = (lk > 0.f) ? lk * __expf(p.pf_m[(size_t)row * KP + k] * kLn2 - M) : 0.f;
+        wpf[k] = w;
         wsum += w;
     }
 #pragma unroll
@@ -986,6 +1052,13 @@ __global__ void __launch_bounds__(256) splitk_reduce_kernel(const DecodeParams p
             const float w = wsh[i];
             if (w > 0.f) {
                 float4 x = *reinterpret_cast<const float4*>(ob + (size_t)i * D);
+                a.x += w * x.x; a.y += w * x.y; a.z += w * x.z; a.w += w * x.w;
+            }
+        }
+        for (int k = warp; k < KP; k += 8) {
+            const float w = wpf[k];
+            if (w > 0.f) {
+                float4 x = *reinterpret_cast<const float4*>(p.pf_o + ((size_t)row * KP + k) * D + c0);
                 a.x += w * x.x; a.y += w * x.y; a.z += w * x.z; a.w += w * x.w;
             }
         }

@@ -60,9 +60,25 @@ struct PrefillParams {
     int lpt;                    // 1: CTAs take units longest-first (schedule fits in shared memory)
     float qk_scale_log2;
     int hd;                     // head_dim of q, out and the cache (<= D; columns hd .. D-1 are zero)
+    // shared-prefix mode (launch_prefix): the query rows are the decode sequences (q [num_seqs,
+    // Hq, hd]), the keys the prefix's tokens [0, prefix_tokens) read through row 0 of
+    // block_tables, cut into pieces of piece_tokens; sequence s sees keys t < context_lens[s].
+    // Each (sequence, head, piece) gets a partial: pf_m (base-2 log of the weights' reference),
+    // pf_l (sum of the weights) and pf_o (the normalised output, kernel head_dim columns).
+    const int32_t* context_lens;
+    float* pf_m;                // [num_seqs * Hq][pf_parts]
+    float* pf_l;                // [num_seqs * Hq][pf_parts]
+    float* pf_o;                // [num_seqs * Hq][pf_parts][D]
+    int num_seqs, prefix_tokens, piece_tokens, pf_parts;
 };
 
 cudaError_t launch_prefill(int bf16, int head_dim, int group, const PrefillParams& params, const CUtensorMap& tmK,
                            const CUtensorMap& tmV, cudaStream_t stream);
+
+// The shared-prefix pass (prefill kernel in shared-prefix mode): grid of query-tile pairs x KV
+// heads x prefix pieces.  Its CTAs let a programmatic dependent launch (the suffix decode) start
+// at once.
+cudaError_t launch_prefix(int bf16, int head_dim, int group, const PrefillParams& params, const CUtensorMap& tmK,
+                          const CUtensorMap& tmV, cudaStream_t stream);
 
 }  // namespace pa

@@ -100,3 +100,29 @@ def test_rope_write_validation_rejects_before_any_device_work(lib):
                                          100, 1, None) == -6         # q misaligned
     assert lib.pa_rope_reshape_and_cache(vp, None, vp, vp, vp, vp, vp, vp, 4, 16, 8, 128, 16, 10, 100, 1,
                                          None) == -1                 # key NULL
+
+
+def test_shared_prefix_sizes_and_validation(lib):
+    """pa_decode_shared_prefix: with nothing shared its workspace is pa_decode's; with a shared
+    prefix it is the prefix pass's partials (pieces of 128 tokens at most: m, l, o regions, each
+    256-byte aligned) plus the split-K workspace of the tokens past the prefix.  Bad sizes are
+    rejected on the host."""
+    ws = pa.pa_decode_shared_prefix_workspace_size
+    assert ws(4, 32, 128, 32768, 0) == pa.pa_decode_workspace_size(4, 32, 128, 32768)
+    assert ws(4, 32, 128, 32768, 15) == pa.pa_decode_workspace_size(4, 32, 128, 32768)
+    rows = 128 * 16 * (1024 // 128)
+    pf = 2 * ((rows * 4 + 255) // 256 * 256) + (rows * 128 * 4 + 255) // 256 * 256
+    assert ws(128, 16, 128, 2048, 1024) == pf + pa.pa_decode_workspace_size(128, 16, 128, 2048 - 1024)
+    # only whole 16-token chunks within the longest context are shared
+    rows = 2 * 8 * 2
+    pf = 2 * ((rows * 4 + 255) // 256 * 256) + (rows * 64 * 4 + 255) // 256 * 256
+    assert ws(2, 8, 64, 200, 1000) == pf + pa.pa_decode_workspace_size(2, 8, 64, 200 - 192)
+    vp = ctypes.c_void_p(16)   # never dereferenced: validation fails first
+    call = lambda prefix, piece=0, maxL=100: lib.pa_decode_shared_prefix(
+        vp, vp, vp, vp, vp, 8, vp, maxL, 1, 8, 8, 128, 16, 10, 0.1, 1, prefix, piece, vp, 1 << 30, None)
+    assert call(129) == -5              # prefix beyond the table's 8 x 16 tokens
+    assert call(-1) == -5
+    assert call(64, maxL=129) == -5     # max_context_len beyond the table
+    assert call(64, piece=100) == -3    # pieces are multiples of 128
+    assert lib.pa_decode_shared_prefix(vp, vp, vp, vp, vp, 8, vp, 100, 1, 8, 8, 80, 16, 10, 0.1, 1, 64, 0, vp,
+                                       1 << 30, None) == -3   # head_dim

@@ -259,10 +259,8 @@ def build_workload(name: str, seed: int, *, dtype: int, n_q_heads: int, n_kv_hea
     ql = [int(x) for x in prefill_q_lens]
     cl = [int(x) for x in prefill_ctx_lens]
     assert len(ql) == len(cl)
-    if shared_prefix_blocks:
-        assert all(L > shared_prefix_blocks * bs for L in decode_lens)
     need = shared_prefix_blocks
-    need += sum(_ceil_div(L, bs) - shared_prefix_blocks for L in decode_lens)
+    need += sum(max(0, _ceil_div(L, bs) - shared_prefix_blocks) for L in decode_lens)
     need += sum(_ceil_div(c + q, bs) for q, c in zip(ql, cl))
     need += 1 + extra_blocks  # poison block + unused blocks
     nb = pool_blocks if pool_blocks is not None else need
@@ -275,14 +273,15 @@ def build_workload(name: str, seed: int, *, dtype: int, n_q_heads: int, n_kv_hea
     decode = write = prefill = None
     if decode_lens:
         S = len(decode_lens)
-        mb = max_blocks_per_seq or max(_ceil_div(L, bs) for L in decode_lens)
+        mb = max_blocks_per_seq or max([_ceil_div(L, bs) for L in decode_lens] + [shared_prefix_blocks])
         bt = np.full((S, mb), poison, dtype=np.int32)
         prefix = alloc.take(shared_prefix_blocks) if shared_prefix_blocks else np.empty(0, np.int64)
         for s, L in enumerate(decode_lens):
             nblk = _ceil_div(L, bs)
-            assert nblk <= mb
-            ids = np.concatenate([prefix, alloc.take(nblk - shared_prefix_blocks)])
-            bt[s, :nblk] = ids
+            assert max(nblk, shared_prefix_blocks) <= mb
+            # every row lists the whole shared prefix, also when its own context ends inside it
+            ids = np.concatenate([prefix, alloc.take(max(0, nblk - shared_prefix_blocks))])
+            bt[s, :ids.size] = ids
             for t0 in range(0, L, bs):
                 valid[ids[t0 // bs], : min(bs, L - t0)] = True
         q = normal_bits(derive_seed(seed, TAG_Q), S * n_q_heads * head_dim, dtype).reshape(S, n_q_heads, head_dim)
@@ -317,7 +316,7 @@ def build_workload(name: str, seed: int, *, dtype: int, n_q_heads: int, n_kv_hea
     pool = _fill_pool(seed, dtype, nb, bs, n_kv_heads, head_dim, valid, poison, nan_canaries)
     return Workload(name, seed, pool, decode, write, prefill,
                     meta=dict(dtype=dtype, n_q_heads=n_q_heads, n_kv_heads=n_kv_heads, head_dim=head_dim,
-                              block_size=bs))
+                              block_size=bs, shared_prefix_tokens=shared_prefix_blocks * bs))
 
 
 # ----------------------------------------------------------------- the five workloads
