@@ -249,15 +249,41 @@ def unique_decode_bytes(b, pool):
     return kv + 2 * nbytes(b.q) + int(np.ceil(L / bs).sum()) * 4 + nbytes(b.context_lens)
 
 
-def run_ours(args, rank, world, local_rank):
+def workload_config(w, k, wl, world):
+    """The workload a line measures: the same dict in both arms (the GPU kernels and the fp64
+    oracle), so that the two lines' configs compare equal."""
+    p, b, wr, pre = w.pool, w.decode, w.write, w.prefill
+    cfg = {"workload": workload_name(k, wl), "n_kv_heads": p.n_kv_heads, "head_dim": p.head_dim,
+           "block_size": p.block_size}
+    if b is not None:
+        cfg.update({"num_seqs": int(b.num_seqs), "n_q_heads": int(b.q.shape[1]),
+                    "total_context_tokens": int(b.context_lens.sum())})
+        if w.meta.get("shared_prefix_tokens", 0):
+            cfg["shared_prefix_tokens"] = int(w.meta["shared_prefix_tokens"])
+    if wr is not None:
+        cfg.update(write_rows=int(wr.slot_mapping.size), padded_rows=int((wr.slot_mapping < 0).sum()))
+    if pre is not None:
+        cfg.update(prefill_chunks=pre.num_chunks, prefill_rows=int(pre.q.shape[0]),
+                   prefill_kv_lens=[int(x) for x in pre.seq_lens])
+    cfg.update({"l2": "GPU arm: 512 MiB memset between timed steps, outside the events",
+                "parallelism": f"replicas x{world} (independent batches, no collective)"})
+    return cfg
+
+
+class _Ctx:
+    pass
+
+
+def prepare(args, name, dev, with_host=False):
+    """Device inputs and the launches of one step of workload `name` (every rank builds its own
+    copy of the same batch: weak scaling)."""
     import torch
     import paged_kv_cache_232_gb300 as pa
     import workloads as wl
 
-    dev = torch.device("cuda", local_rank)
-    torch.cuda.set_device(dev)
-    k = WORKLOADS[args.workload]
-    w = make_bench_workload(k, wl)   # every rank gets its own copy of the same batch (weak scaling)
+    c = _Ctx()
+    c.name, c.k = name, WORKLOADS[name]
+    w = c.w = make_bench_workload(c.k, wl)
     p, b, wr, pre = w.pool, w.decode, w.write, w.prefill
     dt = torch.bfloat16 if p.dtype == wl.BF16 else torch.float16
 
@@ -269,6 +295,7 @@ def run_ours(args, rank, world, local_rank):
 
     kc, vc = dev_bits(p.k_cache), dev_bits(p.v_cache)
     stages = []   # name, launch, algorithmic amount, kind
+    h_dev = []    # the step's inputs, for the end-to-end leg
     rope = getattr(w, "rope", None)
     if rope is not None and b is not None:
         q_host = np.concatenate([b.q, pre.q]) if pre is not None else b.q
@@ -278,15 +305,17 @@ def run_ours(args, rank, world, local_rank):
         q_rope = dev_bits(rope["q"])
     if wr is not None:
         key, val, sm = dev_bits(wr.key), dev_bits(wr.value), dev_int(wr.slot_mapping)
+        h_dev += [key, val, sm]
         if rope is None:
             stages.append(("write", lambda: pa.pa_reshape_and_cache(key, val, kc, vc, sm), write_bytes(wr, p), "hbm"))
         else:
             pos_d = dev_int(rope["positions"])
+            h_dev += [pos_d] + ([q_rope] if b is None else [])
             cos_sin = pa.rope_cos_sin(ROPE_MAX_POS, p.head_dim, ROPE_THETA, dev)
             stages.append(("rope_write", lambda: pa.pa_rope_reshape_and_cache(key, val, kc, vc, sm, pos_d, cos_sin,
                                                                               q=q_rope),
                            rope_write_bytes(w), "hbm"))
-    S, which, dec_logical = 0, 0, 0
+    S, which, dec_logical, dec_launches, part, prefix = 0, 0, 0, 0, 0, 0
     if b is not None:
         S, hq, D = b.q.shape
         if rope is None:
@@ -294,10 +323,11 @@ def run_ours(args, rank, world, local_rank):
             q = dev_bits(q_host)                   # decode rows first, then prefill rows
         out = torch.empty_like(q)
         bt, cl = dev_int(b.block_tables), dev_int(b.context_lens)
+        h_dev += [q, bt, cl]
         maxL = int(b.context_lens.max())
         ws = torch.empty(max(pa.pa_decode_workspace_size(S, hq, D, maxL, 0), 16), dtype=torch.uint8, device=dev)
-        which, part = pa.pa_decode_plan(S, hq, p.n_kv_heads, D, p.block_size, maxL,
-                                        pa.PA_BF16 if p.dtype == wl.BF16 else pa.PA_F16)
+        code = pa.PA_BF16 if p.dtype == wl.BF16 else pa.PA_F16
+        which, part = pa.pa_decode_plan(S, hq, p.n_kv_heads, D, p.block_size, maxL, code)
         if args.decode_path == "v1":
             which = 1
         elif args.decode_path == "splitk":
@@ -312,8 +342,7 @@ def run_ours(args, rank, world, local_rank):
             which = 3
             ws = torch.empty(max(pa.pa_decode_shared_prefix_workspace_size(S, hq, D, maxL, prefix), 16),
                              dtype=torch.uint8, device=dev)
-            sw, _ = pa.pa_decode_plan(S, hq, p.n_kv_heads, D, p.block_size, maxL - prefix,
-                                      pa.PA_BF16 if p.dtype == wl.BF16 else pa.PA_F16)
+            sw, part = pa.pa_decode_plan(S, hq, p.n_kv_heads, D, p.block_size, maxL - prefix, code)
             dec_launches = 2 if sw == 1 else 3
             dec_fn = lambda: pa.pa_decode_shared_prefix(out[:S], q[:S], kc, vc, bt, cl, maxL, b.scale, prefix, ws,
                                                         prefix_piece_tokens=args.prefix_piece)
@@ -337,56 +366,81 @@ def run_ours(args, rank, world, local_rank):
         # one prefill launch over every row: decode sequences as one-row chunks, then the chunks
         u = wl.unified_batch(w)
         pbt, qsl, sl = dev_int(u.block_tables), dev_int(u.query_start_loc), dev_int(u.seq_lens)
+        h_dev += [pbt, qsl, sl]
         stages = [s_ for s_ in stages if s_[0] != "decode"]
         stages.append(("unified", lambda: pa.pa_prefill_chunk(out, q, kc, vc, pbt, qsl, sl, u.max_q_len, u.scale),
                        prefill_flops(u, hq, D), "tensor"))
-        which, dec_logical = 0, 0
+        which, dec_logical, dec_launches = 0, 0, 0
     elif pre is not None:
         pbt, qsl, sl = dev_int(pre.block_tables), dev_int(pre.query_start_loc), dev_int(pre.seq_lens)
+        h_dev += [pbt, qsl, sl]
         stages.append(("prefill", lambda: pa.pa_prefill_chunk(out[S:], q[S:], kc, vc, pbt, qsl, sl, pre.max_q_len,
                                                               pre.scale),
                        prefill_flops(pre, hq, D), "tensor"))
-    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
-    stream = torch.cuda.current_stream(dev)
-    ns = len(stages)
+    c.stages, c.out, c.h_dev = stages, out, h_dev
+    c.launches = (1 if wr is not None else 0) + dec_launches + (1 if pre is not None else 0)
+    wbytes = 0 if wr is None else (rope_write_bytes(w) if rope is not None else write_bytes(wr, p))
+    c.step_bytes = wbytes + (decode_bytes(b, p) if (b is not None and args.unified) else dec_logical) + (
+        prefill_bytes(pre, p) if pre is not None else 0)
+    c.dec_logical = dec_logical
+    c.has_pre_and_dec = pre is not None and b is not None
+    c.decode_path = None
+    if b is not None:
+        c.decode_path = ("unified: decode rows as one-row chunks of the prefill launch" if which == 0
+                         else (f"shared prefix of {prefix} tokens on the tensor cores + suffix "
+                               + ("one-pass" if dec_launches == 2 else f"split-K/{part}") if which == 3
+                               else ("one-pass" if which == 1 else f"split-K/{part}"))
+                         + ("" if args.decode_path in ("auto", "plain") else " (forced)"))
+    return c
+
+
+def step_fn(c, stream):
+    ns = len(c.stages)
 
     def step(ev=None):
-        for i, st in enumerate(stages):
+        for i, st in enumerate(c.stages):
             if ev:
                 ev[i].record(stream)
             st[1]()
         if ev:
             ev[ns].record(stream)
+    return step
 
-    launches_per_step = ((1 if wr is not None else 0) + (0 if (b is None or which == 0) else dec_launches)
-                         + (1 if pre is not None else 0))
-    for _ in range(args.warmup):
+
+def time_steps(c, steps, warmup, world, local_rank, flush, stream):
+    """W untimed steps, then `steps` timed ones (L2 flushed before each, outside the events);
+    returns per-stage milliseconds [steps, stages], the clock summary and the wall time."""
+    import torch
+    import paged_kv_cache_232_gb300 as pa
+    step = step_fn(c, stream)
+    ns = len(c.stages)
+    for _ in range(warmup):
         step()
     torch.cuda.synchronize()
     assert pa.pa_device_errors(clear=True) == 0
-
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(ns + 1)] for _ in range(args.steps)]
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(ns + 1)] for _ in range(steps)]
     barrier(world)
     torch.cuda.synchronize()
     t_wall0 = time.perf_counter()
     with ClockSampler(local_rank) as clocks:
-        for i in range(args.steps):
+        for i in range(steps):
             flush.zero_()                       # L2 flush between steps, outside the timed events
             step(evs[i])
         torch.cuda.synchronize()
     barrier(world)
     t_wall = time.perf_counter() - t_wall0
-    st_ms = np.array([[e[i].elapsed_time(e[i + 1]) for i in range(ns)] for e in evs])   # [steps, stages]
+    assert pa.pa_device_errors(clear=True) == 0
+    st_ms = np.array([[e[i].elapsed_time(e[i + 1]) for i in range(ns)] for e in evs])
+    return st_ms, clocks.summary(), t_wall
+
+
+def summarize(c, st_ms, world, peaks, traffic=None):
+    """Step time (max over ranks), whole-job value, per-stage rates and the dominant kernel's
+    roofline."""
     step_ms = max_over_ranks(float(st_ms.sum(axis=1).mean()), world)
     mean_ms = st_ms.mean(axis=0)
-
-    wbytes = 0 if wr is None else (rope_write_bytes(w) if rope is not None else write_bytes(wr, p))
-    step_bytes = wbytes + (decode_bytes(b, p) if (b is not None and args.unified) else dec_logical) + (
-        prefill_bytes(pre, p) if pre is not None else 0)
-    value = world * step_bytes / (step_ms * 1e-3) / 1e9
-    peaks = measured_peaks()
     breakdown = {}
-    for (name, _, amount, kind), ms in zip(stages, mean_ms):
+    for (name, _, amount, kind), ms in zip(c.stages, mean_ms):
         if kind == "hbm":
             breakdown[name] = {"us": round(float(ms) * 1e3, 2), "gbs": round(amount / (ms * 1e-3) / 1e9, 1),
                                "frac_hbm": round(amount / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"], 4)}
@@ -394,43 +448,58 @@ def run_ours(args, rank, world, local_rank):
             breakdown[name] = {"us": round(float(ms) * 1e3, 2), "tflops": round(amount / (ms * 1e-3) / 1e12, 1),
                                "frac_bf16": round(amount / (ms * 1e-3) / 1e12 / peaks["bf16_tflops"], 4),
                                "flop": amount}
-    if pre is not None and b is not None and "decode" in breakdown:
-        breakdown["decode"]["logical_gbs"] = round(dec_logical / (mean_ms[0] * 1e-3) / 1e9, 1)
+    if c.has_pre_and_dec and "decode" in breakdown:
+        breakdown["decode"]["logical_gbs"] = round(c.dec_logical / (mean_ms[0] * 1e-3) / 1e9, 1)
+        breakdown["decode"]["note"] = "gbs / frac_hbm on unique bytes (a shared block counted once)"
     dom = int(np.argmax(mean_ms))
-    dname, _, damount, dkind = stages[dom]
+    dname, _, damount, dkind = c.stages[dom]
     dms = float(mean_ms[dom])
+    if traffic is None:
+        traffic = recorded_traffic(c.name, dname)
     if dkind == "hbm":
         ach = damount / (dms * 1e-3) / 1e9
         roof = {"bound": "hbm", "kernel": f"{dname}", "achieved": round(ach, 1), "peak": peaks["hbm_gbs"],
                 "peak_source": peaks["source"], "unit": "GB/s", "frac": round(ach / peaks["hbm_gbs"], 4),
-                "traffic": args.traffic if args.traffic is not None else recorded_traffic(args.workload, dname),
-                "algorithmic_bytes": damount}
+                "traffic": traffic, "algorithmic_bytes": damount}
     else:
         ach = damount / (dms * 1e-3) / 1e12
         roof = {"bound": "tensor", "kernel": f"{dname}", "achieved": round(ach, 1), "peak": peaks["bf16_tflops"],
                 "peak_source": peaks["source"], "unit": "TFLOP/s", "frac": round(ach / peaks["bf16_tflops"], 4),
-                "traffic": args.traffic if args.traffic is not None else recorded_traffic(args.workload, dname),
-                "algorithmic_flops": damount}
+                "traffic": traffic, "algorithmic_flops": damount}
+    return step_ms, world * c.step_bytes / (step_ms * 1e-3) / 1e9, breakdown, roof
+
+
+# every configuration of the workload list, measured after the headline in the default run
+ALL_CONFIGS = ("single", "decode64", "long4", "mixed", "write64k")
+
+
+def run_ours(args, rank, world, local_rank):
+    import torch
+    import paged_kv_cache_232_gb300 as pa
+    import workloads as wl
+
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    c = prepare(args, args.workload, dev)
+    p = c.w.pool
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    peaks = measured_peaks()
+    st_ms, clocks, t_wall = time_steps(c, args.steps, args.warmup, world, local_rank, flush, stream)
+    step_ms, value, breakdown, roof = summarize(c, st_ms, world, peaks, args.traffic)
 
     # end to end through the C ABI with host buffers: inputs up, result down, every step
-    pin = lambda t: t.cpu().pin_memory()
-    h_in = [(q, pin(q)), (bt, pin(bt)), (cl, pin(cl))] if b is not None else []
-    if rope is not None:
-        h_in += [(pos_d, pin(pos_d))] + ([(q_rope, pin(q_rope))] if b is None else [])
-    if wr is not None:
-        h_in += [(key, pin(key)), (val, pin(val)), (sm, pin(sm))]
-    if pre is not None:
-        h_in += [(pbt, pin(pbt)), (qsl, pin(qsl)), (sl, pin(sl))]
-    h_out = torch.empty_like(out, device="cpu").pin_memory()
+    h_in = [(t, t.cpu().pin_memory()) for t in c.h_dev]
+    h_out = torch.empty_like(c.out, device="cpu").pin_memory()
     h2d = sum(t.numel() * t.element_size() for t, _ in h_in)
-    d2h = out.numel() * out.element_size()
+    d2h = c.out.numel() * c.out.element_size()
 
     def e2e_step():
         for d_, h_ in h_in:
             d_.copy_(h_, non_blocking=True)
-        for st in stages:
+        for st in c.stages:
             st[1]()
-        h_out.copy_(out, non_blocking=True)
+        h_out.copy_(c.out, non_blocking=True)
 
     for _ in range(3):
         e2e_step()
@@ -442,14 +511,14 @@ def run_ours(args, rank, world, local_rank):
         e2e_step()
         e2e_ev[i][1].record(stream)
     torch.cuda.synchronize()
-    e2e_ms = max_over_ranks(float(np.mean([a.elapsed_time(c) for a, c in e2e_ev])), world)
+    e2e_ms = max_over_ranks(float(np.mean([a.elapsed_time(b_) for a, b_ in e2e_ev])), world)
 
     # the same step captured once into a CUDA graph and replayed (launch overhead removed)
     graph_ms = None
     try:
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g):
-            for st in stages:
+            for st in c.stages:
                 st[1]()
         for _ in range(3):
             g.replay()
@@ -461,26 +530,11 @@ def run_ours(args, rank, world, local_rank):
             g.replay()
             g_ev[i][1].record(stream)
         torch.cuda.synchronize()
-        graph_ms = max_over_ranks(float(np.mean([a.elapsed_time(c) for a, c in g_ev])), world)
+        graph_ms = max_over_ranks(float(np.mean([a.elapsed_time(b_) for a, b_ in g_ev])), world)
         assert pa.pa_device_errors(clear=True) == 0
     except RuntimeError as ex:   # capture refused: report it instead of a number
         graph_ms = f"capture failed: {str(ex).splitlines()[0][:120]}"
 
-    cfg = {"workload": workload_name(k, wl), "n_kv_heads": p.n_kv_heads, "head_dim": p.head_dim,
-           "block_size": p.block_size}
-    if b is not None:
-        cfg.update({"num_seqs": int(S), "n_q_heads": int(hq), "total_context_tokens": int(b.context_lens.sum()),
-                    "decode_path": ("unified: decode rows as one-row chunks of the prefill launch" if which == 0
-                                    else (f"shared prefix of {prefix} tokens on the tensor cores + suffix decode"
-                                          if which == 3 else ("one-pass" if which == 1 else f"split-K/{part}"))
-                                    + ("" if args.decode_path in ("auto", "plain") else " (forced)"))})
-    cfg.update({"l2": "512 MiB memset between timed steps (outside the events)",
-                "parallelism": f"replicas x{world} (independent batches, no collective)"})
-    if wr is not None:
-        cfg.update(write_rows=int(wr.slot_mapping.size), padded_rows=int((wr.slot_mapping < 0).sum()))
-    if pre is not None:
-        cfg.update(prefill_chunks=pre.num_chunks, prefill_rows=int(pre.q.shape[0]),
-                   prefill_kv_lens=[int(x) for x in pre.seq_lens])
     res = {
         "metric": "paged decode attn us/step & achieved HBM GB/s (% of GB300 peak); KV-write GB/s",
         "value": round(value, 2),
@@ -495,28 +549,49 @@ def run_ours(args, rank, world, local_rank):
         "vs_baseline": None,
         "dtype": "bf16" if p.dtype == wl.BF16 else "f16",
         "data": "synthetic (seeded SplitMix64/Box-Muller N(0,1), RNE to the 16-bit format)",
-        "config": cfg,
+        "config": workload_config(c.w, c.k, wl, world),
+        "decode_path": c.decode_path,
         "breakdown": breakdown,
-        "step_bytes": step_bytes,
+        "step_bytes": c.step_bytes,
         "roofline": roof,
         "e2e": {
-            "value": round(world * step_bytes / (e2e_ms * 1e-3) / 1e9, 2),
+            "value": round(world * c.step_bytes / (e2e_ms * 1e-3) / 1e9, 2),
             "unit": "GB/s",
             "ms_per_step": round(e2e_ms, 5),
             "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h,
         },
-        "graph": ({"us_per_step": round(graph_ms * 1e3, 2), "value": round(world * step_bytes / (graph_ms * 1e-3) / 1e9, 2),
+        "graph": ({"us_per_step": round(graph_ms * 1e3, 2),
+                   "value": round(world * c.step_bytes / (graph_ms * 1e-3) / 1e9, 2),
                    "unit": "GB/s", "note": "the step's launches captured once into a CUDA graph, replayed per step"}
                   if isinstance(graph_ms, float) else {"unavailable": graph_ms}),
-        "gpu_launches": launches_per_step * args.steps,
+        "gpu_launches": c.launches * args.steps,
         "wall_s_timed_region": round(t_wall, 4),
     }
-    cs = clocks.summary()
-    if cs:
-        res["clocks"] = cs
+    if clocks:
+        res["clocks"] = clocks
+    w_head, k_head = c.w, c.k
+    del c, h_in, h_out, e2e_step
+    if args.all_configs and args.workload == "step256":
+        # the other configurations, each timed the same way in this run (its own clocks)
+        extra = argparse.Namespace(**vars(args))
+        extra.decode_path, extra.unified, extra.partition, extra.prefix_piece = "auto", False, 0, 0
+        res["workloads"] = {}
+        for name in ALL_CONFIGS:
+            torch.cuda.empty_cache()
+            c2 = prepare(extra, name, dev)
+            st2, clk2, _ = time_steps(c2, args.steps, args.warmup, world, local_rank, flush, stream)
+            ms2, val2, br2, roof2 = summarize(c2, st2, world, peaks)
+            res["workloads"][name] = {
+                "config": workload_config(c2.w, c2.k, wl, world), "decode_path": c2.decode_path,
+                "us_per_step": round(ms2 * 1e3, 2), "value": round(val2, 2), "unit": "GB/s",
+                "breakdown": br2, "roofline": roof2, "gpu_launches": c2.launches * args.steps,
+                "clocks": clk2,
+            }
+            del c2
     if rank == 0 and not args.no_cpu_baseline:
-        res["cpu_baseline"] = cpu_baseline(w, k, budget_s=args.cpu_seconds)
+        res["cpu_baseline"] = cpu_baseline(w_head, k_head, budget_s=args.cpu_seconds,
+                                           single_thread=args.all_configs and args.workload == "step256")
     return res
 
 
@@ -567,8 +642,7 @@ def _sample_size(w, budget_s):
     return n, nb, dt
 
 
-def cpu_baseline(w, k, budget_s=10.0):
-    import oracle
+def _timed_oracle(w, budget_s):
     n, nb, dt = _sample_size(w, budget_s)
     # time enough repetitions of the sample to fill roughly the budget
     reps = max(1, int(budget_s / max(dt, 1e-3)))
@@ -578,9 +652,30 @@ def cpu_baseline(w, k, budget_s=10.0):
         b_, _ = oracle_sample_step(w, n)
         tot += b_
     el = time.perf_counter() - t0
-    return {"value": round(tot / el / 1e9, 4), "unit": "GB/s", "cores": oracle.num_threads(), "kind": "oracle",
-            "sample": (f"{n} of {w.decode.num_seqs} sequences (their write rows + decode)" if w.decode is not None
-                       else f"{n} of {sample_units(w)} write rows") + f", {reps} reps, {el:.1f} s"}
+    what = (f"{n} of {w.decode.num_seqs} sequences (their write rows + decode)" if w.decode is not None
+            else f"{n} of {sample_units(w)} write rows") + f", {reps} reps, {el:.1f} s"
+    return tot / el / 1e9, what
+
+
+def cpu_baseline(w, k, budget_s=10.0, single_thread=False):
+    """The fp64 oracle as it stands on the host's cores (all of them), on a bounded sample of
+    the same workload; with single_thread, also on one core for the single-request, batch-64
+    and long-context decode workloads."""
+    import oracle
+    import workloads as wl
+    v, what = _timed_oracle(w, budget_s)
+    res = {"value": round(v, 4), "unit": "GB/s", "cores": oracle.num_threads(), "kind": "oracle", "sample": what}
+    if single_thread:
+        all_cores = oracle.num_threads()
+        oracle.set_num_threads(1)
+        try:
+            res["single_thread"] = {}
+            for name in ("single", "decode64", "long4"):
+                v1, what1 = _timed_oracle(make_bench_workload(WORKLOADS[name], wl), 2.0)
+                res["single_thread"][name] = {"value": round(v1, 4), "unit": "GB/s", "cores": 1, "sample": what1}
+        finally:
+            oracle.set_num_threads(all_cores)
+    return res
 
 
 def run_reference(args, rank, world):
@@ -607,7 +702,7 @@ def run_reference(args, rank, world):
         "value": round(value, 4), "unit": "GB/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(el / args.steps * 1e3, 3), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic (same seeded workload)",
-        "config": {"workload": workload_name(k, wl), f"num_{what.replace(' ', '_')}": units, "sampled": n},
+        "config": workload_config(w, k, wl, world),
         "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": oracle.num_threads(), "kind": "oracle",
                          "sample": f"{n} of {units} {what} per step"},
         "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -650,9 +745,12 @@ def main(argv=None):
     ap.add_argument("--prefix-piece", type=int, default=0,
                     help="shared-prefix pass: keys per CTA (multiple of 128; 0 = the library's choice)")
     ap.add_argument("--partition", type=int, default=0, help="split-K piece length in tokens (with --decode-path splitk)")
+    ap.add_argument("--headline-only", action="store_true",
+                    help="skip the other configurations the default (batch-256 step) run also measures")
     ap.add_argument("--traffic", type=float, default=None,
                     help="dram bytes per decode launch from an ncu capture of this workload (reported as-is)")
     args = ap.parse_args(argv)
+    args.all_configs = not args.headline_only
     assert args.warmup >= 3, "at least 3 warm-up steps"
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))

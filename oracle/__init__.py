@@ -90,6 +90,8 @@ def lib():
         L.pao_naive_contiguous.argtypes = [vp, vp, vp, vp, vp, i32, vp, i32, i32, i32, i32, i32, i64, dbl, i32]
         L.pao_naive_contiguous.restype = i32
         L.pao_num_threads.restype = i32
+        L.pao_set_num_threads.argtypes = [i32]
+        L.pao_set_num_threads.restype = None
         _lib = L
     return _lib
 
@@ -101,6 +103,11 @@ def _c(a, dtype):
 
 def num_threads() -> int:
     return int(lib().pao_num_threads())
+
+
+def set_num_threads(n: int) -> None:
+    """Threads the oracle's OpenMP loops use from now on (results do not depend on it)."""
+    lib().pao_set_num_threads(int(n))
 
 
 def to_double(bits, dtype: int) -> np.ndarray:

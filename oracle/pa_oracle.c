@@ -493,6 +493,16 @@ int pao_naive_contiguous(double* out, const uint16_t* q, const uint16_t* k_cache
     return PAO_OK;
 }
 
+/* Threads the OpenMP loops use from now on (the bench times the oracle on one core as well as on
+ * all of them); no effect on any result: every row is computed the same way by whichever thread. */
+void pao_set_num_threads(int n) {
+#ifdef _OPENMP
+    if (n > 0) omp_set_num_threads(n);
+#else
+    (void)n;
+#endif
+}
+
 int pao_num_threads(void) {
 #ifdef _OPENMP
     return omp_get_max_threads();
