@@ -211,7 +211,10 @@ int decode_impl(void* out, const void* q, const void* k_cache, const void* v_cac
         const int64_t nb = ((int64_t)max_blocks_per_seq * block_size + 15) / 16 + 2;
         const int ring = pa::decode_ring_bytes(kernel_dim(head_dim));
         p.lpt = (resident > 0 && units > slots && ((int64_t)num_seqs + nb) * 4 <= ring) ? 1 : 0;
-        p.persist = (p.lpt && n_q_heads / n_kv_heads <= 2 && units >= 2 * slots &&
+        // (not after a shared-prefix pass: its CTAs hold some SMs at the start, and the persistent
+        // grid's fixed unit lists cannot move work off those SMs; hardware dispatch can -- GB300,
+        // mixed batch decode rows 64.2 -> 62.1 us)
+        p.persist = (p.lpt && p.pf_parts == 0 && n_q_heads / n_kv_heads <= 2 && units >= 2 * slots &&
                      units <= (int64_t)pa::decode_list_max() * slots && (2 * (int64_t)num_seqs + 2 * nb) * 4 <= ring)
                         ? 1 : 0;
         if (p.persist) grid = (int)slots;

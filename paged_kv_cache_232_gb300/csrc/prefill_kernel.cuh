@@ -206,9 +206,12 @@ __device__ __forceinline__ void tmem_store16_stride2(uint32_t taddr, const uint3
 // reference; a sub-tile whose weights outgrow that is redone with a raised reference (S is
 // still intact), after O -- complete through the previous sub-tile's PV -- is rescaled.
 template <bool BF16, int D>
+// pv_wait: O holds earlier PVs of this row's unit (the previous one must be complete before a
+// rescale), pv_parity: the parity of that PV's PV_DONE phase.
 __device__ __forceinline__ void softmax_sub64(const uint32_t tSb, const uint32_t tO, const bool masked, const int kbase,
                                               const int lim, const float sc, float& m_ref, float& l,
-                                              const uint32_t pv_done, const int u, unsigned* err) {
+                                              const uint32_t pv_done, const bool pv_wait, const uint32_t pv_parity,
+                                              unsigned* err) {
     using F = F16x2<BF16>;
     constexpr uint32_t kBits256 = BF16 ? 0x4380u : 0x5C00u;  // 2^8 as a packed 16-bit value
     // decided per warp: the branch holds warp-collective TMEM loads and stores
@@ -239,7 +242,7 @@ __device__ __forceinline__ void softmax_sub64(const uint32_t tSb, const uint32_t
             if (__any_sync(0xffffffffu, alpha != 1.f)) {
                 // O must hold every PV before this sub-tile (and none after: its PV waits for
                 // these weights)
-                if (u > 0) (void)warp_wait(pv_done, (u - 1) & 1, err);
+                if (pv_wait) (void)warp_wait(pv_done, pv_parity, err);
                 tc::fence_after();
 #pragma unroll 1
                 for (int q = 0; q < D / 16; ++q) {
@@ -467,7 +470,7 @@ prefill_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmK, c
             tc::fence_after();
             const int kbase = k0 + u * BS;
             softmax_sub64<BF16, D>(tS + (uint32_t)(b * BS), tO, kbase + BS - 1 > lim_min, kbase, lim, sc, m_ref, l,
-                                bars + 8 * (PV_DONE + t), u, p.err);
+                                bars + 8 * (PV_DONE + t), u > 0, (uint32_t)((u - 1) & 1), p.err);
             tc::wait_st();
             tc::fence_before();
             __syncwarp();

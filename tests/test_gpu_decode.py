@@ -116,6 +116,23 @@ def test_decode_edge_lengths(dt, hq, hkv, d, mode, part):
     check(got, oracle_decode(w), dt, f"edge {mode}/{part}")
 
 
+@pytest.mark.parametrize("mode,part", [("v1", 0), ("splitk", 0), ("splitk", 64), ("splitk", 512), ("auto", 0)])
+def test_decode_empty_contexts_among_others(mode, part):
+    """Sequences with an empty context give an all-zero row, whichever grid runs them (in the
+    split-K grid's longest-first order such a sequence has one empty piece, ranked last)."""
+    lens = [0, 300, 0, 1000, 17, 0, 2049, 1]
+    w = wl.build_workload("empty", 91, dtype=wl.BF16, n_q_heads=16, n_kv_heads=8, head_dim=128,
+                          decode_lens=[max(L, 1) for L in lens], max_blocks_per_seq=200, extra_blocks=3)
+    w.decode.context_lens = np.asarray(lens, dtype=np.int32)
+    got = Dev(w).run(mode, part)
+    check(got, oracle_decode(w), wl.BF16, f"empty contexts {mode}/{part}")
+    rows = got.reshape(len(lens), 16, 128)
+    for s_, L in enumerate(lens):
+        if L == 0:
+            assert not rows[s_].any(), f"row {s_} not zero"
+    assert pa.pa_device_errors(clear=True) == 0
+
+
 def test_single_token_context_returns_v_bitwise():
     w = wl.build_workload("one", 5, dtype=wl.BF16, n_q_heads=16, n_kv_heads=8, head_dim=128, decode_lens=[1] * 9)
     p, b = w.pool, w.decode
