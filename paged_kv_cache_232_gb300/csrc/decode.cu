@@ -35,24 +35,11 @@ static cudaError_t launch_decode_t(const DecodeParams& p, const CUtensorMap& tmK
                                    bool with_reduce, cudaStream_t st) {
     using C = DecodeCfg<D, G, BF16>;
     cudaError_t e;
-    // after a shared-prefix pass the decode is its programmatic dependent: its CTAs start while
-    // that pass runs and wait for its partials (griddepcontrol.wait) only at their merge
+    // always a programmatic dependent launch: its grid is set up while the previous kernel of the
+    // stream drains (a KV write signals at its start), and its CTAs wait (griddepcontrol.wait)
+    // before reading anything; after a shared-prefix pass they wait only at their merge
     auto launch = [&](auto kern, int smem) -> cudaError_t {
-        if (p.pf_parts <= 0) {
-            kern<<<grid, C::THREADS, smem, st>>>(p, tmK, tmV);
-            return cudaGetLastError();
-        }
-        cudaLaunchConfig_t cfg = {};
-        cfg.gridDim = dim3((unsigned)grid);
-        cfg.blockDim = dim3(C::THREADS);
-        cfg.dynamicSmemBytes = (size_t)smem;
-        cfg.stream = st;
-        cudaLaunchAttribute attr[1];
-        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-        attr[0].val.programmaticStreamSerializationAllowed = 1;
-        cfg.attrs = attr;
-        cfg.numAttrs = 1;
-        return cudaLaunchKernelEx(&cfg, kern, p, tmK, tmV);
+        return launch_dependent(kern, (unsigned)grid, C::THREADS, (size_t)smem, st, p, tmK, tmV);
     };
     if (p.persist) {
         // group sizes 1 and 2 only: larger groups run out of registers in the unit loop
@@ -82,17 +69,7 @@ static cudaError_t launch_decode_t(const DecodeParams& p, const CUtensorMap& tmK
     }
     // a programmatic dependent launch: the merge grid is set up while the piece kernel drains and
     // waits for it (griddepcontrol.wait) before reading the partials
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)(p.num_seqs * p.n_q_heads));
-    cfg.blockDim = dim3(256);
-    cfg.dynamicSmemBytes = red_smem;
-    cfg.stream = st;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, rk, p);
+    return launch_dependent(rk, (unsigned)(p.num_seqs * p.n_q_heads), 256, red_smem, st, p);
 }
 
 template <int D, bool BF16>

@@ -423,6 +423,10 @@ decode_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmK, con
     const uint32_t bar_full = ring + C::BAR_OFF;
     const uint32_t bar_empty = bar_full + C::NST * 8;
 
+    // launched as a programmatic dependent of whatever kernel precedes it in the stream: nothing is
+    // read before that kernel has completed (a no-op when it never signalled early); after a
+    // shared-prefix pass, which waited itself before letting this grid launch, only the merge waits
+    if (p.pf_parts == 0) asm volatile("griddepcontrol.wait;" ::: "memory");
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int units = p.num_seqs * p.n_kv_heads;
     // split-K: the grid runs the highest piece index first -- only long contexts have one -- so the
@@ -699,6 +703,10 @@ decode_kernel_persistent(const DecodeParams p, const __grid_constant__ CUtensorM
     const uint32_t bar_full = ring + C::P_BAR_OFF;
     const uint32_t bar_empty = bar_full + C::NST * 8;
 
+    // launched as a programmatic dependent of whatever kernel precedes it in the stream: nothing is
+    // read before that kernel has completed (a no-op when it never signalled early); after a
+    // shared-prefix pass, which waited itself before letting this grid launch, only the merge waits
+    if (p.pf_parts == 0) asm volatile("griddepcontrol.wait;" ::: "memory");
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     int* list = reinterpret_cast<int*>(smem + C::P_LIST_OFF);
     volatile int* flags = reinterpret_cast<volatile int*>(smem + C::P_FLAG_OFF);  // [0] units, [1] abort

@@ -21,6 +21,9 @@ __global__ void kv_write_kernel(const uint4* __restrict__ key, const uint4* __re
                                 int row_vecs, int64_t num_slots, unsigned* err) {
     constexpr int U = kKvWriteRowsPerIter;
     const int t = threadIdx.x;
+    // the next kernel of the step (the decode, launched as a programmatic dependent) may start its
+    // launch now; it waits (griddepcontrol.wait) for this grid to complete before reading the cache
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     for (int64_t r0 = (int64_t)blockIdx.x * U; r0 < num_tokens; r0 += (int64_t)gridDim.x * U) {
         int64_t slot[U];
 #pragma unroll

@@ -26,6 +26,25 @@ inline cudaError_t smem_limit_once(const void* func, int bytes, std::atomic<unsi
 }
 
 
+// Launch `kern` as a programmatic dependent of the previous kernel in the stream: its grid may be
+// set up while that kernel drains; the kernel itself executes griddepcontrol.wait before reading
+// anything the previous kernel may write (a no-op when that kernel never signalled early).
+template <typename Kern, typename... Args>
+inline cudaError_t launch_dependent(Kern kern, unsigned grid, unsigned block, size_t smem, cudaStream_t st,
+                                    Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(block);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, args...);
+}
+
 // Launch the decode piece kernel for (dtype, head_dim, group) on `grid` CTAs; when
 // params.part_tokens > 0 and any sequence has more than one piece, also launch the reduce.
 // Bytes of the decode kernel's ring for head_dim (64, 128 or 256).

@@ -19,8 +19,7 @@ static cudaError_t launch_prefill_t(const PrefillParams& p, const CUtensorMap& t
     const long sched_words = 2L * p.num_chunks + 1 + ncost + 3 + pf::THREADS / 32;
     q.lpt = (sched_words * 4 <= pf::SCHED_BYTES) ? 1 : 0;
     const int grid = units * p.num_chunks * p.n_kv_heads;
-    kern<<<grid, pf::THREADS, pf::Layout<D>::SMEM_BYTES, st>>>(q, tmK, tmV);
-    return cudaGetLastError();
+    return launch_dependent(kern, (unsigned)grid, pf::THREADS, pf::Layout<D>::SMEM_BYTES, st, q, tmK, tmV);
 }
 
 template <bool BF16, int D>

@@ -308,9 +308,12 @@ prefill_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmK, c
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     int unit, c, g, q0, q_len, kv_len;
     int k0 = 0, piece = 0;  // shared-prefix mode: the piece and its first key
+    // launched as a programmatic dependent of whatever kernel precedes it in the stream: nothing is
+    // read before that kernel has completed (a no-op when it never signalled early)
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     if constexpr (PREFIX) {
-        // the suffix decode, launched as a programmatic dependent, may start now: it reads these
-        // partials only after its griddepcontrol.wait
+        // the suffix decode, launched as a programmatic dependent, may start now (its inputs are
+        // complete: this grid has waited above); it reads these partials only after its own wait
         asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
         const int pairs = p.tiles_per_chunk;
         unit = (int)blockIdx.x % pairs;

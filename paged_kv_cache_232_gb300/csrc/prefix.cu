@@ -25,8 +25,7 @@ static cudaError_t launch_prefix_t(const PrefillParams& p, const CUtensorMap& tm
     q.lpt = 0;
     const long grid = (long)q.tiles_per_chunk * p.n_kv_heads * p.pf_parts;
     if (grid <= 0 || grid > 0x7fffffffL) return cudaErrorInvalidValue;
-    kern<<<(unsigned)grid, pf::THREADS, pf::Layout<D>::SMEM_BYTES, st>>>(q, tmK, tmV);
-    return cudaGetLastError();
+    return launch_dependent(kern, (unsigned)grid, pf::THREADS, pf::Layout<D>::SMEM_BYTES, st, q, tmK, tmV);
 }
 
 template <bool BF16, int D>

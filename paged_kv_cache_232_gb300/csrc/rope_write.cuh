@@ -53,6 +53,9 @@ __global__ void rope_write_kernel(uint4* q, const uint4* __restrict__ key, const
     constexpr int PAIRS = D / 16;  // rotation chunk pairs per head row (= chunk distance of D/2)
     const int nq = q ? n_q_heads * PAIRS : 0, nk = n_kv_heads * PAIRS, nv = n_kv_heads * VEC;
     const int units = nq + nk + nv;
+    // the next kernel of the step (the decode, launched as a programmatic dependent) may start its
+    // launch now; it waits (griddepcontrol.wait) for this grid to complete before reading anything
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     for (int64_t r0 = (int64_t)blockIdx.x * R; r0 < num_tokens; r0 += (int64_t)gridDim.x * R) {
         int64_t pos[R], slot[R];
         bool live[R];
