@@ -115,3 +115,52 @@ def test_prefill_graph_replay_matches_eager():
     torch.cuda.synchronize()
     assert np.array_equal(bits_of(out), eager)
     assert pa.pa_device_errors(clear=True) == 0
+
+
+@pytest.mark.parametrize("case", ["mixed", "split_suffix"])
+def test_shared_prefix_graph_replay(case):
+    """pa_decode_shared_prefix captured once -- the prefix pass, the suffix decode as its
+    programmatic dependent and, for long suffixes, the split-K merge as theirs -- replays bit for
+    bit, and after new query rows and shorter contexts are written in place it matches the oracle
+    (mini_engine, "Features": shared prefix blocks; "Roadmap": decode CUDA graphs)."""
+    if case == "mixed":
+        w = wl.make_workload(5)
+        P = 1024
+    else:
+        w = wl.build_workload("gsp", 61, dtype=wl.BF16, n_q_heads=32, n_kv_heads=8, head_dim=128,
+                              decode_lens=[12000, 9000, 16000, 2049], shared_prefix_blocks=128)
+        P = 2048
+    p, b = w.pool, w.decode
+    kc, vc = to_dev(p.k_cache, p.dtype), to_dev(p.v_cache, p.dtype)
+    q = to_dev(b.q, p.dtype)
+    out = torch.empty_like(q)
+    bt, cl = to_dev_i(b.block_tables, torch.int32), to_dev_i(b.context_lens, torch.int32)
+    maxL = int(b.context_lens.max())
+    S, hq, D = b.q.shape
+    ws = torch.zeros(pa.pa_decode_shared_prefix_workspace_size(S, hq, D, maxL, P), dtype=torch.uint8, device="cuda")
+
+    def step():
+        pa.pa_decode_shared_prefix(out, q, kc, vc, bt, cl, maxL, b.scale, P, ws)
+
+    step()                                   # eager first call: one-time set-up
+    torch.cuda.synchronize()
+    eager = bits_of(out)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        step()
+    out.fill_(float("nan"))
+    g.replay()
+    torch.cuda.synchronize()
+    assert np.array_equal(bits_of(out), eager)
+    # new inputs in place: fresh query rows, contexts shortened by up to 50 tokens (never below 1)
+    q_new = wl.normal_bits(wl.derive_seed(61, 9), b.q.size, p.dtype).reshape(b.q.shape)
+    cut = wl.uniform_ints(wl.derive_seed(61, 10), S, 0, 50).astype(np.int32)
+    lens = np.maximum(b.context_lens - cut, 1).astype(np.int32)
+    q.copy_(to_dev(q_new, p.dtype))
+    cl.copy_(to_dev_i(lens, torch.int32))
+    g.replay()
+    torch.cuda.synchronize()
+    ex = oracle.decode(q_new, p.k_cache, p.v_cache, b.block_tables, lens, b.scale, p.dtype)
+    cd = oracle.decode(q_new, p.k_cache, abs_bits(p.v_cache), b.block_tables, lens, b.scale, p.dtype)
+    check_attention(bits_of(out), ex, p.dtype, f"shared prefix replay {case}", cond=cd, rel=1e-4 + 2.0 ** -16)
+    assert pa.pa_device_errors(clear=True) == 0
