@@ -33,6 +33,21 @@ sys.path.insert(0, ROOT)
 FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
 L2_FLUSH_BYTES = 512 << 20
+L2_CLEAN_BYTES = 256 << 20
+
+
+class L2Flush:
+    """Between timed steps (outside the events): write a buffer four times the L2 (129 MB) and
+    then read another twice its size, so that a step starts with nothing of its own data in L2
+    and with no dirty lines from the flush still to be written back during it."""
+
+    def __init__(self, torch, dev):
+        self.w = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+        self.r = torch.zeros(L2_CLEAN_BYTES // 4, dtype=torch.float32, device=dev)
+
+    def __call__(self):
+        self.w.zero_()
+        self.r.sum()
 
 
 # ----------------------------------------------------------------------------- helpers
@@ -265,7 +280,8 @@ def workload_config(w, k, wl, world):
     if pre is not None:
         cfg.update(prefill_chunks=pre.num_chunks, prefill_rows=int(pre.q.shape[0]),
                    prefill_kv_lens=[int(x) for x in pre.seq_lens])
-    cfg.update({"l2": "GPU arm: 512 MiB memset between timed steps, outside the events",
+    cfg.update({"l2": "GPU arm: between timed steps, outside the events, a 512 MiB memset (L2 flush) then a 256 MiB "
+                      "read (no dirty flush lines left to write back)",
                 "parallelism": f"replicas x{world} (independent batches, no collective)"})
     return cfg
 
@@ -407,9 +423,12 @@ def step_fn(c, stream):
     return step
 
 
-def time_steps(c, steps, warmup, world, local_rank, flush, stream):
-    """W untimed steps, then `steps` timed ones (L2 flushed before each, outside the events);
-    returns per-stage milliseconds [steps, stages], the clock summary and the wall time."""
+def time_steps(c, steps, warmup, world, local_rank, flush, stream, per_stage=True):
+    """W untimed steps, then `steps` timed ones (L2 flushed before each, outside the events).
+    per_stage: an event between every two launches, returning milliseconds [steps, stages];
+    otherwise events only around each whole step (the launches of a step run back to back, as
+    in use: the decode is a programmatic dependent of the write), returning [steps, 1].  Also
+    returns the clock summary and the wall time."""
     import torch
     import paged_kv_cache_232_gb300 as pa
     step = step_fn(c, stream)
@@ -418,26 +437,31 @@ def time_steps(c, steps, warmup, world, local_rank, flush, stream):
         step()
     torch.cuda.synchronize()
     assert pa.pa_device_errors(clear=True) == 0
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(ns + 1)] for _ in range(steps)]
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(ns + 1 if per_stage else 2)] for _ in range(steps)]
     barrier(world)
     torch.cuda.synchronize()
     t_wall0 = time.perf_counter()
     with ClockSampler(local_rank) as clocks:
         for i in range(steps):
-            flush.zero_()                       # L2 flush between steps, outside the timed events
-            step(evs[i])
+            flush()                             # L2 flush between steps, outside the timed events
+            if per_stage:
+                step(evs[i])
+            else:
+                evs[i][0].record(stream)
+                step()
+                evs[i][1].record(stream)
         torch.cuda.synchronize()
     barrier(world)
     t_wall = time.perf_counter() - t_wall0
     assert pa.pa_device_errors(clear=True) == 0
-    st_ms = np.array([[e[i].elapsed_time(e[i + 1]) for i in range(ns)] for e in evs])
+    st_ms = np.array([[e[i].elapsed_time(e[i + 1]) for i in range(len(e) - 1)] for e in evs])
     return st_ms, clocks.summary(), t_wall
 
 
-def summarize(c, st_ms, world, peaks, traffic=None):
-    """Step time (max over ranks), whole-job value, per-stage rates and the dominant kernel's
-    roofline."""
-    step_ms = max_over_ranks(float(st_ms.sum(axis=1).mean()), world)
+def summarize(c, st_ms, world, peaks, traffic=None, whole_ms=None):
+    """Step time (max over ranks; the whole-step timing when given, else the sum of the stages),
+    whole-job value, per-stage rates and the dominant kernel's roofline."""
+    step_ms = max_over_ranks(float(st_ms.sum(axis=1).mean()) if whole_ms is None else float(whole_ms.mean()), world)
     mean_ms = st_ms.mean(axis=0)
     breakdown = {}
     for (name, _, amount, kind), ms in zip(c.stages, mean_ms):
@@ -482,11 +506,16 @@ def run_ours(args, rank, world, local_rank):
     torch.cuda.set_device(dev)
     c = prepare(args, args.workload, dev)
     p = c.w.pool
-    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    flush = L2Flush(torch, dev)
     stream = torch.cuda.current_stream(dev)
     peaks = measured_peaks()
-    st_ms, clocks, t_wall = time_steps(c, args.steps, args.warmup, world, local_rank, flush, stream)
-    step_ms, value, breakdown, roof = summarize(c, st_ms, world, peaks, args.traffic)
+    # the timed region: whole steps (one event pair per step); then, for a step of several
+    # launches, a second pass with an event between every two launches for the per-kernel times
+    whole, clocks, t_wall = time_steps(c, args.steps, args.warmup, world, local_rank, flush, stream, per_stage=False)
+    st_ms = whole
+    if len(c.stages) > 1:
+        st_ms, _, _ = time_steps(c, args.steps, args.warmup, world, local_rank, flush, stream, per_stage=True)
+    step_ms, value, breakdown, roof = summarize(c, st_ms, world, peaks, args.traffic, whole_ms=whole[:, 0])
 
     # end to end through the C ABI with host buffers: inputs up, result down, every step
     h_in = [(t, t.cpu().pin_memory()) for t in c.h_dev]
@@ -506,7 +535,7 @@ def run_ours(args, rank, world, local_rank):
     torch.cuda.synchronize()
     e2e_ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
     for i in range(args.steps):
-        flush.zero_()
+        flush()
         e2e_ev[i][0].record(stream)
         e2e_step()
         e2e_ev[i][1].record(stream)
@@ -525,7 +554,7 @@ def run_ours(args, rank, world, local_rank):
         torch.cuda.synchronize()
         g_ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
         for i in range(args.steps):
-            flush.zero_()
+            flush()
             g_ev[i][0].record(stream)
             g.replay()
             g_ev[i][1].record(stream)
@@ -552,6 +581,8 @@ def run_ours(args, rank, world, local_rank):
         "config": workload_config(c.w, c.k, wl, world),
         "decode_path": c.decode_path,
         "breakdown": breakdown,
+        "breakdown_method": ("value: events around whole steps; breakdown and roofline: a second pass of the same "
+                             "steps with an event between every two launches"),
         "step_bytes": c.step_bytes,
         "roofline": roof,
         "e2e": {
@@ -580,8 +611,11 @@ def run_ours(args, rank, world, local_rank):
         for name in ALL_CONFIGS:
             torch.cuda.empty_cache()
             c2 = prepare(extra, name, dev)
-            st2, clk2, _ = time_steps(c2, args.steps, args.warmup, world, local_rank, flush, stream)
-            ms2, val2, br2, roof2 = summarize(c2, st2, world, peaks)
+            wh2, clk2, _ = time_steps(c2, args.steps, args.warmup, world, local_rank, flush, stream, per_stage=False)
+            st2 = wh2
+            if len(c2.stages) > 1:
+                st2, _, _ = time_steps(c2, args.steps, args.warmup, world, local_rank, flush, stream, per_stage=True)
+            ms2, val2, br2, roof2 = summarize(c2, st2, world, peaks, whole_ms=wh2[:, 0])
             res["workloads"][name] = {
                 "config": workload_config(c2.w, c2.k, wl, world), "decode_path": c2.decode_path,
                 "us_per_step": round(ms2 * 1e3, 2), "value": round(val2, 2), "unit": "GB/s",
