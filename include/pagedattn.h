@@ -133,7 +133,10 @@ int pa_rope_reshape_and_cache(void* q, const void* key, const void* value, void*
  *   m [num_seqs, n_q_heads, P] float  -- per-piece max of scale*q.K (natural-log units)
  *   l [num_seqs, n_q_heads, P] float  -- per-piece sum of exp(s - m)
  *   o [num_seqs, n_q_heads, P, head_dim] float -- per-piece normalised output
- * The caller owns it; its contents between calls are unspecified.
+ *   256 bytes of control: the counter from which the split-K grid's CTAs take their pieces; a
+ *       call that splits at group size 1 or 2 zeroes it first with a 4-byte cudaMemsetAsync on
+ *       its stream
+ * The caller owns it; its contents between calls are unspecified (nothing needs to start at zero).
  */
 size_t pa_decode_workspace_size(int num_seqs, int n_q_heads, int head_dim, int max_context_len,
                                 int partition_tokens);
@@ -198,10 +201,11 @@ int pa_decode_v1(void* out, const void* q, const void* k_cache, const void* v_ca
 /*
  * pa_decode_splitk -- split-K decode (mini_engine, "Custom CUDA kernels", v2):
  * the context is cut into pieces of partition_tokens tokens (a multiple of
- * block_size and of 16; <= 0 means 256) processed by separate CTAs, each writing its max,
- * exp-sum and normalised output to the workspace; a reduce kernel merges them
- * with weights l_p * exp(m_p - max m).  Sequences with one piece are written
- * directly.  Arguments as pa_decode.
+ * block_size and of 16; <= 0 means 256), each piece's max, exp-sum and normalised output
+ * written to the workspace; a reduce kernel merges them with weights l_p * exp(m_p - max m).
+ * Sequences with one piece are written directly.  When some sequence has several pieces, one
+ * CTA per resident slot takes pieces, highest piece index first, from a counter in the
+ * workspace (so that the SMs that stream faster take more of them).  Arguments as pa_decode.
  */
 int pa_decode_splitk(void* out, const void* q, const void* k_cache, const void* v_cache,
                      const int32_t* block_tables, int max_blocks_per_seq, const int32_t* context_lens,

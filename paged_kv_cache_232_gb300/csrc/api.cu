@@ -106,16 +106,18 @@ int partition_or_default(int part) { return part > 0 ? part : PA_DEFAULT_PARTITI
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 struct WsLayout {
-    size_t m_off, l_off, o_off, total;
+    size_t m_off, l_off, o_off, ctl_off, total;
 };
 
+// m, l, o regions, then a 256-byte control region (the dynamic grid's piece counter)
 WsLayout ws_layout(int num_seqs, int n_q_heads, int head_dim, int max_parts) {
     const size_t rows = (size_t)num_seqs * n_q_heads * max_parts;
     WsLayout w;
     w.m_off = 0;
     w.l_off = align256(rows * sizeof(float));
     w.o_off = w.l_off + align256(rows * sizeof(float));
-    w.total = w.o_off + align256(rows * head_dim * sizeof(float));
+    w.ctl_off = w.o_off + align256(rows * head_dim * sizeof(float));
+    w.total = w.ctl_off + 256;
     return w;
 }
 
@@ -193,11 +195,28 @@ int decode_impl(void* out, const void* q, const void* k_cache, const void* v_cac
             p.ws_m = reinterpret_cast<float*>(base + w.m_off);
             p.ws_l = reinterpret_cast<float*>(base + w.l_off);
             p.ws_o = reinterpret_cast<float*>(base + w.o_off);
+            p.dyn_counter = reinterpret_cast<int*>(base + w.ctl_off);
             reduce = true;
         }
         p.part_tokens = part_tokens;
         p.max_parts = max_parts;
         grid = units * max_parts;
+        if (reduce && n_q_heads / n_kv_heads <= 2) {
+            // the dynamic grid: one CTA per resident slot taking pieces from the counter (zeroed
+            // here, in the stream, before the launch), when there are more pieces than slots;
+            // with fewer it would run the static grid's CTAs plus the zeroing.  Group sizes 1 and
+            // 2 only: at 4 its piece loop spills registers and the static grid is faster (GB300,
+            // 4 sequences of 32K tokens at 32 q / 8 KV heads: 113.7 against 105.5 us)
+            const int resident = pa::decode_dyn_resident_ctas(dtype == PA_BF16, kernel_dim(head_dim),
+                                                              n_q_heads / n_kv_heads);
+            if (resident <= 0) return PA_ERR_CUDA;
+            const int64_t slots = (int64_t)dev->sm_count * resident;
+            if ((int64_t)grid > slots) {
+                p.dyn = 1;
+                grid = (int)slots;
+                if (cudaMemsetAsync(p.dyn_counter, 0, sizeof(int), stream) != cudaSuccess) return PA_ERR_CUDA;
+            }
+        }
     } else {
         p.part_tokens = 0;
         p.max_parts = 1;
@@ -238,7 +257,8 @@ int decode_impl(void* out, const void* q, const void* k_cache, const void* v_cac
 // 3 % and 2.25 waves of 1024 by 10 %), and the plan takes the fewest pieces whose cost is
 // within 2 % of the best.  Pieces are at least 256 tokens, so a workspace sized for the
 // default piece fits every plan.
-int plan(int64_t units, int max_context_len, int sm_count, int resident, int block_size, int* part_tokens) {
+int plan(int64_t units, int max_context_len, int sm_count, int resident, int block_size, int group,
+         int* part_tokens) {
     const int min_piece = PA_DEFAULT_PARTITION_TOKENS;
     if (part_tokens) *part_tokens = min_piece;
     if (max_context_len <= min_piece) return 1;
@@ -250,7 +270,11 @@ int plan(int64_t units, int max_context_len, int sm_count, int resident, int blo
         // streaming alone; quarter-context pieces keep every SM busy to the end (GB300, 64
         // sequences of 100..2048 tokens: 62.2 us against 65.0 one-pass)
         if (units >= 2 * slots || max_context_len < 1024) return 1;
-        const int64_t piece = std::max<int64_t>(min_piece, ((L + 3) / 4 + align - 1) / align * align);
+        int64_t piece = std::max<int64_t>(min_piece, ((L + 3) / 4 + align - 1) / align * align);
+        // at group size 1 or 2 the split-K grid is dynamic (CTAs take pieces as they free up):
+        // there pieces of at most 512 tokens balance best (GB300, 64 sequences of 100..4096 /
+        // 100..8192 tokens: 97.3 / 179.2 us at 512 against 103.4 / 197.6 at a quarter context)
+        if (group <= 2) piece = std::min<int64_t>(piece, 512);
         if (part_tokens) *part_tokens = (int)piece;
         return 2;
     }
@@ -421,7 +445,7 @@ int pa_decode_plan(int num_seqs, int n_q_heads, int n_kv_heads, int head_dim, in
     const int resident = pa::decode_resident_ctas(dtype == PA_BF16, kernel_dim(head_dim), n_q_heads / n_kv_heads);
     if (resident <= 0) return PA_ERR_CUDA;
     return plan((int64_t)num_seqs * n_kv_heads, max_context_len, dev->sm_count, resident, block_size,
-                partition_tokens);
+                n_q_heads / n_kv_heads, partition_tokens);
 }
 
 int pa_decode_v1(void* out, const void* q, const void* k_cache, const void* v_cache, const int32_t* block_tables,
@@ -612,7 +636,7 @@ int pa_decode_shared_prefix(void* out, const void* q, const void* k_cache, const
     if (resident <= 0) return PA_ERR_CUDA;
     int part = 0;
     const int which = plan((int64_t)num_seqs * n_kv_heads, max_context_len - P, dev->sm_count, resident, block_size,
-                           &part);
+                           G, &part);
     const PrefixPartials pin{P, kp, pf_m, pf_l, pf_o};
     void* ws2 = base + pw.total;
     const size_t ws2_bytes = workspace_bytes - pw.total;

@@ -41,7 +41,18 @@ static cudaError_t launch_decode_t(const DecodeParams& p, const CUtensorMap& tmK
     auto launch = [&](auto kern, int smem) -> cudaError_t {
         return launch_dependent(kern, (unsigned)grid, C::THREADS, (size_t)smem, st, p, tmK, tmV);
     };
-    if (p.persist) {
+    if (p.dyn) {
+        // group sizes 1 and 2 only (at 4 the piece loop spills and the static grid is faster)
+        if constexpr (G <= 2) {
+            auto kern = decode_kernel_dyn<D, G, BF16>;
+            static std::atomic<unsigned long long> s_dyn{0};
+            e = smem_limit_once(reinterpret_cast<const void*>(kern), C::P_SMEM_BYTES, s_dyn);
+            if (e != cudaSuccess) return e;
+            e = launch(kern, C::P_SMEM_BYTES);
+        } else {
+            return cudaErrorInvalidValue;
+        }
+    } else if (p.persist) {
         // group sizes 1 and 2 only: larger groups run out of registers in the unit loop
         if constexpr (G <= 2) {
             auto kern = decode_kernel_persistent<D, G, BF16>;
@@ -97,6 +108,40 @@ static int resident_by_group(int group) {
             return 0;
         default: return 0;
     }
+}
+
+// CTAs of the dynamic split-K kernel resident per SM (0 on a CUDA error), queried once per device.
+template <int D, int G, bool BF16>
+static int dyn_resident_t() {
+    static std::atomic<int> cache[64];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    int r = cache[dev & 63].load(std::memory_order_acquire);
+    if (r > 0) return r;
+    using C = DecodeCfg<D, G, BF16>;
+    auto kern = decode_kernel_dyn<D, G, BF16>;
+    static std::atomic<unsigned long long> s_dyn_q{0};
+    if (smem_limit_once(reinterpret_cast<const void*>(kern), C::P_SMEM_BYTES, s_dyn_q) != cudaSuccess) return 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&r, kern, C::THREADS, C::P_SMEM_BYTES) != cudaSuccess || r < 1)
+        return 0;
+    cache[dev & 63].store(r, std::memory_order_release);
+    return r;
+}
+
+template <int D, bool BF16>
+static int dyn_resident_by_group(int group) {
+    switch (group) {
+        case 1: return dyn_resident_t<D, 1, BF16>();
+        case 2: return dyn_resident_t<D, 2, BF16>();
+        default: return 0;  // the dynamic grid runs group sizes 1 and 2 only
+    }
+}
+
+int decode_dyn_resident_ctas(int bf16, int head_dim, int group) {
+    if (head_dim == 256) return bf16 ? dyn_resident_by_group<256, true>(group) : dyn_resident_by_group<256, false>(group);
+    if (head_dim == 128) return bf16 ? dyn_resident_by_group<128, true>(group) : dyn_resident_by_group<128, false>(group);
+    if (head_dim == 64) return bf16 ? dyn_resident_by_group<64, true>(group) : dyn_resident_by_group<64, false>(group);
+    return 0;
 }
 
 int decode_resident_ctas(int bf16, int head_dim, int group) {

@@ -59,6 +59,8 @@ struct DecodeParams {
     // griddepcontrol.wait (they are launched as programmatic dependents of that pass).
     int prefix_tokens;
     int pf_parts;              // 0: no shared prefix
+    int dyn;                   // split-K only: decode_kernel_dyn, gridDim.x CTAs taking pieces from *dyn_counter
+    int* dyn_counter;          // the next piece to hand out (zeroed before the launch)
     const float* pf_m;         // [S * Hq][pf_parts]
     const float* pf_l;
     const float* pf_o;         // [S * Hq][pf_parts][D]
@@ -965,6 +967,322 @@ decode_kernel_persistent(const DecodeParams p, const __grid_constant__ CUtensorM
         // the merge area is rewritten by the next unit; every warp has seen the abort flag
         asm volatile("bar.sync 1, %0;" ::"n"(C::NCW * 32) : "memory");
         if (*abort_flag) break;
+    }
+    // the producer has seen every load land (barrier 2 counts it too)
+    asm volatile("bar.sync 2, %0;" ::"n"(C::THREADS) : "memory");
+}
+
+// The dynamic split-K grid (p.dyn): gridDim.x CTAs, one per resident slot, take work items --
+// the split-K pieces, highest piece index first as in decode_kernel's grid -- from a counter the
+// launcher zeroes.  The producer warp fetches an item, publishes it through a small queue in
+// shared memory and streams its chunks into the ring, the next item's while the consumers merge
+// this one; the SMs that stream faster take more pieces, so the grid ends evenly, and no CTA pays
+// its start-up more than once.  Each item starts on a ring index that is a multiple of the
+// consumer-warp count, so consumer warp w always takes the item's chunks w, w + NCW, ... (the
+// order of accumulation does not depend on which items a CTA took) and every ring stage keeps one
+// owning warp; both sides count each stage's uses for the barrier parities, as the skipped ring
+// indices never touch a stage.  The per-chunk work is decode_kernel's.
+template <int D, int G, bool BF16>
+__global__ void __launch_bounds__(DecodeCfg<D, G, BF16>::THREADS,
+                                  D == 256 ? (G <= 2 ? 2 : 1) : ((G <= 4) ? 3 : (D == 64 ? 2 : 1)))
+decode_kernel_dyn(const DecodeParams p, const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV) {
+    using C = DecodeCfg<D, G, BF16>;
+    using F = F16x2<BF16>;
+    constexpr int NQS = 4;  // item queue slots
+    static_assert(2 * NQS * 8 + NQS * 8 * 4 <= C::LIST_MAX * 3 * 4, "item queue area");
+    static_assert(C::NST <= 32, "stage bit masks");
+    extern __shared__ __align__(1024) unsigned char smem_raw[];
+    // 1024-byte alignment for the 128-byte swizzle pattern of TMA
+    unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const uint32_t ring = smem_addr(smem);
+    float* p_buf = reinterpret_cast<float*>(smem + C::RING_BYTES);
+    float* a_buf = reinterpret_cast<float*>(smem + C::RING_BYTES + C::P_BYTES);
+    const uint32_t bar_full = ring + C::P_BAR_OFF;
+    const uint32_t bar_empty = bar_full + C::NST * 8;
+    const uint32_t bar_qfull = ring + C::P_LIST_OFF;   // [NQS] an item (or the end) published
+    const uint32_t bar_qempty = bar_qfull + NQS * 8;   // [NQS] the consumers are done with the slot
+    volatile int* qslot = reinterpret_cast<volatile int*>(smem + C::P_LIST_OFF + 2 * NQS * 8);  // [NQS][8]
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    // launched as a programmatic dependent of whatever kernel precedes it in the stream: nothing is
+    // read before that kernel has completed; after a shared-prefix pass only the merge waits
+    if (p.pf_parts == 0) asm volatile("griddepcontrol.wait;" ::: "memory");
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < C::NST; ++i) {
+            mbar_init(bar_full + 8 * i, 1);
+            mbar_init(bar_empty + 8 * i, 1);
+        }
+        for (int k = 0; k < NQS; ++k) {
+            mbar_init(bar_qfull + 8 * k, 1);
+            mbar_init(bar_qempty + 8 * k, 1);
+        }
+        fence_barrier_init();
+    }
+    __syncthreads();
+
+    const int units = p.num_seqs * p.n_kv_heads;
+    const long long total = (long long)units * p.max_parts;
+    int cap = table_row_tokens(p.max_blocks_per_seq, p.cpb_log2);
+    if (p.prefix_tokens + p.max_parts * p.part_tokens < cap) cap = p.prefix_tokens + p.max_parts * p.part_tokens;
+
+    if (warp == C::NCW) {
+        // ------------------------------------------------------------ producer warp
+        if (lane == 0) {
+            tma_prefetch_desc(&tmK);
+            tma_prefetch_desc(&tmV);
+        }
+        const uint64_t pol = l2_policy_evict_first();
+        const bool half8 = p.cpb_log2 < 0;
+        const int per_load = half8 ? 16 : 32;  // chunks whose table entries one warp-wide load covers
+        uint32_t fused = 0, fpar = 0;          // per stage: filled before; parity of its fill count
+        int ring_next = 0, nq = 0;             // ring index of the next chunk; items published
+        bool ok = true;
+        while (ok) {
+            int item = 0;
+            if (lane == 0) item = atomicAdd(p.dyn_counter, 1);
+            item = __shfl_sync(0xffffffffu, item, 0);
+            const bool end = (long long)item >= total;
+            int s = -1, g = 0, piece = 0, t_begin = 0, t_end = 0, n_parts = 0;
+            if (!end) {
+                const int qpos = item / units, sg = item - qpos * units;
+                piece = (p.max_parts - 1) - qpos;
+                s = sg / p.n_kv_heads;
+                g = sg - s * p.n_kv_heads;
+                int L = __ldg(p.context_lens + s);
+                if (L < 0 || L > cap) {
+                    if (piece == 0 && g == 0 && lane == 0) flag_error(p.err, PA_DEVERR_LENGTH);
+                    L = L < 0 ? 0 : cap;
+                }
+                const int base = min(L, p.prefix_tokens);
+                t_begin = min(L, base + piece * p.part_tokens);
+                t_end = min(L, t_begin + p.part_tokens);
+                n_parts = (L - base + p.part_tokens - 1) / p.part_tokens;
+                if (t_begin >= t_end && piece > 0) continue;  // a piece past this sequence's context
+            }
+            const int nblk = end ? 0 : (t_end - t_begin + C::BS - 1) / C::BS;
+            const int r0 = (ring_next + C::NCW - 1) / C::NCW * C::NCW;
+            const int k = nq % NQS;
+            if (lane == 0) {
+                if (nq >= NQS) ok = mbar_wait(bar_qempty + 8 * k, ((nq / NQS) - 1) & 1, p.err);
+                if (ok) {
+                    volatile int* q = qslot + 8 * k;
+                    q[0] = end ? -1 : s;
+                    q[1] = g;
+                    q[2] = piece;
+                    q[3] = t_begin;
+                    q[4] = t_end;
+                    q[5] = n_parts;
+                    q[6] = r0;
+                    mbar_arrive(bar_qfull + 8 * k);
+                }
+            }
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+            ++nq;
+            if (end || !ok) break;
+            // the item's chunks into ring indices r0 .. r0 + nblk - 1; 16-token chunk c of the
+            // sequence: table entry c >> cpb_log2, rows 16 (c mod 2^cpb_log2) + 0..15 (blocks of 8:
+            // entries 2c and 2c + 1, the second only if the context reaches it)
+            const int blk0 = t_begin / C::BS;
+            const int32_t* bt = p.block_tables + (size_t)s * p.max_blocks_per_seq;
+            for (int b0 = 0; b0 < nblk && ok; b0 += per_load) {
+                const int nb = min(per_load, nblk - b0);
+                int my = p.num_blocks;  // outside the tensor map: TMA fills zeros
+                const int e = half8 ? 2 * (blk0 + b0) + lane : (blk0 + b0 + lane) >> p.cpb_log2;
+                if (half8 ? (lane < 2 * nb && 8 * e < t_end) : (lane < nb)) {
+                    my = __ldg(bt + e);
+                    if (my < 0 || my >= p.num_blocks) {
+                        flag_error(p.err, PA_DEVERR_BLOCK);
+                        my = p.num_blocks;
+                    }
+                }
+                for (int j = 0; j < nb; ++j) {
+                    const int blk = __shfl_sync(0xffffffffu, my, half8 ? 2 * j : j);
+                    const int blk_b = __shfl_sync(0xffffffffu, my, (2 * j + 1) & 31);  // half8 only
+                    const int st = (r0 + b0 + j) % C::NST;
+                    if (lane == 0) {
+                        const int row0 = half8 ? 0 : ((blk0 + b0 + j) & ((1 << p.cpb_log2) - 1)) * C::BS;
+                        if ((fused >> st) & 1) ok = mbar_wait(bar_empty + 8 * st, ((fpar >> st) & 1) ^ 1, p.err);
+                        if (ok) {
+                            const uint32_t dst = ring + st * C::STAGE_BYTES;
+                            mbar_arrive_expect_tx(bar_full + 8 * st, C::STAGE_BYTES);
+#pragma unroll
+                            for (int kv = 0; kv < 2; ++kv) {
+                                const CUtensorMap* map = kv ? &tmV : &tmK;
+                                const uint32_t tile = dst + kv * C::TILE_BYTES;
+#pragma unroll
+                                for (int hf = 0; hf < C::HALVES; ++hf) {
+                                    tma_load_4d(tile + hf * C::SLAB_BYTES, map, hf * 64, g, row0, blk, bar_full + 8 * st, pol);
+                                    if (half8)
+                                        tma_load_4d(tile + hf * C::SLAB_BYTES + 8 * 128, map, hf * 64, g, 0, blk_b,
+                                                    bar_full + 8 * st, pol);
+                                }
+                            }
+                        }
+                    }
+                    ok = __shfl_sync(0xffffffffu, ok, 0);
+                    if (!ok) break;
+                    fused |= 1u << st;
+                    fpar ^= 1u << st;
+                }
+            }
+            ring_next = r0 + nblk;
+        }
+        // No load may still be landing when the CTA exits (after a time-out the consumers may not
+        // have taken every stage): wait, with the time limit, for the last fill of every stage.
+        if (lane == 0) {
+            for (int st = 0; st < C::NST; ++st)
+                if ((fused >> st) & 1) (void)mbar_wait(bar_full + 8 * st, ((fpar >> st) & 1) ^ 1, p.err);
+        }
+        __syncwarp();
+        asm volatile("bar.arrive 2, %0;" ::"n"(C::THREADS) : "memory");
+        return;
+    }
+
+    // ---------------------------------------------------------------- consumer warps
+    const int tg = lane >> 3, dl = lane & 7;  // q.K layout: token group, lane within token
+    int chunk_col[C::CPL];
+#pragma unroll
+    for (int j = 0; j < C::CPL; ++j) {
+        const int half = (C::HALVES == 4) ? j : (C::HALVES == 2) ? (dl >> 2) : 0;
+        const int c = (C::HALVES == 2) ? ((2 * (dl & 3) + half + j) & 7) : dl;
+        chunk_col[j] = half * 64 + c * 8;
+    }
+    const int n0 = 4 * G;
+    int my_h;
+    {
+        int base = ((lane & 4) ? n0 / 2 : 0) + ((lane & 2) ? n0 / 4 : 0) + ((n0 >= 8 && (lane & 1)) ? n0 / 8 : 0);
+        my_h = base / 4;
+    }
+    const int hmask = (G == 1) ? 0 : (G == 2) ? 4 : (G == 4) ? 6 : 7;
+    const bool rep = (tg == 0) && ((dl & ~hmask) == 0);
+    const int dg = lane % C::CR, tgp = lane / C::CR;  // P.V layout
+    float* pw = p_buf + warp * C::BS * G;
+    float* aw = a_buf + warp * 8;
+    float* mo = reinterpret_cast<float*>(smem + C::P_MERGE_OFF);  // [NCW][G][D]
+    float* mm = mo + C::NCW * G * D;                             // [NCW][G]
+    float* ml = mm + C::NCW * G;                                 // [NCW][G]
+
+    // [0] the slot arrived, [1] abort: decisions every consumer warp takes together, so that all
+    // of them meet the named merge barrier the same number of times
+    volatile int* flags = reinterpret_cast<volatile int*>(smem + C::P_FLAG_OFF);
+    if (threadIdx.x == 0) flags[1] = 0;
+    uint32_t cpar = 0;  // per stage this warp owns: parity of its consume count
+    bool ok = true, waited = false;
+    for (int nq = 0;; ++nq) {
+        const int k = nq % NQS;
+        if (threadIdx.x == 0) flags[0] = mbar_wait(bar_qfull + 8 * k, (nq / NQS) & 1, p.err) ? 1 : 0;
+        asm volatile("bar.sync 1, %0;" ::"n"(C::NCW * 32) : "memory");
+        if (!flags[0]) break;  // the producer stopped (a wait gave up)
+        const volatile int* q = qslot + 8 * k;
+        const int s = q[0];
+        if (s < 0) break;  // no more items
+        const int g = q[1], piece = q[2], t_begin = q[3], t_end = q[4], n_parts = q[5], r0 = q[6];
+        const bool direct = n_parts <= 1;
+        float qf[G][C::CPL][8];
+        {
+            const uint16_t* qrow = static_cast<const uint16_t*>(p.q) + ((size_t)s * p.n_q_heads + (size_t)g * G) * p.hd;
+#pragma unroll
+            for (int h = 0; h < G; ++h)
+#pragma unroll
+                for (int j = 0; j < C::CPL; ++j) {
+                    uint4 raw = chunk_col[j] < p.hd ? ldg_nc_128(qrow + h * p.hd + chunk_col[j]) : make_uint4(0u, 0u, 0u, 0u);
+                    unpack8<BF16>(raw, qf[h][j]);
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) qf[h][j][e] *= p.qk_scale_log2;
+                }
+        }
+        float m_run = -INFINITY, l_run = 0.f;
+        float o[G][8];
+#pragma unroll
+        for (int h = 0; h < G; ++h)
+#pragma unroll
+            for (int e = 0; e < 8; ++e) o[h][e] = 0.f;
+        const int nblk = (t_end - t_begin + C::BS - 1) / C::BS;
+        // r0 is a multiple of NCW: this warp's chunks b = warp, warp + NCW, ... sit at ring indices
+        // r0 + b, all in stages it owns
+        for (int b = warp; ok && b < nblk; b += C::NCW) {
+            const int st = (r0 + b) % C::NST;
+            const bool arrived = mbar_wait(bar_full + 8 * st, (cpar >> st) & 1, p.err);
+            if (!__all_sync(0xffffffffu, arrived)) { ok = false; break; }
+            const uint32_t kt = ring + st * C::STAGE_BYTES;
+            const int nvalid = min(C::BS, t_end - (t_begin + b * C::BS));
+            consume_chunk<D, G, BF16>(kt, nvalid, qf, chunk_col, lane, my_h, rep, pw, aw, m_run, l_run, o);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar_empty + 8 * st);
+            cpar ^= 1u << st;
+        }
+        // fold the token groups of the P.V layout
+#pragma unroll
+        for (int h = 0; h < G; ++h)
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                float x = o[h][e];
+                if constexpr (C::TGP >= 2) x += __shfl_xor_sync(0xffffffffu, x, C::CR);
+                if constexpr (C::TGP >= 4) x += __shfl_xor_sync(0xffffffffu, x, 2 * C::CR);
+                o[h][e] = x;
+            }
+        if (!ok) {
+            m_run = -INFINITY;
+            l_run = 0.f;
+            if (lane == 0) flags[1] = 1;  // every consumer warp stops after this item
+        }
+        if (tgp == 0) {
+#pragma unroll
+            for (int h = 0; h < G; ++h) {
+                float4* dst = reinterpret_cast<float4*>(mo + (warp * G + h) * D + dg * 8);
+                dst[0] = make_float4(o[h][0], o[h][1], o[h][2], o[h][3]);
+                dst[1] = make_float4(o[h][4], o[h][5], o[h][6], o[h][7]);
+            }
+        }
+        if (rep) {
+            mm[warp * G + my_h] = m_run;
+            ml[warp * G + my_h] = l_run;
+        }
+        asm volatile("bar.sync 1, %0;" ::"n"(C::NCW * 32) : "memory");
+        // the shared-prefix partials are complete and visible past this point
+        if (p.pf_parts > 0 && !waited) {
+            asm volatile("griddepcontrol.wait;" ::: "memory");
+            waited = true;
+        }
+        const int tid = threadIdx.x;  // 0 .. 127
+        const int hq0 = g * G;
+        for (int idx = 2 * tid; idx < G * D; idx += 2 * C::NCW * 32) {
+            const int h = idx / D, d = idx - h * D;
+            const size_t row = (size_t)s * p.n_q_heads + hq0 + h;
+            const bool fold = direct && p.pf_parts > 0;
+            float M = -INFINITY;
+#pragma unroll
+            for (int w = 0; w < C::NCW; ++w) M = fmaxf(M, mm[w * G + h]);
+            if (fold) M = prefix_max(p, row, M);
+            float Lsum = 0.f, o0 = 0.f, o1 = 0.f;
+            if (M != -INFINITY) {
+#pragma unroll
+                for (int w = 0; w < C::NCW; ++w) {
+                    const float wt = ex2(mm[w * G + h] - M);
+                    Lsum = fmaf(ml[w * G + h], wt, Lsum);
+                    o0 = fmaf(mo[(w * G + h) * D + d], wt, o0);
+                    o1 = fmaf(mo[(w * G + h) * D + d + 1], wt, o1);
+                }
+                if (fold) prefix_add(p, row, d, D, M, Lsum, o0, o1);
+            }
+            const float inv = (Lsum > 0.f) ? 1.f / Lsum : 0.f;
+            if (direct) {
+                if (d < p.hd)
+                    *reinterpret_cast<uint32_t*>(static_cast<uint16_t*>(p.out) + row * p.hd + d) = F::pack_rn(o0 * inv, o1 * inv);
+            } else {
+                const size_t pr = row * p.max_parts + piece;
+                *reinterpret_cast<float2*>(p.ws_o + pr * D + d) = make_float2(o0 * inv, o1 * inv);
+                if (d == 0) {
+                    p.ws_m[pr] = M * 0.69314718055994531f;  // back to natural-log units
+                    p.ws_l[pr] = Lsum;
+                }
+            }
+        }
+        // the merge area and the queue slot are reused by the next item; every warp has seen the
+        // abort flag
+        asm volatile("bar.sync 1, %0;" ::"n"(C::NCW * 32) : "memory");
+        if (threadIdx.x == 0) mbar_arrive(bar_qempty + 8 * k);
+        if (flags[1]) break;
     }
     // the producer has seen every load land (barrier 2 counts it too)
     asm volatile("bar.sync 2, %0;" ::"n"(C::THREADS) : "memory");

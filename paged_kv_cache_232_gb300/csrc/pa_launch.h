@@ -61,6 +61,8 @@ inline int decode_list_max() { return DecodeCfg<128, 1, true>::LIST_MAX; }
 // CTAs of the decode kernel for (dtype, head_dim, group) that fit on one SM (0 on a CUDA error);
 // queried once per device, so a call inside a stream capture makes no CUDA call.
 int decode_resident_ctas(int bf16, int head_dim, int group);
+// The same for the dynamic split-K kernel (decode_kernel_dyn).
+int decode_dyn_resident_ctas(int bf16, int head_dim, int group);
 
 cudaError_t launch_decode(int bf16, int head_dim, int group, const DecodeParams& params, const CUtensorMap& tmK,
                           const CUtensorMap& tmV, int grid, bool with_reduce, cudaStream_t stream);

@@ -39,10 +39,11 @@ def test_host_only_calls(lib):
     assert pa.version() >= 100
     assert pa.status_string(0) == "ok"
     assert pa.status_string(-7).startswith("split-K workspace")
-    # one piece needs no workspace; several pieces need m, l (256-byte aligned) and o
+    # one piece needs no workspace; several pieces need m, l (256-byte aligned), o and a 256-byte
+    # control region (the dynamic grid's piece counter)
     assert pa.pa_decode_workspace_size(4, 32, 128, 256) == 0
     rows = 4 * 32 * 128
-    expect = 2 * ((rows * 4 + 255) // 256 * 256) + (rows * 128 * 4 + 255) // 256 * 256
+    expect = 2 * ((rows * 4 + 255) // 256 * 256) + (rows * 128 * 4 + 255) // 256 * 256 + 256
     assert pa.pa_decode_workspace_size(4, 32, 128, 32768) == expect
 
 
@@ -111,11 +112,11 @@ def test_shared_prefix_sizes_and_validation(lib):
     assert ws(4, 32, 128, 32768, 0) == pa.pa_decode_workspace_size(4, 32, 128, 32768)
     assert ws(4, 32, 128, 32768, 15) == pa.pa_decode_workspace_size(4, 32, 128, 32768)
     rows = 128 * 16 * (1024 // 128)
-    pf = 2 * ((rows * 4 + 255) // 256 * 256) + (rows * 128 * 4 + 255) // 256 * 256
+    pf = 2 * ((rows * 4 + 255) // 256 * 256) + (rows * 128 * 4 + 255) // 256 * 256 + 256
     assert ws(128, 16, 128, 2048, 1024) == pf + pa.pa_decode_workspace_size(128, 16, 128, 2048 - 1024)
     # only whole 16-token chunks within the longest context are shared
     rows = 2 * 8 * 2
-    pf = 2 * ((rows * 4 + 255) // 256 * 256) + (rows * 64 * 4 + 255) // 256 * 256
+    pf = 2 * ((rows * 4 + 255) // 256 * 256) + (rows * 64 * 4 + 255) // 256 * 256 + 256
     assert ws(2, 8, 64, 200, 1000) == pf + pa.pa_decode_workspace_size(2, 8, 64, 200 - 192)
     vp = ctypes.c_void_p(16)   # never dereferenced: validation fails first
     call = lambda prefix, piece=0, maxL=100: lib.pa_decode_shared_prefix(

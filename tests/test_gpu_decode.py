@@ -267,6 +267,41 @@ def test_dispatcher_plan_pieces(S, hq, hkv, d, bs, L):
     assert pa.pa_decode_plan(256, 16, 8, 128, 16, 2048)[0] == 1       # one-pass: enough units, short contexts
 
 
+@pytest.mark.parametrize("dt,hq,hkv,d,bs", [(wl.BF16, 16, 8, 128, 16), (wl.F16, 8, 8, 64, 8), (wl.BF16, 4, 2, 256, 32),
+                                            (wl.F16, 16, 8, 96, 16)])
+def test_dynamic_split_grid(dt, hq, hkv, d, bs):
+    """Group size 1 or 2 with more split-K pieces than resident CTAs: one CTA per resident slot
+    takes pieces from a counter in the workspace, in whatever order the CTAs free up.  A piece's
+    arithmetic does not depend on which CTA takes it, so repeated calls agree bit for bit; the
+    counter is zeroed by the call (the workspace starts filled with 0x7f bytes); against the
+    oracle, with empty and one-token contexts among long ones."""
+    lens = wl.uniform_ints(wl.derive_seed(77, hq + d), 96, 1, 3000)
+    lens[[3, 40, 41]] = 0
+    lens[[10, 90]] = 1
+    lens[50] = 3000
+    w = wl.build_workload("dyn", 77 + hq + d + bs, dtype=dt, n_q_heads=hq, n_kv_heads=hkv, head_dim=d, block_size=bs,
+                          decode_lens=lens.tolist(), extra_blocks=3)
+    dev = Dev(w)
+    ref = oracle_decode(w)
+    S = w.decode.num_seqs
+    pa.pa_device_errors(clear=True)
+    for part in (256, 512):
+        ws = torch.full((max(16, pa.pa_decode_workspace_size(S, hq, d, dev.maxL, part)),), 0x7F, dtype=torch.uint8,
+                        device="cuda")
+        first = None
+        for _ in range(4):
+            out = torch.full_like(dev.q, float("nan"))
+            pa.pa_decode_splitk(out, dev.q, dev.kc, dev.vc, dev.bt, dev.cl, dev.maxL, dev.scale, ws, part)
+            torch.cuda.synchronize()
+            got = bits_of(out)
+            if first is None:
+                first = got
+                check(got, ref, dt, f"dynamic split grid {part}")
+            assert np.array_equal(got, first)
+    check(dev.run("auto"), ref, dt, "dispatcher")
+    assert pa.pa_device_errors(clear=True) == 0
+
+
 def test_long_context_planned_pieces_match_oracle():
     """The dispatcher's piece length for four 32K-token contexts (not a power of two) through
     pa_decode, against the oracle."""
