@@ -69,18 +69,12 @@ static cudaError_t launch_decode_t(const DecodeParams& p, const CUtensorMap& tmK
         e = launch(kern, C::SMEM_BYTES);
     }
     if (e != cudaSuccess || !with_reduce) return e;
-    const size_t red_smem = (size_t)(((p.max_parts + 3) & ~3) + ((p.pf_parts + 3) & ~3) + 8 * D) * sizeof(float);
-    auto rk = splitk_reduce_kernel<D, BF16>;
-    if (red_smem > 227 * 1024) return cudaErrorInvalidValue;
-    if (red_smem > 48 * 1024) {
-        // set once to the per-CTA maximum, so that no later (larger) piece count needs it again
-        static std::atomic<unsigned long long> s_red_done{0};
-        e = smem_limit_once(reinterpret_cast<const void*>(rk), 227 * 1024, s_red_done);
-        if (e != cudaSuccess) return e;
-    }
     // a programmatic dependent launch: the merge grid is set up while the piece kernel drains and
     // waits for it (griddepcontrol.wait) before reading the partials
-    return launch_dependent(rk, (unsigned)(p.num_seqs * p.n_q_heads), 256, red_smem, st, p);
+    const int rows = p.num_seqs * p.n_q_heads;
+    constexpr int per_cta = 8;  // rows (warps) per CTA
+    return launch_dependent(splitk_merge_kernel<D, BF16>, (unsigned)((rows + per_cta - 1) / per_cta), 32 * per_cta, 0,
+                            st, p);
 }
 
 template <int D, bool BF16>

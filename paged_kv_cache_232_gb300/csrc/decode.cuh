@@ -1288,17 +1288,45 @@ decode_kernel_dyn(const DecodeParams p, const __grid_constant__ CUtensorMap tmK,
     asm volatile("bar.sync 2, %0;" ::"n"(C::THREADS) : "memory");
 }
 
+// CW consecutive floats (16-byte aligned when CW >= 4, else 8-byte) into registers.
+template <int CW>
+__device__ __forceinline__ void load_cols(const float* x, float (&v)[CW]) {
+    if constexpr (CW % 4 == 0) {
+#pragma unroll
+        for (int c = 0; c < CW; c += 4) {
+            const float4 t = *reinterpret_cast<const float4*>(x + c);
+            v[c] = t.x;
+            v[c + 1] = t.y;
+            v[c + 2] = t.z;
+            v[c + 3] = t.w;
+        }
+    } else {
+#pragma unroll
+        for (int c = 0; c < CW; c += 2) {
+            const float2 t = *reinterpret_cast<const float2*>(x + c);
+            v[c] = t.x;
+            v[c + 1] = t.y;
+        }
+    }
+}
+
 // Split-K merge (mini_engine, "Custom CUDA kernels", v2 reduce): for each (s, h) with more
 // than one piece, M = max_p m_p, w_p = l_p exp(m_p - M), out = sum_p w_p o_p / sum_p w_p.
 // The shared-prefix partials (if any) take part as further pieces.
-// One CTA of 256 threads per (s, h): 8 warps take pieces round-robin, each lane 4 columns.
+// One warp per (s, h) row, no shared memory: lane i weighs
+// pieces i, i + 32, ... and holds D / 32 columns of every piece.  The first 2048 / D pieces'
+// columns are loaded before the weights are known, so that in the common case (up to 16 pieces
+// at head_dim 128) the merge after the piece kernel is one round trip to L2 for m, l and o
+// together, then the store.
 template <int D, bool BF16>
-__global__ void __launch_bounds__(256) splitk_reduce_kernel(const DecodeParams p) {
+__global__ void __launch_bounds__(256, 2) splitk_merge_kernel(const DecodeParams p) {
     using F = F16x2<BF16>;
-    // w[max_parts rounded up to 4] | prefix weights [pf_parts rounded up to 4] | acc[8][D]
-    extern __shared__ float4 red_smem4[];
-    float* red_smem = reinterpret_cast<float*>(red_smem4);
-    const int row = blockIdx.x;          // s * Hq + h
+    constexpr int CW = D / 32;  // columns per lane: 2, 4 or 8
+    constexpr int PRE = 64 / CW;  // pieces whose columns are loaded up front: 32, 16 or 8
+    constexpr float kLn2 = 0.69314718055994531f;  // the prefix partials' m is base 2
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int row = blockIdx.x * (blockDim.x >> 5) + warp;  // s * Hq + h
+    if (row >= p.num_seqs * p.n_q_heads) return;
     const int s = row / p.n_q_heads;
     int L = __ldg(p.context_lens + s);
     const int cap = min(table_row_tokens(p.max_blocks_per_seq, p.cpb_log2), p.prefix_tokens + p.max_parts * p.part_tokens);
@@ -1308,99 +1336,87 @@ __global__ void __launch_bounds__(256) splitk_reduce_kernel(const DecodeParams p
     // launched as a programmatic dependent of the piece kernel: its partials (and, through it, the
     // shared-prefix pass's) are complete and visible past this point
     asm volatile("griddepcontrol.wait;" ::: "memory");
-    float* wsh = red_smem;
-    float* wpf = red_smem + ((p.max_parts + 3) & ~3);
-    float* acc = wpf + ((p.pf_parts + 3) & ~3);  // 16-byte aligned for the float4 stores
-    const int KP = p.pf_parts;
-    constexpr float kLn2 = 0.69314718055994531f;  // the prefix partials' m is base 2
     const float* m = p.ws_m + (size_t)row * p.max_parts;
     const float* l = p.ws_l + (size_t)row * p.max_parts;
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    __shared__ float red[8];
-    __shared__ float Msh, Wsh;
+    const float* ob = p.ws_o + (size_t)row * p.max_parts * D + lane * CW;
+    const int KP = p.pf_parts;
 
-    float mx = -INFINITY;
-    for (int i = tid; i < n_parts; i += 256) mx = fmaxf(mx, m[i]);
-    for (int k = tid; k < KP; k += 256)
-        if (p.pf_l[(size_t)row * KP + k] > 0.f) mx = fmaxf(mx, p.pf_m[(size_t)row * KP + k] * kLn2);
+    float pre[PRE][CW];
 #pragma unroll
-    for (int o = 16; o; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-    if (lane == 0) red[warp] = mx;
-    __syncthreads();
-    if (tid == 0) {
-        float M = red[0];
-        for (int w = 1; w < 8; ++w) M = fmaxf(M, red[w]);
-        Msh = M;
-    }
-    __syncthreads();
-    const float M = Msh;
-    float wsum = 0.f;
-    for (int i = tid; i < n_parts; i += 256) {
-        const float w = (l[i] > 0.f) ? l[i] * __expf(m[i] - M) : 0.f;
-        wsh[i] = w;
-        wsum += w;
-    }
-    for (int k = tid; k < KP; k += 256) {
-        const float lk = p.pf_l[(size_t)row * KP + k];
-        const float w = (lk > 0.f) ? lk * __expf(p.pf_m[(size_t)row * KP + k] * kLn2 - M) : 0.f;
-        wpf[k] = w;
-        wsum += w;
-    }
+    for (int i = 0; i < PRE; ++i) {
+        if (i < n_parts) {
+            load_cols<CW>(ob + (size_t)i * D, pre[i]);
+        } else {
 #pragma unroll
-    for (int o = 16; o; o >>= 1) wsum += __shfl_xor_sync(0xffffffffu, wsum, o);
-    __syncthreads();
-    if (lane == 0) red[warp] = wsum;
-    __syncthreads();
-    if (tid == 0) {
-        float W = 0.f;
-        for (int w = 0; w < 8; ++w) W += red[w];
-        Wsh = W;
-    }
-    __syncthreads();
-
-    // each lane sums float4 columns lane * 4 + 128 k of the row's pieces (warp w: pieces w, w + 8, ...)
-    for (int c0 = lane * 4; c0 < D; c0 += 128) {
-        float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
-        const float* ob = p.ws_o + (size_t)row * p.max_parts * D + c0;
-        int i = warp;
-        for (; i + 24 < n_parts; i += 32) {
-            float4 x0 = *reinterpret_cast<const float4*>(ob + (size_t)i * D);
-            float4 x1 = *reinterpret_cast<const float4*>(ob + (size_t)(i + 8) * D);
-            float4 x2 = *reinterpret_cast<const float4*>(ob + (size_t)(i + 16) * D);
-            float4 x3 = *reinterpret_cast<const float4*>(ob + (size_t)(i + 24) * D);
-            const float w0 = wsh[i], w1 = wsh[i + 8], w2 = wsh[i + 16], w3 = wsh[i + 24];
-            a.x += w0 * x0.x + w1 * x1.x + w2 * x2.x + w3 * x3.x;
-            a.y += w0 * x0.y + w1 * x1.y + w2 * x2.y + w3 * x3.y;
-            a.z += w0 * x0.z + w1 * x1.z + w2 * x2.z + w3 * x3.z;
-            a.w += w0 * x0.w + w1 * x1.w + w2 * x2.w + w3 * x3.w;
+            for (int c = 0; c < CW; ++c) pre[i][c] = 0.f;
         }
-        for (; i < n_parts; i += 8) {
-            const float w = wsh[i];
-            if (w > 0.f) {
-                float4 x = *reinterpret_cast<const float4*>(ob + (size_t)i * D);
-                a.x += w * x.x; a.y += w * x.y; a.z += w * x.z; a.w += w * x.w;
+    }
+    float M = -INFINITY;
+    for (int i = lane; i < n_parts; i += 32)
+        if (l[i] > 0.f) M = fmaxf(M, m[i]);
+    for (int k = lane; k < KP; k += 32)
+        if (p.pf_l[(size_t)row * KP + k] > 0.f) M = fmaxf(M, p.pf_m[(size_t)row * KP + k] * kLn2);
+#pragma unroll
+    for (int o = 16; o; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+
+    float acc[CW];
+#pragma unroll
+    for (int c = 0; c < CW; ++c) acc[c] = 0.f;
+    float W = 0.f;
+    for (int i0 = 0; i0 < n_parts; i0 += 32) {
+        float wl = 0.f;
+        if (i0 + lane < n_parts) {
+            const float li = l[i0 + lane];
+            if (li > 0.f) wl = li * __expf(m[i0 + lane] - M);
+        }
+        W += wl;
+        const int nb = min(32, n_parts - i0);
+        int j = 0;
+        if (i0 == 0) {
+#pragma unroll
+            for (; j < PRE; ++j) {
+                const float wj = __shfl_sync(0xffffffffu, wl, j);
+#pragma unroll
+                for (int c = 0; c < CW; ++c) acc[c] = fmaf(wj, pre[j][c], acc[c]);
             }
         }
-        for (int k = warp; k < KP; k += 8) {
-            const float w = wpf[k];
-            if (w > 0.f) {
-                float4 x = *reinterpret_cast<const float4*>(p.pf_o + ((size_t)row * KP + k) * D + c0);
-                a.x += w * x.x; a.y += w * x.y; a.z += w * x.z; a.w += w * x.w;
+#pragma unroll 4
+        for (; j < nb; ++j) {
+            const float wj = __shfl_sync(0xffffffffu, wl, j);
+            float v[CW];
+            load_cols<CW>(ob + (size_t)(i0 + j) * D, v);
+#pragma unroll
+            for (int c = 0; c < CW; ++c) acc[c] = fmaf(wj, v[c], acc[c]);
+        }
+    }
+    for (int k0 = 0; k0 < KP; k0 += 32) {
+        float wl = 0.f;
+        if (k0 + lane < KP) {
+            const size_t i = (size_t)row * KP + k0 + lane;
+            const float lk = p.pf_l[i];
+            if (lk > 0.f) wl = lk * __expf(p.pf_m[i] * kLn2 - M);
+        }
+        W += wl;
+        const int nb = min(32, KP - k0);
+        for (int j = 0; j < nb; ++j) {
+            const float wj = __shfl_sync(0xffffffffu, wl, j);
+            if (wj > 0.f) {
+                float v[CW];
+                load_cols<CW>(p.pf_o + ((size_t)row * KP + k0 + j) * D + lane * CW, v);
+#pragma unroll
+                for (int c = 0; c < CW; ++c) acc[c] = fmaf(wj, v[c], acc[c]);
             }
         }
-        *reinterpret_cast<float4*>(acc + warp * D + c0) = a;
     }
-    __syncthreads();
-    if (2 * tid < p.hd) {
-        const int d = 2 * tid;
-        float s0 = 0.f, s1 = 0.f;
 #pragma unroll
-        for (int w = 0; w < 8; ++w) {
-            s0 += acc[w * D + d];
-            s1 += acc[w * D + d + 1];
-        }
-        const float inv = (Wsh > 0.f) ? 1.f / Wsh : 0.f;
-        *reinterpret_cast<uint32_t*>(static_cast<uint16_t*>(p.out) + (size_t)row * p.hd + d) = F::pack_rn(s0 * inv, s1 * inv);
+    for (int o = 16; o; o >>= 1) W += __shfl_xor_sync(0xffffffffu, W, o);
+    const float inv = (W > 0.f) ? 1.f / W : 0.f;
+    const int c0 = lane * CW;
+    if (c0 < p.hd) {
+        uint16_t* dst = static_cast<uint16_t*>(p.out) + (size_t)row * p.hd + c0;
+#pragma unroll
+        for (int c = 0; c < CW; c += 2)
+            reinterpret_cast<uint32_t*>(dst)[c / 2] = F::pack_rn(acc[c] * inv, acc[c + 1] * inv);
     }
 }
 
