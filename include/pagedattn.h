@@ -128,8 +128,13 @@ int pa_rope_reshape_and_cache(void* q, const void* key, const void* value, void*
 
 /*
  * Split-K workspace size in bytes for pa_decode / pa_decode_splitk with these
- * sizes (partition_tokens <= 0 means PA_DEFAULT_PARTITION_TOKENS).  Layout, each
- * region starting on a 256-byte boundary, P = ceil(max_context_len / partition_tokens):
+ * sizes (partition_tokens <= 0 means PA_DEFAULT_PARTITION_TOKENS): 0 when
+ * ceil(max_context_len / partition_tokens) <= 1 (one piece per sequence, written directly).
+ * Otherwise, each region starting on a 256-byte boundary, P = ceil(max_context_len /
+ * partition_tokens) + 3: the dynamic split-K grid (group size 1 or 2, batches of up to 256
+ * sequences) cuts the last partition_tokens of every context into pieces of a quarter of that
+ * (at most three pieces more); a workspace sized for P = ceil(max_context_len /
+ * partition_tokens) only is still accepted and runs uniform pieces:
  *   m [num_seqs, n_q_heads, P] float  -- per-piece max of scale*q.K (natural-log units)
  *   l [num_seqs, n_q_heads, P] float  -- per-piece sum of exp(s - m)
  *   o [num_seqs, n_q_heads, P, head_dim] float -- per-piece normalised output

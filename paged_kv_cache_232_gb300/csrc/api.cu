@@ -200,6 +200,7 @@ int decode_impl(void* out, const void* q, const void* k_cache, const void* v_cac
         }
         p.part_tokens = part_tokens;
         p.max_parts = max_parts;
+        p.cover_parts = max_parts;
         grid = units * max_parts;
         if (reduce && n_q_heads / n_kv_heads <= 2) {
             // the dynamic grid: one CTA per resident slot taking pieces from the counter (zeroed
@@ -214,6 +215,24 @@ int decode_impl(void* out, const void* q, const void* k_cache, const void* v_cac
             if ((int64_t)grid > slots) {
                 p.dyn = 1;
                 grid = (int)slots;
+                // tail pieces (batches of up to kDynTailMaxSeqs sequences, when the workspace has
+                // room for the extra pieces): the last part_tokens of every context go in pieces
+                // of a quarter of that, so the items handed out last are short and the CTAs end
+                // together
+                const int align = block_size < 16 ? 16 : block_size;
+                const int tail_tokens = ((part_tokens / 4 + align - 1) / align) * align;
+                const int tail_parts = max_parts - 1 + (part_tokens + tail_tokens - 1) / tail_tokens;
+                const WsLayout wt = ws_layout(num_seqs, n_q_heads, kernel_dim(head_dim), tail_parts);
+                if (num_seqs <= pa::kDynTailMaxSeqs && workspace_bytes >= wt.total &&
+                    (int64_t)units * tail_parts <= INT32_MAX) {
+                    char* base = static_cast<char*>(workspace);
+                    p.ws_m = reinterpret_cast<float*>(base + wt.m_off);
+                    p.ws_l = reinterpret_cast<float*>(base + wt.l_off);
+                    p.ws_o = reinterpret_cast<float*>(base + wt.o_off);
+                    p.dyn_counter = reinterpret_cast<int*>(base + wt.ctl_off);
+                    p.tail_tokens = tail_tokens;
+                    p.max_parts = tail_parts;
+                }
                 if (cudaMemsetAsync(p.dyn_counter, 0, sizeof(int), stream) != cudaSuccess) return PA_ERR_CUDA;
             }
         }
@@ -432,7 +451,8 @@ size_t pa_decode_workspace_size(int num_seqs, int n_q_heads, int head_dim, int m
     const int part = partition_or_default(partition_tokens);
     const int max_parts = max_context_len > 0 ? (max_context_len + part - 1) / part : 1;
     if (max_parts <= 1) return 0;
-    return ws_layout(num_seqs, n_q_heads, kernel_dim(head_dim), max_parts).total;
+    // room for the dynamic grid's tail pieces: at most three more than the uniform split
+    return ws_layout(num_seqs, n_q_heads, kernel_dim(head_dim), max_parts + 3).total;
 }
 
 int pa_decode_plan(int num_seqs, int n_q_heads, int n_kv_heads, int head_dim, int block_size, int max_context_len,

@@ -46,9 +46,10 @@ static cudaError_t launch_decode_t(const DecodeParams& p, const CUtensorMap& tmK
         if constexpr (G <= 2) {
             auto kern = decode_kernel_dyn<D, G, BF16>;
             static std::atomic<unsigned long long> s_dyn{0};
-            e = smem_limit_once(reinterpret_cast<const void*>(kern), C::P_SMEM_BYTES, s_dyn);
+            static_assert(C::DYN_SMAX == kDynTailMaxSeqs, "tail-piece batch limit");
+            e = smem_limit_once(reinterpret_cast<const void*>(kern), C::D_SMEM_BYTES, s_dyn);
             if (e != cudaSuccess) return e;
-            e = launch(kern, C::P_SMEM_BYTES);
+            e = launch(kern, C::D_SMEM_BYTES);
         } else {
             return cudaErrorInvalidValue;
         }
@@ -115,8 +116,8 @@ static int dyn_resident_t() {
     using C = DecodeCfg<D, G, BF16>;
     auto kern = decode_kernel_dyn<D, G, BF16>;
     static std::atomic<unsigned long long> s_dyn_q{0};
-    if (smem_limit_once(reinterpret_cast<const void*>(kern), C::P_SMEM_BYTES, s_dyn_q) != cudaSuccess) return 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&r, kern, C::THREADS, C::P_SMEM_BYTES) != cudaSuccess || r < 1)
+    if (smem_limit_once(reinterpret_cast<const void*>(kern), C::D_SMEM_BYTES, s_dyn_q) != cudaSuccess) return 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&r, kern, C::THREADS, C::D_SMEM_BYTES) != cudaSuccess || r < 1)
         return 0;
     cache[dev & 63].store(r, std::memory_order_release);
     return r;

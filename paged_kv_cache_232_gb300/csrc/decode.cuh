@@ -45,7 +45,10 @@ struct DecodeParams {
     unsigned* err;
     int num_seqs, n_q_heads, n_kv_heads, max_blocks_per_seq;
     int part_tokens;           // 0: whole context in one CTA
-    int max_parts;             // P (grid pieces per (s, g))
+    int max_parts;             // P (pieces per (s, g): the workspace stride)
+    int cover_parts;           // pieces of part_tokens that cover the longest context (the length clamp)
+    int tail_tokens;           // decode_kernel_dyn only: > 0 splits each sequence's last part_tokens
+                               // into pieces of this many tokens (pieces_of); 0: pieces of part_tokens
     int num_blocks;
     int cpb_log2;              // log2 of the 16-token chunks per cache block; -1: blocks of 8 tokens
     float qk_scale_log2;       // scale * log2(e)
@@ -68,6 +71,21 @@ struct DecodeParams {
 
 // Tokens of a sequence of context L the decode kernels stream: the part past the shared prefix.
 __device__ __forceinline__ int streamed_tokens(const DecodeParams& p, int L) { return max(L - p.prefix_tokens, 0); }
+
+// Split-K pieces of a sequence with L (clamped) tokens.  Uniform: pieces of part_tokens.  With
+// tail_tokens (the dynamic grid): every piece but the last part_tokens-sized stretch is full, and
+// that stretch (1 .. part_tokens tokens) goes in pieces of tail_tokens, so the items handed out
+// last are short.  0 pieces: nothing streamed.
+__device__ __forceinline__ int full_pieces_of(const DecodeParams& p, int Ls) {
+    return Ls > 0 ? (Ls + p.part_tokens - 1) / p.part_tokens - 1 : 0;
+}
+__device__ __forceinline__ int pieces_of(const DecodeParams& p, int L) {
+    const int Ls = streamed_tokens(p, L);
+    if (p.tail_tokens == 0) return (Ls + p.part_tokens - 1) / p.part_tokens;
+    if (Ls == 0) return 0;
+    const int f = full_pieces_of(p, Ls);
+    return f + (Ls - f * p.part_tokens + p.tail_tokens - 1) / p.tail_tokens;
+}
 
 // Folds the shared-prefix partials of output row `row` into a merge in progress: raises the
 // running maximum M (base 2) first (pass 0), then adds each partial's weight l_k 2^(m_k - M) to
@@ -251,6 +269,13 @@ struct DecodeCfg {
     static constexpr int P_LIST_OFF = P_BAR_OFF + 2 * NST * 8;          // [LIST_MAX][3] (seq, KV head, 0)
     static constexpr int P_FLAG_OFF = P_LIST_OFF + LIST_MAX * 3 * 4;    // unit count, abort flag
     static constexpr int P_SMEM_BYTES = P_FLAG_OFF + 16 + 1024;
+    // decode_kernel_dyn: the persistent layout, then (with tail pieces) per sequence of a batch of
+    // up to DYN_SMAX: the clamped length, running counts of full and of tail pieces
+    static constexpr int DYN_SMAX = 256;
+    static constexpr int D_LEN_OFF = P_FLAG_OFF + 16;
+    static constexpr int D_CUMA_OFF = D_LEN_OFF + DYN_SMAX * 4;
+    static constexpr int D_CUMB_OFF = D_CUMA_OFF + (DYN_SMAX + 1) * 4;
+    static constexpr int D_SMEM_BYTES = D_CUMB_OFF + (DYN_SMAX + 1) * 4 + 1024;
     // Consumer warp w takes blocks b = w, w + NCW, ...; with NST a multiple of NCW every ring stage
     // belongs to one warp, which waits on its phases in order -- a stage's full barrier is then
     // never two phases behind the phase its warp waits for (where the parity test would pass early).
@@ -455,8 +480,8 @@ decode_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmK, con
     // context length, clamped to what the table (and the split-K grid) can address
     int L = __ldg(p.context_lens + s);
     int cap = table_row_tokens(p.max_blocks_per_seq, p.cpb_log2);  // tokens the table row addresses
-    if (p.part_tokens > 0 && p.prefix_tokens + p.max_parts * p.part_tokens < cap)
-        cap = p.prefix_tokens + p.max_parts * p.part_tokens;
+    if (p.part_tokens > 0 && p.prefix_tokens + p.cover_parts * p.part_tokens < cap)
+        cap = p.prefix_tokens + p.cover_parts * p.part_tokens;
     if (L < 0 || L > cap) {
         if (piece == 0 && g == 0 && threadIdx.x == 0) flag_error(p.err, PA_DEVERR_LENGTH);
         L = L < 0 ? 0 : cap;
@@ -972,6 +997,48 @@ decode_kernel_persistent(const DecodeParams p, const __grid_constant__ CUtensorM
     asm volatile("bar.sync 2, %0;" ::"n"(C::THREADS) : "memory");
 }
 
+// decode_kernel_dyn's per-sequence layout with tail pieces: len[s] = the clamped context length,
+// cumA[s] / cumB[s] = full / tail pieces of the sequences before s (a sequence with nothing
+// streamed has one empty tail piece, which writes its output row).  All threads call this.
+__device__ __forceinline__ void dyn_piece_counts(const DecodeParams& p, int cap, int* len, int* cumA, int* cumB) {
+    const int S = p.num_seqs, tid = threadIdx.x, lane = tid & 31;
+    for (int i = tid; i < S; i += blockDim.x) {
+        int L = __ldg(p.context_lens + i);
+        if (L < 0 || L > cap) {
+            if (blockIdx.x == 0) flag_error(p.err, PA_DEVERR_LENGTH);
+            L = L < 0 ? 0 : cap;
+        }
+        const int Ls = streamed_tokens(p, L), f = full_pieces_of(p, Ls);
+        len[i] = L;
+        cumA[i + 1] = f;
+        cumB[i + 1] = Ls > 0 ? pieces_of(p, L) - f : 1;
+    }
+    __syncthreads();
+    if (tid < 32) {
+        int runA = 0, runB = 0;
+        if (lane == 0) cumA[0] = cumB[0] = 0;
+        for (int b = 0; b < S; b += 32) {
+            const int i = b + lane;
+            int a = i < S ? cumA[i + 1] : 0, c = i < S ? cumB[i + 1] : 0;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int ya = __shfl_up_sync(0xffffffffu, a, o), yc = __shfl_up_sync(0xffffffffu, c, o);
+                if (lane >= o) {
+                    a += ya;
+                    c += yc;
+                }
+            }
+            if (i < S) {
+                cumA[i + 1] = runA + a;
+                cumB[i + 1] = runB + c;
+            }
+            runA += __shfl_sync(0xffffffffu, a, 31);
+            runB += __shfl_sync(0xffffffffu, c, 31);
+        }
+    }
+    __syncthreads();
+}
+
 // The dynamic split-K grid (p.dyn): gridDim.x CTAs, one per resident slot, take work items --
 // the split-K pieces, highest piece index first as in decode_kernel's grid -- from a counter the
 // launcher zeroes.  The producer warp fetches an item, publishes it through a small queue in
@@ -1021,9 +1088,21 @@ decode_kernel_dyn(const DecodeParams p, const __grid_constant__ CUtensorMap tmK,
     __syncthreads();
 
     const int units = p.num_seqs * p.n_kv_heads;
-    const long long total = (long long)units * p.max_parts;
     int cap = table_row_tokens(p.max_blocks_per_seq, p.cpb_log2);
-    if (p.prefix_tokens + p.max_parts * p.part_tokens < cap) cap = p.prefix_tokens + p.max_parts * p.part_tokens;
+    if (p.prefix_tokens + p.cover_parts * p.part_tokens < cap) cap = p.prefix_tokens + p.cover_parts * p.part_tokens;
+    // the item order: with tail pieces, each CTA first lays out per sequence its clamped length and
+    // running counts of full and of tail pieces (shared memory, batches of up to DYN_SMAX
+    // sequences); items are then the full pieces, sequence by sequence (KV head fastest), followed
+    // by the tail pieces.  Without: (piece index from the highest down) x unit, skipping the pieces
+    // past a context.
+    const bool tail = p.tail_tokens > 0;
+    int* o_len = reinterpret_cast<int*>(smem + C::D_LEN_OFF);
+    int* o_cumA = reinterpret_cast<int*>(smem + C::D_CUMA_OFF);
+    int* o_cumB = reinterpret_cast<int*>(smem + C::D_CUMB_OFF);
+    if (tail) dyn_piece_counts(p, cap, o_len, o_cumA, o_cumB);
+    const long long n_full = tail ? (long long)o_cumA[p.num_seqs] * p.n_kv_heads : 0;
+    const long long total = tail ? n_full + (long long)o_cumB[p.num_seqs] * p.n_kv_heads
+                                 : (long long)units * p.max_parts;
 
     if (warp == C::NCW) {
         // ------------------------------------------------------------ producer warp
@@ -1043,7 +1122,33 @@ decode_kernel_dyn(const DecodeParams p, const __grid_constant__ CUtensorMap tmK,
             item = __shfl_sync(0xffffffffu, item, 0);
             const bool end = (long long)item >= total;
             int s = -1, g = 0, piece = 0, t_begin = 0, t_end = 0, n_parts = 0;
-            if (!end) {
+            if (!end && tail) {
+                const bool full = (long long)item < n_full;
+                const int r = full ? item : (int)((long long)item - n_full);
+                const int e = r / p.n_kv_heads;
+                g = r - e * p.n_kv_heads;
+                const int* cum = full ? o_cumA : o_cumB;
+                // the sequence s with cum[s] <= e < cum[s + 1]
+                int lo = 0, hi = p.num_seqs;
+                while (hi - lo > 1) {
+                    const int mid = (lo + hi) >> 1;
+                    if (cum[mid] <= e) lo = mid; else hi = mid;
+                }
+                s = lo;
+                const int L = o_len[s], base = min(L, p.prefix_tokens), Ls = L - base;
+                const int f = o_cumA[s + 1] - o_cumA[s];
+                if (full) {
+                    piece = e - o_cumA[s];
+                    t_begin = base + piece * p.part_tokens;
+                    t_end = t_begin + p.part_tokens;
+                } else {
+                    const int k = e - o_cumB[s];
+                    piece = f + k;
+                    t_begin = min(L, base + f * p.part_tokens + k * p.tail_tokens);
+                    t_end = min(L, t_begin + p.tail_tokens);
+                }
+                n_parts = Ls > 0 ? f + (o_cumB[s + 1] - o_cumB[s]) : 0;
+            } else if (!end) {
                 const int qpos = item / units, sg = item - qpos * units;
                 piece = (p.max_parts - 1) - qpos;
                 s = sg / p.n_kv_heads;
@@ -1329,9 +1434,9 @@ __global__ void __launch_bounds__(256, 2) splitk_merge_kernel(const DecodeParams
     if (row >= p.num_seqs * p.n_q_heads) return;
     const int s = row / p.n_q_heads;
     int L = __ldg(p.context_lens + s);
-    const int cap = min(table_row_tokens(p.max_blocks_per_seq, p.cpb_log2), p.prefix_tokens + p.max_parts * p.part_tokens);
+    const int cap = min(table_row_tokens(p.max_blocks_per_seq, p.cpb_log2), p.prefix_tokens + p.cover_parts * p.part_tokens);
     L = L < 0 ? 0 : (L > cap ? cap : L);
-    const int n_parts = (streamed_tokens(p, L) + p.part_tokens - 1) / p.part_tokens;
+    const int n_parts = pieces_of(p, L);
     if (n_parts <= 1) return;  // written directly by the piece kernel
     // launched as a programmatic dependent of the piece kernel: its partials (and, through it, the
     // shared-prefix pass's) are complete and visible past this point

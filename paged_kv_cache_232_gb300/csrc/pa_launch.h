@@ -61,6 +61,9 @@ inline int decode_list_max() { return DecodeCfg<128, 1, true>::LIST_MAX; }
 // CTAs of the decode kernel for (dtype, head_dim, group) that fit on one SM (0 on a CUDA error);
 // queried once per device, so a call inside a stream capture makes no CUDA call.
 int decode_resident_ctas(int bf16, int head_dim, int group);
+// Batches of up to this many sequences get the dynamic split-K grid's tail pieces (its
+// per-sequence counts live in shared memory).
+constexpr int kDynTailMaxSeqs = 256;
 // The same for the dynamic split-K kernel (decode_kernel_dyn).
 int decode_dyn_resident_ctas(int bf16, int head_dim, int group);
 

@@ -267,27 +267,41 @@ def test_dispatcher_plan_pieces(S, hq, hkv, d, bs, L):
     assert pa.pa_decode_plan(256, 16, 8, 128, 16, 2048)[0] == 1       # one-pass: enough units, short contexts
 
 
-@pytest.mark.parametrize("dt,hq,hkv,d,bs", [(wl.BF16, 16, 8, 128, 16), (wl.F16, 8, 8, 64, 8), (wl.BF16, 4, 2, 256, 32),
-                                            (wl.F16, 16, 8, 96, 16)])
-def test_dynamic_split_grid(dt, hq, hkv, d, bs):
+def _uniform_split_ws_bytes(S, hq, d, maxL, part):
+    """The split-K workspace without room for tail pieces: m, l, o for ceil(maxL / part) pieces
+    (each region 256-byte aligned) and the 256-byte control region."""
+    kd = 128 if d == 96 else d
+    rows = S * hq * (-(-maxL // part))
+    a = lambda n: (n + 255) // 256 * 256
+    return 2 * a(rows * 4) + a(rows * kd * 4) + 256
+
+
+@pytest.mark.parametrize("dt,hq,hkv,d,bs,S,maxlen", [(wl.BF16, 16, 8, 128, 16, 96, 3000), (wl.F16, 8, 8, 64, 8, 96, 3000),
+                                                   (wl.BF16, 4, 2, 256, 32, 96, 3000), (wl.F16, 16, 8, 96, 16, 96, 3000),
+                                                   (wl.BF16, 16, 8, 128, 16, 300, 1200),
+                                                   (wl.BF16, 8, 8, 128, 64, 40, 5000)])
+def test_dynamic_split_grid(dt, hq, hkv, d, bs, S, maxlen):
     """Group size 1 or 2 with more split-K pieces than resident CTAs: one CTA per resident slot
-    takes pieces from a counter in the workspace, in whatever order the CTAs free up.  A piece's
-    arithmetic does not depend on which CTA takes it, so repeated calls agree bit for bit; the
-    counter is zeroed by the call (the workspace starts filled with 0x7f bytes); against the
-    oracle, with empty and one-token contexts among long ones."""
-    lens = wl.uniform_ints(wl.derive_seed(77, hq + d), 96, 1, 3000)
-    lens[[3, 40, 41]] = 0
-    lens[[10, 90]] = 1
-    lens[50] = 3000
-    w = wl.build_workload("dyn", 77 + hq + d + bs, dtype=dt, n_q_heads=hq, n_kv_heads=hkv, head_dim=d, block_size=bs,
-                          decode_lens=lens.tolist(), extra_blocks=3)
+    takes pieces from a counter in the workspace, in whatever order the CTAs free up; batches of
+    up to 256 sequences cut the last piece-length of every context into quarter pieces (tail
+    pieces), larger ones (300) keep uniform pieces, as does a workspace sized without room for the
+    tail pieces.  A piece's arithmetic does not depend on which CTA takes it, so repeated calls
+    agree bit for bit; the counter is zeroed by the call (the workspace starts filled with 0x7f
+    bytes); against the oracle, with empty and one-token contexts among long ones."""
+    lens = wl.uniform_ints(wl.derive_seed(77, hq + d + S), S, 1, maxlen)
+    lens[[3, 20, 21]] = 0
+    lens[[10, 30]] = 1
+    lens[35] = maxlen
+    w = wl.build_workload("dyn", 77 + hq + d + bs + S, dtype=dt, n_q_heads=hq, n_kv_heads=hkv, head_dim=d,
+                          block_size=bs, decode_lens=lens.tolist(), extra_blocks=3)
     dev = Dev(w)
     ref = oracle_decode(w)
-    S = w.decode.num_seqs
     pa.pa_device_errors(clear=True)
-    for part in (256, 512):
-        ws = torch.full((max(16, pa.pa_decode_workspace_size(S, hq, d, dev.maxL, part)),), 0x7F, dtype=torch.uint8,
-                        device="cuda")
+    for part, ws_bytes in ((256, None), (512, None), (256, _uniform_split_ws_bytes(S, hq, d, dev.maxL, 256))):
+        part = max(part, bs)
+        if ws_bytes is None:
+            ws_bytes = pa.pa_decode_workspace_size(S, hq, d, dev.maxL, part)
+        ws = torch.full((max(16, ws_bytes),), 0x7F, dtype=torch.uint8, device="cuda")
         first = None
         for _ in range(4):
             out = torch.full_like(dev.q, float("nan"))
