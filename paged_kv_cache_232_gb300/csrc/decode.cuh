@@ -1096,6 +1096,17 @@ decode_kernel_dyn(const DecodeParams p, const __grid_constant__ CUtensorMap tmK,
     // by the tail pieces.  Without: (piece index from the highest down) x unit, skipping the pieces
     // past a context.
     const bool tail = p.tail_tokens > 0;
+    // the first claim and the block tables' way into L2 overlap the prologue's length loads: the
+    // producer takes its first item now, and every CTA prefetches its share of the table lines
+    // (tables of up to 4 MB)
+    int first = 0;
+    if (warp == C::NCW && lane == 0) first = atomicAdd(p.dyn_counter, 1);
+    {
+        long long lines = ((long long)p.num_seqs * p.max_blocks_per_seq * 4 + 127) / 128;
+        if (lines > 32768) lines = 0;
+        for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < lines; i += (long long)gridDim.x * blockDim.x)
+            asm volatile("prefetch.global.L2 [%0];" ::"l"(reinterpret_cast<const char*>(p.block_tables) + i * 128));
+    }
     int* o_len = reinterpret_cast<int*>(smem + C::D_LEN_OFF);
     int* o_cumA = reinterpret_cast<int*>(smem + C::D_CUMA_OFF);
     int* o_cumB = reinterpret_cast<int*>(smem + C::D_CUMB_OFF);
@@ -1116,9 +1127,9 @@ decode_kernel_dyn(const DecodeParams p, const __grid_constant__ CUtensorMap tmK,
         uint32_t fused = 0, fpar = 0;          // per stage: filled before; parity of its fill count
         int ring_next = 0, nq = 0;             // ring index of the next chunk; items published
         bool ok = true;
-        while (ok) {
-            int item = 0;
-            if (lane == 0) item = atomicAdd(p.dyn_counter, 1);
+        for (bool claimed = true; ok; claimed = false) {
+            int item = first;
+            if (lane == 0 && !claimed) item = atomicAdd(p.dyn_counter, 1);
             item = __shfl_sync(0xffffffffu, item, 0);
             const bool end = (long long)item >= total;
             int s = -1, g = 0, piece = 0, t_begin = 0, t_end = 0, n_parts = 0;
