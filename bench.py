@@ -384,7 +384,8 @@ def prepare(args, name, dev, with_host=False):
         pbt, qsl, sl = dev_int(u.block_tables), dev_int(u.query_start_loc), dev_int(u.seq_lens)
         h_dev += [pbt, qsl, sl]
         stages = [s_ for s_ in stages if s_[0] != "decode"]
-        stages.append(("unified", lambda: pa.pa_prefill_chunk(out, q, kc, vc, pbt, qsl, sl, u.max_q_len, u.scale),
+        stages.append(("unified", lambda: pa.pa_prefill_chunk(out, q, kc, vc, pbt, qsl, sl, u.max_q_len, u.scale,
+                                                              small_m=args.small_m),
                        prefill_flops(u, hq, D), "tensor"))
         which, dec_logical, dec_launches = 0, 0, 0
     elif pre is not None:
@@ -402,7 +403,8 @@ def prepare(args, name, dev, with_host=False):
     c.has_pre_and_dec = pre is not None and b is not None
     c.decode_path = None
     if b is not None:
-        c.decode_path = ("unified: decode rows as one-row chunks of the prefill launch" if which == 0
+        c.decode_path = (("unified: decode rows as one-row chunks of the prefill launch"
+                          + (" (small-M tiles)" if args.small_m else "")) if which == 0
                          else (f"shared prefix of {prefix} tokens on the tensor cores + suffix "
                                + ("one-pass" if dec_launches == 2 else f"split-K/{part}") if which == 3
                                else ("one-pass" if which == 1 else f"split-K/{part}"))
@@ -773,6 +775,8 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--unified", action="store_true",
                     help="mixed batch: decode rows through the prefill kernel in the same launch (one-row chunks)")
+    ap.add_argument("--small-m", action="store_true",
+                    help="with --unified: pa_prefill_chunk_small_m (M = 64 tiles for the decode rows' units)")
     ap.add_argument("--decode-path", choices=["auto", "plain", "v1", "splitk"], default="auto",
                     help="force the one-pass or split-K decode kernel instead of the library's dispatcher "
                          "(plain: the dispatcher without the shared-prefix pass)")

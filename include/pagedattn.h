@@ -311,6 +311,20 @@ int pa_prefill_chunk(void* out, const void* q, const void* k_cache, const void* 
                      int head_dim, int block_size, int64_t num_blocks, float scale, int dtype, void* stream);
 
 /*
+ * pa_prefill_chunk_small_m -- pa_prefill_chunk with small-M tiles: a (chunk, KV head) unit
+ * whose rows (query tokens x the group's heads) fit in 64 runs its tile as M = 64 tensor-core
+ * MMAs instead of M = 128.  Meant for the unified launch, where every decode sequence is a
+ * one-row chunk (G valid rows of a tile).  Source: mini_engine, "Custom CUDA kernels" (the
+ * unified attention mode kept for comparison) and "Results" (unified mode is slower because a
+ * decode query is a single row that wastes almost all of a prefill tile).  Same arguments,
+ * result (up to the order of the arithmetic) and errors as pa_prefill_chunk.
+ */
+int pa_prefill_chunk_small_m(void* out, const void* q, const void* k_cache, const void* v_cache,
+                             const int32_t* block_tables, int max_blocks_per_seq, const int32_t* query_start_loc,
+                             const int32_t* seq_lens, int num_chunks, int max_q_len, int n_q_heads, int n_kv_heads,
+                             int head_dim, int block_size, int64_t num_blocks, float scale, int dtype, void* stream);
+
+/*
  * Reads (and with clear != 0, resets) the error word of the current device.
  * Synchronises the device first.  Returns the PA_DEVERR_* bits, or a negative
  * status if the CUDA calls fail.

@@ -24,7 +24,7 @@ EXPORTED = (
     "pa_reshape_and_cache", "pa_decode_workspace_size", "pa_decode", "pa_decode_plan", "pa_decode_v1",
     "pa_decode_splitk", "pa_prefill_chunk", "pa_device_errors", "pa_status_string", "pa_version",
     "pa_decode_splitk_static", "pa_rope_table", "pa_rope_reshape_and_cache", "pa_decode_shared_prefix",
-    "pa_decode_shared_prefix_workspace_size",
+    "pa_decode_shared_prefix_workspace_size", "pa_prefill_chunk_small_m",
 )
 STATIC_SCRATCH_BYTES = 16 << 20
 
@@ -81,6 +81,8 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
     L.pa_decode_shared_prefix_workspace_size.restype = sz
     L.pa_prefill_chunk.argtypes = [vp, vp, vp, vp, vp, i32, vp, vp, i32, i32, i32, i32, i32, i32, i64, f32, i32, vp]
     L.pa_prefill_chunk.restype = i32
+    L.pa_prefill_chunk_small_m.argtypes = L.pa_prefill_chunk.argtypes
+    L.pa_prefill_chunk_small_m.restype = i32
     L.pa_device_errors.argtypes = [i32]
     L.pa_device_errors.restype = i32
     L.pa_status_string.argtypes = [i32]
@@ -278,8 +280,9 @@ def pa_decode_shared_prefix(out, q, k_cache, v_cache, block_tables, context_lens
 
 
 def pa_prefill_chunk(out, q, k_cache, v_cache, block_tables, query_start_loc, seq_lens, max_q_len: int, scale: float,
-                     stream=None) -> None:
-    """Prefill chunks (bottom-right causal over their cached context) on the tcgen05 tensor cores."""
+                     stream=None, small_m: bool = False) -> None:
+    """Prefill chunks (bottom-right causal over their cached context) on the tcgen05 tensor cores;
+    small_m=True calls pa_prefill_chunk_small_m (M = 64 tiles for units of at most 64 rows)."""
     torch = _torch()
     dt = _dtype_code(q)
     nb, bs, hkv, d = _cache_dims(k_cache)
@@ -287,12 +290,13 @@ def pa_prefill_chunk(out, q, k_cache, v_cache, block_tables, query_start_loc, se
     if d2 != d or tuple(out.shape) != tuple(q.shape):
         raise ValueError("q/out/cache head_dim mismatch")
     C = int(seq_lens.shape[0])
-    st = load().pa_prefill_chunk(_dev(out, "out", q.dtype), _dev(q, "q", q.dtype), _dev(k_cache, "k_cache", q.dtype),
-                                 _dev(v_cache, "v_cache", q.dtype), _dev(block_tables, "block_tables", torch.int32),
-                                 int(block_tables.shape[1]), _dev(query_start_loc, "query_start_loc", torch.int32),
-                                 _dev(seq_lens, "seq_lens", torch.int32), C, int(max_q_len), hq, hkv, d, bs, nb,
-                                 float(scale), dt, _stream(stream, q.device))
-    _check(st, "pa_prefill_chunk")
+    fn = load().pa_prefill_chunk_small_m if small_m else load().pa_prefill_chunk
+    st = fn(_dev(out, "out", q.dtype), _dev(q, "q", q.dtype), _dev(k_cache, "k_cache", q.dtype),
+            _dev(v_cache, "v_cache", q.dtype), _dev(block_tables, "block_tables", torch.int32),
+            int(block_tables.shape[1]), _dev(query_start_loc, "query_start_loc", torch.int32),
+            _dev(seq_lens, "seq_lens", torch.int32), C, int(max_q_len), hq, hkv, d, bs, nb,
+            float(scale), dt, _stream(stream, q.device))
+    _check(st, "pa_prefill_chunk_small_m" if small_m else "pa_prefill_chunk")
 
 
 def pa_device_errors(clear: bool = True) -> int:

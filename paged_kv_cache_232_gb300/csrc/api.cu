@@ -506,10 +506,11 @@ int pa_decode(void* out, const void* q, const void* k_cache, const void* v_cache
                             workspace, workspace_bytes, stream);
 }
 
-int pa_prefill_chunk(void* out, const void* q, const void* k_cache, const void* v_cache,
-                     const int32_t* block_tables, int max_blocks_per_seq, const int32_t* query_start_loc,
-                     const int32_t* seq_lens, int num_chunks, int max_q_len, int n_q_heads, int n_kv_heads,
-                     int head_dim, int block_size, int64_t num_blocks, float scale, int dtype, void* stream) {
+static int prefill_impl(void* out, const void* q, const void* k_cache, const void* v_cache,
+                        const int32_t* block_tables, int max_blocks_per_seq, const int32_t* query_start_loc,
+                        const int32_t* seq_lens, int num_chunks, int max_q_len, int n_q_heads, int n_kv_heads,
+                        int head_dim, int block_size, int64_t num_blocks, float scale, int dtype, void* stream,
+                        bool small_m) {
     if (num_chunks < 0 || max_q_len < 0 || max_blocks_per_seq <= 0 || num_blocks <= 0) return PA_ERR_SHAPE;
     int st = check_heads(n_q_heads, n_kv_heads, head_dim, block_size, dtype);
     if (st != PA_OK) return st;
@@ -542,9 +543,30 @@ int pa_prefill_chunk(void* out, const void* q, const void* k_cache, const void* 
     CUtensorMap tk, tv;
     if ((st = encode_cache_map(&tk, k_cache, dtype, num_blocks, block_size, n_kv_heads, head_dim)) != PA_OK) return st;
     if ((st = encode_cache_map(&tv, v_cache, dtype, num_blocks, block_size, n_kv_heads, head_dim)) != PA_OK) return st;
-    cudaError_t e = pa::launch_prefill(dtype == PA_BF16, kernel_dim(head_dim), G, p, tk, tv, static_cast<cudaStream_t>(stream));
+    cudaError_t e = small_m ? pa::launch_prefill_small(dtype == PA_BF16, kernel_dim(head_dim), G, p, tk, tv,
+                                                       static_cast<cudaStream_t>(stream))
+                            : pa::launch_prefill(dtype == PA_BF16, kernel_dim(head_dim), G, p, tk, tv,
+                                                 static_cast<cudaStream_t>(stream));
     if (e == cudaErrorNotSupported) return PA_ERR_UNSUPPORTED;
     return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
+int pa_prefill_chunk(void* out, const void* q, const void* k_cache, const void* v_cache,
+                     const int32_t* block_tables, int max_blocks_per_seq, const int32_t* query_start_loc,
+                     const int32_t* seq_lens, int num_chunks, int max_q_len, int n_q_heads, int n_kv_heads,
+                     int head_dim, int block_size, int64_t num_blocks, float scale, int dtype, void* stream) {
+    return prefill_impl(out, q, k_cache, v_cache, block_tables, max_blocks_per_seq, query_start_loc, seq_lens,
+                        num_chunks, max_q_len, n_q_heads, n_kv_heads, head_dim, block_size, num_blocks, scale, dtype,
+                        stream, false);
+}
+
+int pa_prefill_chunk_small_m(void* out, const void* q, const void* k_cache, const void* v_cache,
+                             const int32_t* block_tables, int max_blocks_per_seq, const int32_t* query_start_loc,
+                             const int32_t* seq_lens, int num_chunks, int max_q_len, int n_q_heads, int n_kv_heads,
+                             int head_dim, int block_size, int64_t num_blocks, float scale, int dtype, void* stream) {
+    return prefill_impl(out, q, k_cache, v_cache, block_tables, max_blocks_per_seq, query_start_loc, seq_lens,
+                        num_chunks, max_q_len, n_q_heads, n_kv_heads, head_dim, block_size, num_blocks, scale, dtype,
+                        stream, true);
 }
 
 // ---- shared prefix --------------------------------------------------------------------------

@@ -98,6 +98,9 @@ struct PrefillParams {
 
 cudaError_t launch_prefill(int bf16, int head_dim, int group, const PrefillParams& params, const CUtensorMap& tmK,
                            const CUtensorMap& tmV, cudaStream_t stream);
+// The same launch with M = 64 tiles for the units whose rows (query tokens x group heads) fit in 64.
+cudaError_t launch_prefill_small(int bf16, int head_dim, int group, const PrefillParams& params,
+                                 const CUtensorMap& tmK, const CUtensorMap& tmV, cudaStream_t stream);
 
 // The shared-prefix pass (prefill kernel in shared-prefix mode): grid of query-tile pairs x KV
 // heads x prefix pieces.  Its CTAs let a programmatic dependent launch (the suffix decode) start

@@ -289,7 +289,9 @@ __device__ __forceinline__ void softmax_sub64(const uint32_t tSb, const uint32_t
 // itself, bottom-right causal).  PREFIX = true: the shared-prefix pass of a decode batch (rows =
 // the sequences' decode queries, keys = one piece of the prefix all of them share, each row cut
 // at its own context length), writing fp32 (m, l, o) partials that the decode merges.
-template <int G, bool BF16, int D, bool PREFIX>
+// SMALL: units whose rows fit in 64 run M = 64 tiles (pa_prefill_chunk_small_m, the unified
+// launch's A/B); instantiated separately, so that the other kernels carry none of its code.
+template <int G, bool BF16, int D, bool PREFIX, bool SMALL = false>
 __global__ void __launch_bounds__(pf::THREADS, 1)
 prefill_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV) {
     using namespace pf;
@@ -364,6 +366,10 @@ prefill_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmK, c
     const int j0 = unit * NQ * TQ;
     if (j0 >= q_len) return;  // whole CTA: past the chunk
     const int ctx = kv_len - q_len;
+    // small-M tile: a unit whose rows fit in 64 (a decode row of the unified launch is one token x G
+    // heads) runs tile 0 as M = 64 MMAs, half the tensor work of a 128-row tile.  At M = 64 row r
+    // of S, P and O sits in TMEM lane (r mod 16) + 32 (r / 16): lanes 0-15 of each warp's quarter.
+    const bool small = SMALL && (q_len - j0) * G <= 64;
     int n_sub[NQT];           // 64-key S sub-tiles each query tile needs (0: tile past the chunk)
 #pragma unroll
     for (int t = 0; t < NQT; ++t) {
@@ -412,11 +418,13 @@ prefill_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmK, c
         // ------------------------------------------------------------ softmax warpgroups (with
         // one query tile per CTA the second warpgroup has no work)
         const int t = warp >> 2;                    // query tile of this warpgroup
-        const int r = threadIdx.x & 127;            // row of the tile == TMEM lane
+        // row of the tile: the TMEM lane, or at M = 64 lanes 0-15 of each quarter (-1: no row)
+        const int r = !small ? (int)(threadIdx.x & 127) : (lane < 16 ? 16 * (warp & 3) + lane : -1);
+        const int rr = r < 0 ? 0 : r;
         const int jt0 = j0 + t * TQ;
-        const int jr = jt0 + r / G;
-        const int hr = g * G + (r % G);
-        const bool row_valid = jr < q_len;
+        const int jr = jt0 + rr / G;
+        const int hr = g * G + (rr % G);
+        const bool row_valid = r >= 0 && jr < q_len;
         int lim, lim_min;  // keys <= lim are visible to this row; lim_min: smallest limit of the warp's rows
         if constexpr (PREFIX) {
             const int Ls = row_valid ? max(__ldg(p.context_lens + jr), 0) : 0;
@@ -453,6 +461,18 @@ prefill_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmK, c
                 }
             }
             tc::fence_async_smem();
+            if (small) {
+                // M = 64: zero this warp's lanes of the tile's S buffers before the first QK (the
+                // issuer waits for Q_FULL); the lanes without a row keep S = 0 from then on
+                uint32_t z[64];
+#pragma unroll
+                for (int i = 0; i < 64; ++i) z[i] = 0u;
+                const uint32_t tSz = tmem + ((uint32_t)((warp & 3) * 32) << 16) + (uint32_t)(t * 128);
+                tc::st64(tSz, z);
+                tc::st64(tSz + 64, z);
+                tc::wait_st();
+                tc::fence_before();
+            }
             mbar_arrive(bars + 8 * Q_FULL);
         }
         // this row's output, formed before the loop so that only the pointer stays live across it
@@ -462,7 +482,10 @@ prefill_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmK, c
         const uint32_t tS = tmem + lane_base + (uint32_t)(t * 128);
         const uint32_t tO = tmem + lane_base + O_COL + (uint32_t)(t * D);
         const float sc = p.qk_scale_log2;
-        float m_ref = -INFINITY, l = 0.f;
+        // M = 64: a lane without a row sees S = 0 (its S columns are zeroed before the first QK and
+        // it writes back zero weights) and keeps a reference of +inf, so its weights are 0 and it
+        // never asks its warp for a max pass or a rescale
+        float m_ref = (r < 0) ? INFINITY : -INFINITY, l = 0.f;
         bool ok = true;
         for (int u = 0; u < nsub; ++u) {
             const int b = u & 1;
@@ -612,8 +635,8 @@ prefill_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmK, c
         // issuer per tile, one tile's MMAs go out while the other issuer waits.
         const int t = (warp == MMA_WARP) ? 0 : 1;
         const int nst = (t == 0) ? n_sub[0] : n_sub[1];
-        constexpr uint32_t ID_QK = tc::idesc_f16(BF16, false, BM, BS);
-        constexpr uint32_t ID_PV = tc::idesc_f16(BF16, true, BM, D);
+        const uint32_t ID_QK = small ? tc::idesc_f16(BF16, false, 64, BS) : tc::idesc_f16(BF16, false, BM, BS);
+        const uint32_t ID_PV = small ? tc::idesc_f16(BF16, true, 64, D) : tc::idesc_f16(BF16, true, BM, D);
         // descriptors of the tile bases as (low, high) words; a K-step adds its byte offset >> 4
         // to the start-address field in the low word (addresses stay below 256 KB: no carry)
         const uint64_t dq = tc::sdesc_sw128(sQ + t * QTILE, 16, 1024), dk = tc::sdesc_sw128(sK, 16, 1024);

@@ -20,7 +20,7 @@ pytestmark = pytest.mark.gpu
 P_ROUND = {wl.BF16: 2.0 ** -16, wl.F16: 2.0 ** -22}
 
 
-def run_prefill(w, out=None, q=None, kc=None, vc=None):
+def run_prefill(w, out=None, q=None, kc=None, vc=None, small_m=False):
     p, pre = w.pool, w.prefill
     kc = to_dev(p.k_cache, p.dtype) if kc is None else kc
     vc = to_dev(p.v_cache, p.dtype) if vc is None else vc
@@ -28,7 +28,7 @@ def run_prefill(w, out=None, q=None, kc=None, vc=None):
     out = torch.empty_like(q) if out is None else out
     pa.pa_prefill_chunk(out, q, kc, vc, to_dev_i(pre.block_tables, torch.int32),
                         to_dev_i(pre.query_start_loc, torch.int32), to_dev_i(pre.seq_lens, torch.int32),
-                        pre.max_q_len, pre.scale)
+                        pre.max_q_len, pre.scale, small_m=small_m)
     torch.cuda.synchronize()
     return out
 
@@ -75,6 +75,23 @@ def test_prefill_ragged_chunks_full_parity(dt, hq, hkv, d):
                           prefill_ctx_lens=[0, 20, 5, 127, 300, 1000, 16], extra_blocks=3)
     got = bits_of(run_prefill(w))
     check(got, oracle_rows(w), dt, f"prefill {dt} {hq}/{hkv} hd {d}")
+    assert pa.pa_device_errors(clear=True) == 0
+
+
+@pytest.mark.parametrize("dt,hq,hkv,d", [(wl.BF16, 16, 8, 128), (wl.F16, 32, 8, 128), (wl.BF16, 16, 2, 64),
+                                         (wl.BF16, 8, 8, 128), (wl.F16, 16, 8, 256)])
+def test_prefill_small_m_tiles(dt, hq, hkv, d):
+    """pa_prefill_chunk_small_m: chunks whose rows (query tokens x group heads) fit in 64 run as
+    M = 64 MMAs (rows in TMEM lanes 0-15 of each quarter; the other lanes hold S = 0 and weight
+    0): chunks right at 64 rows and one token past it (a 128-row tile), single tokens over long
+    contexts (the unified launch's decode rows), every row against the oracle."""
+    G = hq // hkv
+    at = 64 // G
+    w = wl.build_workload("pfsm", 400 + hq + hkv + d, dtype=dt, n_q_heads=hq, n_kv_heads=hkv, head_dim=d,
+                          prefill_q_lens=[at, at + 1, 1, 1, max(1, at // 2), at],
+                          prefill_ctx_lens=[0, 37, 2047, 0, 1000, 3001], extra_blocks=3)
+    got = bits_of(run_prefill(w, small_m=True))
+    check(got, oracle_rows(w), dt, f"small-M {dt} {hq}/{hkv} hd {d}")
     assert pa.pa_device_errors(clear=True) == 0
 
 
@@ -197,10 +214,12 @@ def test_prefill_repeated_runs_bitwise_identical_and_no_device_errors(cfg):
     assert pa.pa_device_errors(clear=True) == 0
 
 
-def test_unified_mixed_batch_single_launch():
+@pytest.mark.parametrize("small_m", [False, True])
+def test_unified_mixed_batch_single_launch(small_m):
     """The mixed batch through one prefill launch: each decode sequence a chunk of one query
     row over its whole context, then the prefill chunks (the unified variant the split
-    dispatch is compared with).  Decode rows against the oracle's decode, prefill rows sampled."""
+    dispatch is compared with), with 128-row tiles and with small-M tiles for the decode rows.
+    Decode rows against the oracle's decode, prefill rows sampled."""
     w = wl.make_workload(5)
     p, b = w.pool, w.decode
     u = wl.unified_batch(w)
@@ -208,7 +227,7 @@ def test_unified_mixed_batch_single_launch():
     out = torch.full_like(q, float("nan"))
     pa.pa_device_errors(clear=True)
     pa.pa_prefill_chunk(out, q, kc, vc, to_dev_i(u.block_tables, torch.int32), to_dev_i(u.query_start_loc, torch.int32),
-                        to_dev_i(u.seq_lens, torch.int32), u.max_q_len, u.scale)
+                        to_dev_i(u.seq_lens, torch.int32), u.max_q_len, u.scale, small_m=small_m)
     torch.cuda.synchronize()
     assert pa.pa_device_errors(clear=True) == 0
     got = bits_of(out)
