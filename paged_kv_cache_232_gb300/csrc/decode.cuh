@@ -477,6 +477,13 @@ decode_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmK, con
         g = sg - s * p.n_kv_heads;
     }
 
+    // a CTA over a whole context from its first token (one pass, no shared prefix, blocks of 16
+    // tokens or more): the producer loads the first table entries at once, next to the context
+    // length instead of after it (one dependent memory latency less before the first K/V tile)
+    const bool spec = p.part_tokens == 0 && p.prefix_tokens == 0 && p.cpb_log2 >= 0;
+    int spec_blk = 0;
+    if (spec && warp == C::NCW && (lane >> p.cpb_log2) < p.max_blocks_per_seq)
+        spec_blk = __ldg(p.block_tables + (size_t)s * p.max_blocks_per_seq + (lane >> p.cpb_log2));
     // context length, clamped to what the table (and the split-K grid) can address
     int L = __ldg(p.context_lens + s);
     int cap = table_row_tokens(p.max_blocks_per_seq, p.cpb_log2);  // tokens the table row addresses
@@ -525,7 +532,7 @@ decode_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmK, con
             int my = p.num_blocks;  // outside the tensor map: TMA fills zeros
             const int e = half8 ? 2 * (blk0 + b0) + lane : (blk0 + b0 + lane) >> p.cpb_log2;
             if (half8 ? (lane < 2 * nb && 8 * e < L) : (lane < nb)) {
-                my = __ldg(bt + e);
+                my = (spec && b0 == 0) ? spec_blk : __ldg(bt + e);
                 if (my < 0 || my >= p.num_blocks) {
                     flag_error(p.err, PA_DEVERR_BLOCK);
                     my = p.num_blocks;
