@@ -158,7 +158,9 @@ size_t pa_decode_workspace_size(int num_seqs, int n_q_heads, int head_dim, int m
  *  out   [num_seqs, n_q_heads, head_dim]   written
  *  q     [num_seqs, n_q_heads, head_dim]   read
  *  block_tables [num_seqs, max_blocks_per_seq] int32 physical block ids; entries
- *                past ceil(context_lens[s]/block_size) are never read
+ *                past ceil(context_lens[s]/block_size) are never used (they may hold
+ *                anything; the first 32 entries of a row may be loaded before the context
+ *                length is known, and the table lines prefetched into L2)
  *  context_lens [num_seqs] int32, tokens in the cache for each sequence (including
  *                the one just written); 0 gives an all-zero output row
  *  max_context_len  host-side upper bound of context_lens (sizes the split-K grid);
