@@ -88,7 +88,7 @@ def test_prefix_zero_is_plain_decode_bitwise():
 
 
 @pytest.mark.parametrize("case", ["whole_context", "mid_block", "mid_chunk", "shorter_than_prefix",
-                                  "loose_bound", "many_tiles", "split_k_suffix"])
+                                  "loose_bound", "many_tiles", "split_k_suffix", "dynamic_split_suffix"])
 def test_shared_prefix_edges(case):
     """whole_context: every context is exactly the prefix (no suffix).  mid_block / mid_chunk: the
     prefix the caller names ends inside a block (and inside a 16-token chunk: the remainder is
@@ -97,7 +97,9 @@ def test_shared_prefix_edges(case):
     the prefix pass meets tokens no sequence owns (NaN canaries) and must cut at the longest
     context.  many_tiles: 300 sequences (five 128-row query tiles per KV head).  split_k_suffix:
     four sequences with long suffixes, where the dispatcher splits the suffix and the split-K
-    merge folds in the prefix partials."""
+    merge folds in the prefix partials.  dynamic_split_suffix: 16 sequences at group size 2 with
+    long suffixes, whose split goes to the dynamic grid (tail pieces; the CTA that finishes a
+    unit merges it with the prefix partials)."""
     maxL = None
     if case == "whole_context":
         w, P = shared_case(21, [512] * 9, 32), 512
@@ -112,11 +114,18 @@ def test_shared_prefix_edges(case):
     elif case == "many_tiles":
         lens = 512 + wl.uniform_ints(wl.derive_seed(26, 1), 300, 1, 700)
         w, P = shared_case(26, lens, 32), 512
-    else:
+    elif case == "split_k_suffix":
         w, P = shared_case(27, [12000, 9000, 16000, 2049], 128, hq=32, hkv=8), 2048
+    else:
+        lens = 1024 + wl.uniform_ints(wl.derive_seed(28, 1), 16, 3000, 8000)
+        lens[5] = 1024
+        w, P = shared_case(28, lens, 64), 1024
     if case == "split_k_suffix":
         which, _ = pa.pa_decode_plan(4, 32, 8, 128, 16, 16000 - 2048)
         assert which == 2
+    if case == "dynamic_split_suffix":
+        which, part = pa.pa_decode_plan(16, 16, 8, 128, 16, int(w.decode.context_lens.max()) - 1024)
+        assert which == 2 and 16 * 8 * -(-(int(w.decode.context_lens.max()) - 1024) // part) > 456
     got = run_shared(w, P, max_context_len=maxL)
     check(got, reference(w), w.pool.dtype, case)
     assert pa.pa_device_errors(clear=True) == 0
