@@ -275,7 +275,11 @@ int pa_decode_splitk_static(void* out, const void* q, const void* k_cache, const
  *                 attends to its own context_lens[s] tokens only.  0 (or fewer than 16 shared
  *                 tokens) runs plain pa_decode.  Must be <= max_blocks_per_seq * block_size.
  *  prefix_piece_tokens  keys per CTA of the prefix pass, a multiple of 128; 0 = the library's
- *                 choice (about a quarter of the SMs busy with the prefix pass).
+ *                 choice (about a quarter of the SMs busy with the prefix pass; a sixteenth when
+ *                 the suffix runs on the dynamic grid: one-pass suffixes at group size 1 or 2,
+ *                 up to 256 sequences, more (sequence, KV head) units than its resident CTAs).
+ *                 That grid's piece counter lives in the workspace's prefix region and is zeroed
+ *                 on the stream (a 4-byte cudaMemsetAsync) before the prefix pass.
  *  workspace  at least pa_decode_shared_prefix_workspace_size(...) bytes, caller-owned.
  *  Returns PA_ERR_BOUNDS for max_context_len or prefix_tokens beyond the table's capacity,
  *  PA_ERR_UNSUPPORTED for a piece that is not a multiple of 128, PA_ERR_WORKSPACE for a missing

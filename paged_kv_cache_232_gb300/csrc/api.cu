@@ -141,6 +141,8 @@ struct PrefixPartials {
     int tokens;  // the decode streams tokens [tokens, L) of each sequence
     int parts;
     const float *m, *l, *o;
+    int* dyn_counter;  // non-null: run the one-pass suffix as the dynamic grid over whole units,
+                       // taking them from this counter (zeroed on the stream before the prefix pass)
 };
 
 int decode_impl(void* out, const void* q, const void* k_cache, const void* v_cache, const int32_t* block_tables,
@@ -236,6 +238,19 @@ int decode_impl(void* out, const void* q, const void* k_cache, const void* v_cac
                 if (cudaMemsetAsync(p.dyn_counter, 0, sizeof(int), stream) != cudaSuccess) return PA_ERR_CUDA;
             }
         }
+    } else if (pf && pf->dyn_counter) {
+        // one piece per unit (the whole streamed context, written directly), handed out longest
+        // first by the dynamic grid, whose CTAs take work off the SMs the prefix pass holds
+        const int streamed = max_context_len - std::min(max_context_len, p.prefix_tokens);
+        p.part_tokens = std::max(16, (streamed + 15) / 16 * 16);
+        p.max_parts = 1;
+        p.cover_parts = 1;
+        p.dyn = 1;
+        p.dyn_units = 1;
+        p.dyn_counter = pf->dyn_counter;
+        const int resident = pa::decode_dyn_resident_ctas(dtype == PA_BF16, kernel_dim(head_dim), n_q_heads / n_kv_heads);
+        if (resident <= 0) return PA_ERR_CUDA;
+        grid = (int)std::min<int64_t>((int64_t)dev->sm_count * resident, (int64_t)units);
     } else {
         p.part_tokens = 0;
         p.max_parts = 1;
@@ -625,14 +640,41 @@ int pa_decode_shared_prefix(void* out, const void* q, const void* k_cache, const
         return PA_ERR_WORKSPACE;
     if (!aligned16(workspace)) return PA_ERR_ALIGN;
 
+    // the suffix: the dispatcher's plan over the tokens past the prefix.  A one-pass suffix at group
+    // size 1 or 2 with more units than the dynamic grid's slots (batches of up to 256 sequences)
+    // runs as that grid over whole units; its counter sits in the prefix region's control area and
+    // is zeroed now, before the prefix pass, so that the suffix still launches as the pass's
+    // programmatic dependent (GB300, mixed batch decode rows: 58.5-61.1 -> 57.0-58.6 us)
+    const int resident = pa::decode_resident_ctas(dtype == PA_BF16, kdim, G);
+    if (resident <= 0) return PA_ERR_CUDA;
+    int part = 0;
+    const int which = plan((int64_t)num_seqs * n_kv_heads, max_context_len - P, dev->sm_count, resident, block_size,
+                           G, &part);
+    int* dyn_counter = nullptr;
+    if (which == 1 && G <= 2 && num_seqs <= pa::kDynTailMaxSeqs && (max_context_len - P) / 16 + 1 <= 8000) {
+        const int dres = pa::decode_dyn_resident_ctas(dtype == PA_BF16, kdim, G);
+        if (dres <= 0) return PA_ERR_CUDA;
+        if ((int64_t)num_seqs * n_kv_heads > (int64_t)dev->sm_count * dres) {
+            // the control area at the end of the prefix region (sized for the smallest pieces),
+            // past the partials of any piece length
+            const WsLayout pw0 = pf_layout(num_seqs, n_q_heads, kdim, (P + kMinPrefixPiece - 1) / kMinPrefixPiece);
+            dyn_counter = reinterpret_cast<int*>(static_cast<char*>(workspace) + pw0.ctl_off);
+            if (cudaMemsetAsync(dyn_counter, 0, sizeof(int), static_cast<cudaStream_t>(stream)) != cudaSuccess)
+                return PA_ERR_CUDA;
+        }
+    }
+
     // the prefix pass: CTAs of (query-tile pair, KV head, piece); the default piece keeps about a
-    // quarter of the SMs on it (its CTAs run beside the suffix decode, which starts at once)
+    // quarter of the SMs on it (its CTAs run beside the suffix decode, which starts at once), a
+    // sixteenth when the suffix runs on the dynamic grid, whose CTAs take over the rest (GB300,
+    // mixed batch decode rows: 57.0 us at 512-token pieces against 58.4 at 256)
     const int tiles = (int)(((int64_t)num_seqs * G + 127) / 128);
     const int pairs = (tiles + 1) / 2;
     int piece = prefix_piece_tokens;
     if (piece == 0) {
         const int64_t per_piece = (int64_t)pairs * n_kv_heads;
-        const int64_t kp = std::max<int64_t>(1, (dev->sm_count / 4 + per_piece - 1) / per_piece);
+        const int64_t want = dyn_counter ? dev->sm_count / 16 : dev->sm_count / 4;
+        const int64_t kp = std::max<int64_t>(1, (want + per_piece - 1) / per_piece);
         piece = (int)((((int64_t)P + kp - 1) / kp + 127) / 128 * 128);
         piece = std::max(piece, 256);
     }
@@ -673,13 +715,7 @@ int pa_decode_shared_prefix(void* out, const void* q, const void* k_cache, const
     if (e == cudaErrorNotSupported) return PA_ERR_UNSUPPORTED;
     if (e != cudaSuccess) return PA_ERR_CUDA;
 
-    // the suffix: the dispatcher's plan over the tokens past the prefix
-    const int resident = pa::decode_resident_ctas(dtype == PA_BF16, kdim, G);
-    if (resident <= 0) return PA_ERR_CUDA;
-    int part = 0;
-    const int which = plan((int64_t)num_seqs * n_kv_heads, max_context_len - P, dev->sm_count, resident, block_size,
-                           G, &part);
-    const PrefixPartials pin{P, kp, pf_m, pf_l, pf_o};
+    const PrefixPartials pin{P, kp, pf_m, pf_l, pf_o, dyn_counter};
     void* ws2 = base + pw.total;
     const size_t ws2_bytes = workspace_bytes - pw.total;
     return decode_impl(out, q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens, max_context_len,

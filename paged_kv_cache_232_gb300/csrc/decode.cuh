@@ -62,7 +62,9 @@ struct DecodeParams {
     // griddepcontrol.wait (they are launched as programmatic dependents of that pass).
     int prefix_tokens;
     int pf_parts;              // 0: no shared prefix
-    int dyn;                   // split-K only: decode_kernel_dyn, gridDim.x CTAs taking pieces from *dyn_counter
+    int dyn;                   // decode_kernel_dyn: gridDim.x CTAs taking pieces from *dyn_counter (split-K, or
+                               // whole units, longest first, when dyn_units)
+    int dyn_units;             // decode_kernel_dyn over whole units (one piece each, written directly)
     int* dyn_counter;          // the next piece to hand out (zeroed before the launch)
     const float* pf_m;         // [S * Hq][pf_parts]
     const float* pf_l;
@@ -1004,6 +1006,56 @@ decode_kernel_persistent(const DecodeParams p, const __grid_constant__ CUtensorM
     asm volatile("bar.sync 2, %0;" ::"n"(C::THREADS) : "memory");
 }
 
+// decode_kernel_dyn over whole units (dyn_units): the sequences by streamed 16-token chunk count,
+// longest first (ties by index), so that the units handed out last are the shortest.  order: S
+// ints; scratch: S + 2 (part_tokens / 16 + 1) ints nothing else uses yet.  Every CTA builds the
+// same order.  All threads call this.
+__device__ __forceinline__ void dyn_unit_order(const DecodeParams& p, int cap, int* order, int* scratch) {
+    const int S = p.num_seqs, tid = threadIdx.x, lane = tid & 31;
+    const int nb = p.part_tokens / 16 + 1;
+    int* key = scratch;     // [S] chunk count
+    int* hist = key + S;    // [nb]
+    int* start = hist + nb;
+    for (int i = tid; i < nb; i += blockDim.x) hist[i] = 0;
+    for (int i = tid; i < S; i += blockDim.x) {
+        int L = __ldg(p.context_lens + i);
+        if (L < 0 || L > cap) {
+            if (blockIdx.x == 0) flag_error(p.err, PA_DEVERR_LENGTH);
+            L = L < 0 ? 0 : cap;
+        }
+        key[i] = min((streamed_tokens(p, L) + 15) >> 4, nb - 1);
+    }
+    __syncthreads();
+    for (int i = tid; i < S; i += blockDim.x) atomicAdd(&hist[key[i]], 1);
+    __syncthreads();
+    if (tid < 32) {
+        int before = 0;
+        for (int top = nb - 1; top >= 0; top -= 32) {
+            const int k = top - lane;
+            const int v = (k >= 0) ? hist[k] : 0;
+            int incl = v;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int y = __shfl_up_sync(0xffffffffu, incl, o);
+                if (lane >= o) incl += y;
+            }
+            if (k >= 0) start[k] = before + incl - v;
+            before += __shfl_sync(0xffffffffu, incl, 31);
+        }
+        __syncwarp();
+        for (int b = 0; b < S; b += 32) {
+            const int i = b + lane;
+            const int k = i < S ? key[i] : -1;
+            const unsigned same = __match_any_sync(0xffffffffu, k);
+            if (k >= 0) order[start[k] + __popc(same & ((1u << lane) - 1u))] = i;
+            __syncwarp();
+            if (k >= 0 && lane == __ffs(same) - 1) start[k] += __popc(same);
+            __syncwarp();
+        }
+    }
+    __syncthreads();
+}
+
 // decode_kernel_dyn's per-sequence layout with tail pieces: len[s] = the clamped context length,
 // cumA[s] / cumB[s] = full / tail pieces of the sequences before s (a sequence with nothing
 // streamed has one empty tail piece, which writes its output row).  All threads call this.
@@ -1118,6 +1170,8 @@ decode_kernel_dyn(const DecodeParams p, const __grid_constant__ CUtensorMap tmK,
     int* o_cumA = reinterpret_cast<int*>(smem + C::D_CUMA_OFF);
     int* o_cumB = reinterpret_cast<int*>(smem + C::D_CUMB_OFF);
     if (tail) dyn_piece_counts(p, cap, o_len, o_cumA, o_cumB);
+    int* o_order = o_cumA;  // dyn_units: the sequences longest first
+    if (p.dyn_units) dyn_unit_order(p, cap, o_order, reinterpret_cast<int*>(smem));  // (the ring: no load yet)
     const long long n_full = tail ? (long long)o_cumA[p.num_seqs] * p.n_kv_heads : 0;
     const long long total = tail ? n_full + (long long)o_cumB[p.num_seqs] * p.n_kv_heads
                                  : (long long)units * p.max_parts;
@@ -1171,6 +1225,7 @@ decode_kernel_dyn(const DecodeParams p, const __grid_constant__ CUtensorMap tmK,
                 piece = (p.max_parts - 1) - qpos;
                 s = sg / p.n_kv_heads;
                 g = sg - s * p.n_kv_heads;
+                if (p.dyn_units) s = o_order[s];  // units longest first
                 int L = __ldg(p.context_lens + s);
                 if (L < 0 || L > cap) {
                     if (piece == 0 && g == 0 && lane == 0) flag_error(p.err, PA_DEVERR_LENGTH);

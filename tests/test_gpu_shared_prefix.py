@@ -88,7 +88,8 @@ def test_prefix_zero_is_plain_decode_bitwise():
 
 
 @pytest.mark.parametrize("case", ["whole_context", "mid_block", "mid_chunk", "shorter_than_prefix",
-                                  "loose_bound", "many_tiles", "split_k_suffix", "dynamic_split_suffix"])
+                                  "loose_bound", "many_tiles", "split_k_suffix", "dynamic_split_suffix",
+                                  "dynamic_units"])
 def test_shared_prefix_edges(case):
     """whole_context: every context is exactly the prefix (no suffix).  mid_block / mid_chunk: the
     prefix the caller names ends inside a block (and inside a 16-token chunk: the remainder is
@@ -99,7 +100,9 @@ def test_shared_prefix_edges(case):
     four sequences with long suffixes, where the dispatcher splits the suffix and the split-K
     merge folds in the prefix partials.  dynamic_split_suffix: 16 sequences at group size 2 with
     long suffixes, whose split goes to the dynamic grid (tail pieces; the CTA that finishes a
-    unit merges it with the prefix partials)."""
+    unit merges it with the prefix partials).  dynamic_units: 200 sequences x 4 KV heads at group
+    size 1 and head_dim 64 with one-pass suffixes (some empty): more units than the dynamic grid's
+    slots, so the suffix runs on that grid over whole units, longest first."""
     maxL = None
     if case == "whole_context":
         w, P = shared_case(21, [512] * 9, 32), 512
@@ -116,6 +119,10 @@ def test_shared_prefix_edges(case):
         w, P = shared_case(26, lens, 32), 512
     elif case == "split_k_suffix":
         w, P = shared_case(27, [12000, 9000, 16000, 2049], 128, hq=32, hkv=8), 2048
+    elif case == "dynamic_units":
+        lens = 512 + wl.uniform_ints(wl.derive_seed(29, 1), 200, 0, 700)
+        lens[[3, 77]] = 512
+        w, P = shared_case(29, lens, 32, hq=4, hkv=4, d=64), 512
     else:
         lens = 1024 + wl.uniform_ints(wl.derive_seed(28, 1), 16, 3000, 8000)
         lens[5] = 1024
