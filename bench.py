@@ -10,7 +10,8 @@ that write plus that decode over resident inputs.
             tables + context lengths, plus the write's rows read and written and its slot
             map) / device time of the step, summed over ranks (weak scaling)
   e2e     = the same bytes / time of a step through the C ABI that also copies the step's
-            inputs host->device (pinned) and its output back
+            inputs host->device (one copy from a pinned buffer holding all of them) and its
+            output back, inside the step's events
   roofline: the dominant kernel (decode) against the measured HBM copy bandwidth
 
 --impl reference times the fp64 CPU oracle on a bounded sample of the same workload.
@@ -290,6 +291,26 @@ class _Ctx:
     pass
 
 
+class _Arena:
+    """One device buffer for a step's inputs, handed out as 256-byte aligned views, and a pinned
+    host buffer with the same layout (the end-to-end leg's single upload)."""
+
+    def __init__(self, torch, dev, capacity):
+        self.dev_buf = torch.empty(capacity, dtype=torch.uint8, device=dev)
+        self.host = torch.empty(capacity, dtype=torch.uint8).pin_memory()
+        self.used = 0
+
+    def put(self, a, torch_dtype):
+        raw = np.ascontiguousarray(a).reshape(-1).view(np.uint8)
+        off, nb = self.used, raw.size
+        assert off + nb <= self.dev_buf.numel(), "input arena too small"
+        self.used = (off + nb + 255) // 256 * 256
+        self.host[off:off + nb].numpy()[:] = raw
+        view = self.dev_buf[off:off + nb]
+        view.copy_(self.host[off:off + nb])
+        return view.view(torch_dtype).view(tuple(a.shape))
+
+
 def prepare(args, name, dev, with_host=False):
     """Device inputs and the launches of one step of workload `name` (every rank builds its own
     copy of the same batch: weak scaling)."""
@@ -303,16 +324,34 @@ def prepare(args, name, dev, with_host=False):
     p, b, wr, pre = w.pool, w.decode, w.write, w.prefill
     dt = torch.bfloat16 if p.dtype == wl.BF16 else torch.float16
 
+    # the step's inputs live in one device buffer (256-byte aligned views) mirrored by one pinned
+    # host buffer, so that the end-to-end leg uploads a step's inputs with one copy
+    cand = []
+    if b is not None:
+        cand += [b.q, b.block_tables, b.context_lens]
+    if pre is not None:
+        cand += [pre.q, pre.block_tables, pre.query_start_loc, pre.seq_lens]
+    if wr is not None:
+        cand += [wr.key, wr.value, wr.slot_mapping]
+    rope = getattr(w, "rope", None)
+    if rope is not None:
+        cand += [rope.get("positions"), rope.get("q")]
+    cap = 2 * sum(int(np.asarray(a).nbytes) + 256 for a in cand if a is not None) + (1 << 20)
+    arena = c.arena = _Arena(torch, dev, cap)
+
     def dev_bits(a):
-        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(dt).to(dev)
+        return arena.put(np.ascontiguousarray(a).view(np.int16), dt)
 
     def dev_int(a):
-        return torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+        a = np.ascontiguousarray(a)
+        return arena.put(a, torch.int64 if a.dtype == np.int64 else torch.int32)
 
-    kc, vc = dev_bits(p.k_cache), dev_bits(p.v_cache)
+    def cache_bits(a):
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(dt).to(dev)
+
+    kc, vc = cache_bits(p.k_cache), cache_bits(p.v_cache)
     stages = []   # name, launch, algorithmic amount, kind
     h_dev = []    # the step's inputs, for the end-to-end leg
-    rope = getattr(w, "rope", None)
     if rope is not None and b is not None:
         q_host = np.concatenate([b.q, pre.q]) if pre is not None else b.q
         q = dev_bits(q_host)                       # rotated in place by the fused write, then decoded
@@ -519,15 +558,16 @@ def run_ours(args, rank, world, local_rank):
         st_ms, _, _ = time_steps(c, args.steps, args.warmup, world, local_rank, flush, stream, per_stage=True)
     step_ms, value, breakdown, roof = summarize(c, st_ms, world, peaks, args.traffic, whole_ms=whole[:, 0])
 
-    # end to end through the C ABI with host buffers: inputs up, result down, every step
-    h_in = [(t, t.cpu().pin_memory()) for t in c.h_dev]
+    # end to end through the C ABI with host buffers, every step: the step's inputs go up in one
+    # copy from the pinned mirror of the input buffer, then the launches, then the result comes down
+    arena = c.arena
     h_out = torch.empty_like(c.out, device="cpu").pin_memory()
-    h2d = sum(t.numel() * t.element_size() for t, _ in h_in)
+    h2d = arena.used
     d2h = c.out.numel() * c.out.element_size()
+    up_dst, up_src = arena.dev_buf[:arena.used], arena.host[:arena.used]
 
     def e2e_step():
-        for d_, h_ in h_in:
-            d_.copy_(h_, non_blocking=True)
+        up_dst.copy_(up_src, non_blocking=True)
         for st in c.stages:
             st[1]()
         h_out.copy_(c.out, non_blocking=True)
@@ -604,7 +644,7 @@ def run_ours(args, rank, world, local_rank):
     if clocks:
         res["clocks"] = clocks
     w_head, k_head = c.w, c.k
-    del c, h_in, h_out, e2e_step
+    del c, h_out, e2e_step, up_dst, up_src, arena
     if args.all_configs and args.workload == "step256":
         # the other configurations, each timed the same way in this run (its own clocks)
         extra = argparse.Namespace(**vars(args))
