@@ -279,7 +279,8 @@ def _uniform_split_ws_bytes(S, hq, d, maxL, part):
 @pytest.mark.parametrize("dt,hq,hkv,d,bs,S,maxlen", [(wl.BF16, 16, 8, 128, 16, 96, 3000), (wl.F16, 8, 8, 64, 8, 96, 3000),
                                                    (wl.BF16, 4, 2, 256, 32, 96, 3000), (wl.F16, 16, 8, 96, 16, 96, 3000),
                                                    (wl.BF16, 16, 8, 128, 16, 300, 1200),
-                                                   (wl.BF16, 8, 8, 128, 64, 40, 5000)])
+                                                   (wl.BF16, 8, 8, 128, 64, 40, 5000),
+                                                   (wl.F16, 16, 8, 128, 128, 64, 4000)])
 def test_dynamic_split_grid(dt, hq, hkv, d, bs, S, maxlen):
     """Group size 1 or 2 with more split-K pieces than resident CTAs: one CTA per resident slot
     takes pieces from a counter in the workspace, in whatever order the CTAs free up; batches of

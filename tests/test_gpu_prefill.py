@@ -79,7 +79,7 @@ def test_prefill_ragged_chunks_full_parity(dt, hq, hkv, d):
 
 
 @pytest.mark.parametrize("dt,hq,hkv,d", [(wl.BF16, 16, 8, 128), (wl.F16, 32, 8, 128), (wl.BF16, 16, 2, 64),
-                                         (wl.BF16, 8, 8, 128), (wl.F16, 16, 8, 256)])
+                                         (wl.BF16, 8, 8, 128), (wl.F16, 16, 8, 256), (wl.F16, 8, 2, 96)])
 def test_prefill_small_m_tiles(dt, hq, hkv, d):
     """pa_prefill_chunk_small_m: chunks whose rows (query tokens x group heads) fit in 64 run as
     M = 64 MMAs (rows in TMEM lanes 0-15 of each quarter; the other lanes hold S = 0 and weight
