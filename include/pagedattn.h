@@ -135,13 +135,20 @@ int pa_rope_reshape_and_cache(void* q, const void* key, const void* value, void*
  * sequences) cuts the last partition_tokens of every context into pieces of a quarter of that
  * (at most three pieces more); a workspace sized for P = ceil(max_context_len /
  * partition_tokens) only is still accepted and runs uniform pieces:
+ *   256 bytes of control, at the start whatever the sizes: bytes 0-3 the int32 counter from
+ *       which the dynamic split-K grid's CTAs take their pieces, bytes 8-15 a tag
+ *       (0x7FC0A5177FC02C32) meaning "the counter is at zero"
  *   m [num_seqs, n_q_heads, P] float  -- per-piece max of scale*q.K (natural-log units)
  *   l [num_seqs, n_q_heads, P] float  -- per-piece sum of exp(s - m)
  *   o [num_seqs, n_q_heads, P, head_dim] float -- per-piece normalised output
- *   256 bytes of control: the counter from which the split-K grid's CTAs take their pieces; a
- *       call that splits at group size 1 or 2 zeroes it first with a 4-byte cudaMemsetAsync on
- *       its stream
- * The caller owns it; its contents between calls are unspecified (nothing needs to start at zero).
+ * The caller owns it; nothing in it needs to start at zero.  A call that runs the dynamic grid
+ * (group size 1 or 2, more pieces than resident CTAs) zeroes nothing before its launch: its merge
+ * kernel leaves the counter at 0 and the tag set, for the next call on the workspace.  A call
+ * that finds another tag (a fresh workspace, or one used for something else in between) hands
+ * the pieces out in a fixed order instead (CTA b takes pieces b, b + grid, ...), with the same
+ * results bit for bit, and leaves the tag set.  So a caller who writes into the workspace
+ * between calls must not write the tag with the counter off zero; pa_decode_shared_prefix
+ * clears the tag when it uses the counter.
  */
 size_t pa_decode_workspace_size(int num_seqs, int n_q_heads, int head_dim, int max_context_len,
                                 int partition_tokens);
@@ -278,8 +285,11 @@ int pa_decode_splitk_static(void* out, const void* q, const void* k_cache, const
  *                 choice (about a quarter of the SMs busy with the prefix pass; a sixteenth when
  *                 the suffix runs on the dynamic grid: one-pass suffixes at group size 1 or 2,
  *                 up to 256 sequences, more (sequence, KV head) units than its resident CTAs).
- *                 That grid's piece counter lives in the workspace's prefix region and is zeroed
- *                 on the stream (a 4-byte cudaMemsetAsync) before the prefix pass.
+ *                 That grid's piece counter is the workspace's first 4 bytes (the control
+ *                 region pa_decode uses); it is zeroed on the stream, with the tag beside it
+ *                 (a 16-byte cudaMemsetAsync), before the prefix pass.  A split-K suffix has
+ *                 its own counter, at the start of the suffix's part of the workspace, zeroed
+ *                 on the stream (4 bytes) before its launch.
  *  workspace  at least pa_decode_shared_prefix_workspace_size(...) bytes, caller-owned.
  *  Returns PA_ERR_BOUNDS for max_context_len or prefix_tokens beyond the table's capacity,
  *  PA_ERR_UNSUPPORTED for a piece that is not a multiple of 128, PA_ERR_WORKSPACE for a missing

@@ -109,15 +109,17 @@ struct WsLayout {
     size_t m_off, l_off, o_off, ctl_off, total;
 };
 
-// m, l, o regions, then a 256-byte control region (the dynamic grid's piece counter)
+// A 256-byte control region (the dynamic grid's piece counter at byte 0, its tag at byte 8),
+// then the m, l, o regions.  The control region sits at the start whatever the sizes, so that the
+// counter a call leaves at zero is where the next call on the workspace looks for it.
 WsLayout ws_layout(int num_seqs, int n_q_heads, int head_dim, int max_parts) {
     const size_t rows = (size_t)num_seqs * n_q_heads * max_parts;
     WsLayout w;
-    w.m_off = 0;
-    w.l_off = align256(rows * sizeof(float));
+    w.ctl_off = 0;
+    w.m_off = 256;
+    w.l_off = w.m_off + align256(rows * sizeof(float));
     w.o_off = w.l_off + align256(rows * sizeof(float));
-    w.ctl_off = w.o_off + align256(rows * head_dim * sizeof(float));
-    w.total = w.ctl_off + 256;
+    w.total = w.o_off + align256(rows * head_dim * sizeof(float));
     return w;
 }
 
@@ -205,9 +207,9 @@ int decode_impl(void* out, const void* q, const void* k_cache, const void* v_cac
         p.cover_parts = max_parts;
         grid = units * max_parts;
         if (reduce && n_q_heads / n_kv_heads <= 2) {
-            // the dynamic grid: one CTA per resident slot taking pieces from the counter (zeroed
-            // here, in the stream, before the launch), when there are more pieces than slots;
-            // with fewer it would run the static grid's CTAs plus the zeroing.  Group sizes 1 and
+            // the dynamic grid: one CTA per resident slot taking pieces from the counter, when
+            // there are more pieces than slots; with fewer it would run the static grid's CTAs
+            // plus the counter's upkeep.  Group sizes 1 and
             // 2 only: at 4 its piece loop spills registers and the static grid is faster (GB300,
             // 4 sequences of 32K tokens at 32 q / 8 KV heads: 113.7 against 105.5 us)
             const int resident = pa::decode_dyn_resident_ctas(dtype == PA_BF16, kernel_dim(head_dim),
@@ -235,7 +237,16 @@ int decode_impl(void* out, const void* q, const void* k_cache, const void* v_cac
                     p.tail_tokens = tail_tokens;
                     p.max_parts = tail_parts;
                 }
-                if (cudaMemsetAsync(p.dyn_counter, 0, sizeof(int), stream) != cudaSuccess) return PA_ERR_CUDA;
+                // The counter: after a shared-prefix pass zeroed here, in the stream, before the
+                // launch.  Otherwise no zeroing: the merge kernel leaves it at zero with the tag
+                // beside it set, for the next call on this workspace, and a call that finds no
+                // tag (a fresh or reused workspace) hands the pieces out in a fixed order instead
+                // (a 4-byte memset costs ~1.2 us of a ~55 us batch-64 decode on GB300).
+                if (pf) {
+                    if (cudaMemsetAsync(p.dyn_counter, 0, sizeof(int), stream) != cudaSuccess) return PA_ERR_CUDA;
+                } else {
+                    p.dyn_tag = reinterpret_cast<unsigned long long*>(reinterpret_cast<char*>(p.dyn_counter) + 8);
+                }
             }
         }
     } else if (pf && pf->dyn_counter) {
@@ -277,6 +288,9 @@ int decode_impl(void* out, const void* q, const void* k_cache, const void* v_cac
     if ((st = encode_cache_map(&tv, v_cache, dtype, num_blocks, block_size, n_kv_heads, head_dim)) != PA_OK) return st;
     cudaError_t e = pa::launch_decode(dtype == PA_BF16, kernel_dim(head_dim), n_q_heads / n_kv_heads, p, tk, tv, grid, reduce,
                                       stream);
+    // a piece grid whose merge did not launch has left the counter wherever it stopped: clear the
+    // tag, so that the next call does not trust it
+    if (e != cudaSuccess && p.dyn_tag) (void)cudaMemsetAsync(p.dyn_tag, 0, sizeof(unsigned long long), stream);
     return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 
@@ -655,11 +669,13 @@ int pa_decode_shared_prefix(void* out, const void* q, const void* k_cache, const
         const int dres = pa::decode_dyn_resident_ctas(dtype == PA_BF16, kdim, G);
         if (dres <= 0) return PA_ERR_CUDA;
         if ((int64_t)num_seqs * n_kv_heads > (int64_t)dev->sm_count * dres) {
-            // the control area at the end of the prefix region (sized for the smallest pieces),
-            // past the partials of any piece length
+            // the control area at the start of the prefix region (and of the workspace), before
+            // the partials of any piece length; the tag beside the counter is cleared with it, since
+            // this grid leaves the counter where its claims stopped (the next pa_decode on this
+            // workspace then hands its pieces out in the fixed order)
             const WsLayout pw0 = pf_layout(num_seqs, n_q_heads, kdim, (P + kMinPrefixPiece - 1) / kMinPrefixPiece);
             dyn_counter = reinterpret_cast<int*>(static_cast<char*>(workspace) + pw0.ctl_off);
-            if (cudaMemsetAsync(dyn_counter, 0, sizeof(int), static_cast<cudaStream_t>(stream)) != cudaSuccess)
+            if (cudaMemsetAsync(dyn_counter, 0, 16, static_cast<cudaStream_t>(stream)) != cudaSuccess)
                 return PA_ERR_CUDA;
         }
     }

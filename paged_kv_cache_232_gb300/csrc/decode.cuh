@@ -65,11 +65,19 @@ struct DecodeParams {
     int dyn;                   // decode_kernel_dyn: gridDim.x CTAs taking pieces from *dyn_counter (split-K, or
                                // whole units, longest first, when dyn_units)
     int dyn_units;             // decode_kernel_dyn over whole units (one piece each, written directly)
-    int* dyn_counter;          // the next piece to hand out (zeroed before the launch)
+    int* dyn_counter;          // the next piece to hand out
+    // non-null: the counter is valid only while *dyn_tag == kDynTag, which the split-K merge
+    // restores at its end (counter 0, tag set) for the next call; with another value the CTAs
+    // take the pieces in a fixed order.  Null: the counter was zeroed before the launch.
+    unsigned long long* dyn_tag;
     const float* pf_m;         // [S * Hq][pf_parts]
     const float* pf_l;
     const float* pf_o;         // [S * Hq][pf_parts][D]
 };
+
+// The dynamic grid's "counter is at zero" mark in the workspace's control region: the bit
+// patterns of two quiet NaNs, which no float the kernels store there takes.
+constexpr unsigned long long kDynTag = 0x7FC0A5177FC02C32ull;
 
 // Tokens of a sequence of context L the decode kernels stream: the part past the shared prefix.
 __device__ __forceinline__ int streamed_tokens(const DecodeParams& p, int L) { return max(L - p.prefix_tokens, 0); }
@@ -1159,7 +1167,11 @@ decode_kernel_dyn(const DecodeParams p, const __grid_constant__ CUtensorMap tmK,
     // producer takes its first item now, and every CTA prefetches its share of the table lines
     // (tables of up to 4 MB)
     int first = 0;
-    if (warp == C::NCW && lane == 0) first = atomicAdd(p.dyn_counter, 1);
+    bool fixed = false;  // the counter is not known to start at zero: CTA b takes items b, b + grid, ...
+    if (warp == C::NCW && lane == 0) {
+        first = atomicAdd(p.dyn_counter, 1);
+        if (p.dyn_tag) fixed = __ldcg(p.dyn_tag) != kDynTag;
+    }
     {
         long long lines = ((long long)p.num_seqs * p.max_blocks_per_seq * 4 + 127) / 128;
         if (lines > 32768) lines = 0;
@@ -1188,9 +1200,11 @@ decode_kernel_dyn(const DecodeParams p, const __grid_constant__ CUtensorMap tmK,
         uint32_t fused = 0, fpar = 0;          // per stage: filled before; parity of its fill count
         int ring_next = 0, nq = 0;             // ring index of the next chunk; items published
         bool ok = true;
-        for (bool claimed = true; ok; claimed = false) {
+        int n_claims = 0;
+        for (bool claimed = true; ok; claimed = false, ++n_claims) {
             int item = first;
-            if (lane == 0 && !claimed) item = atomicAdd(p.dyn_counter, 1);
+            if (lane == 0 && !claimed && !fixed) item = atomicAdd(p.dyn_counter, 1);
+            if (fixed) item = (int)blockIdx.x + n_claims * (int)gridDim.x;
             item = __shfl_sync(0xffffffffu, item, 0);
             const bool end = (long long)item >= total;
             int s = -1, g = 0, piece = 0, t_begin = 0, t_end = 0, n_parts = 0;
@@ -1503,6 +1517,12 @@ __global__ void __launch_bounds__(256, 2) splitk_merge_kernel(const DecodeParams
     constexpr int PRE = 64 / CW;  // pieces whose columns are loaded up front: 32, 16 or 8
     constexpr float kLn2 = 0.69314718055994531f;  // the prefix partials' m is base 2
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    // once the dynamic grid has ended: its counter back to zero, and marked so, for the next call
+    if (p.dyn_tag && blockIdx.x == 0 && threadIdx.x == 0) {
+        asm volatile("griddepcontrol.wait;" ::: "memory");
+        *p.dyn_counter = 0;
+        *p.dyn_tag = kDynTag;
+    }
     const int row = blockIdx.x * (blockDim.x >> 5) + warp;  // s * Hq + h
     if (row >= p.num_seqs * p.n_q_heads) return;
     const int s = row / p.n_q_heads;

@@ -170,7 +170,8 @@ def test_block_relabelling_is_bitwise_invariant():
 
 def test_splitk_intermediates_match_oracle_pieces():
     """fp32 per-piece max, exp-sum and normalised output, read back from the workspace
-    (layout of pa_decode_workspace_size), against the oracle's fp64 pieces at 1e-5."""
+    (layout of pa_decode_workspace_size: the control region, then m, l, o), against the oracle's
+    fp64 pieces at 1e-5.  Eight units of at most six pieces: the static split-K grid."""
     w = wl.build_workload("ws", 9, dtype=wl.BF16, n_q_heads=8, n_kv_heads=2, head_dim=128,
                           decode_lens=[1000, 256, 1300, 3], max_blocks_per_seq=96)
     p, b = w.pool, w.decode
@@ -179,7 +180,7 @@ def test_splitk_intermediates_match_oracle_pieces():
     S, hq, D, P = 4, 8, 128, -(-1300 // 256)
     rows = S * hq * P
     al = lambda x: (x + 255) // 256 * 256
-    raw = d.ws.cpu().numpy()
+    raw = d.ws.cpu().numpy()[256:]    # past the 256-byte control region
     gm = raw[: rows * 4].view(np.float32).reshape(S, hq, P)
     gl = raw[al(rows * 4): al(rows * 4) + rows * 4].view(np.float32).reshape(S, hq, P)
     go = raw[2 * al(rows * 4): 2 * al(rows * 4) + rows * D * 4].view(np.float32).reshape(S, hq, P, D)
@@ -276,6 +277,38 @@ def _uniform_split_ws_bytes(S, hq, d, maxL, part):
     return 2 * a(rows * 4) + a(rows * kd * 4) + 256
 
 
+DYN_TAG = 0x7FC0A5177FC02C32   # the control region's "counter at zero" mark (two quiet-NaN floats)
+
+
+def assert_counter_armed(ws):
+    """After a call on the dynamic grid: the counter (bytes 0-3) at zero, the tag (8-15) set."""
+    ctl = ws[:16].cpu().numpy()
+    assert int(ctl[0:4].view(np.int32)[0]) == 0
+    assert int(ctl[8:16].view(np.uint64)[0]) == DYN_TAG
+
+
+def test_dynamic_grid_workspace_reused_across_sizes():
+    """One workspace for successive batches of other sizes (a decode loop whose contexts grow and
+    whose batch changes): the control region sits at the workspace's start for every size, so the
+    counter each call leaves at zero is the one the next call takes pieces from; every call
+    against the oracle, and the counter left at zero after each."""
+    ws = torch.full((64 << 20,), 0x5A, dtype=torch.uint8, device="cuda")
+    pa.pa_device_errors(clear=True)
+    for i, (S, maxlen, part) in enumerate(((96, 3000, 256), (64, 2048, 512), (130, 1500, 256), (96, 3100, 256))):
+        lens = wl.uniform_ints(wl.derive_seed(91, i), S, 1, maxlen)
+        lens[7] = maxlen
+        w = wl.build_workload("dynre", 91 + i, dtype=wl.BF16, n_q_heads=16, n_kv_heads=8, head_dim=128,
+                              block_size=16, decode_lens=lens.tolist())
+        dev = Dev(w)
+        assert pa.pa_decode_workspace_size(S, 16, 128, dev.maxL, part) <= ws.numel()
+        out = torch.full_like(dev.q, float("nan"))
+        pa.pa_decode_splitk(out, dev.q, dev.kc, dev.vc, dev.bt, dev.cl, dev.maxL, dev.scale, ws, part)
+        torch.cuda.synchronize()
+        check(bits_of(out), oracle_decode(w), wl.BF16, f"reused workspace, batch {i}")
+        assert_counter_armed(ws)
+    assert pa.pa_device_errors(clear=True) == 0
+
+
 @pytest.mark.parametrize("dt,hq,hkv,d,bs,S,maxlen", [(wl.BF16, 16, 8, 128, 16, 96, 3000), (wl.F16, 8, 8, 64, 8, 96, 3000),
                                                    (wl.BF16, 4, 2, 256, 32, 96, 3000), (wl.F16, 16, 8, 96, 16, 96, 3000),
                                                    (wl.BF16, 16, 8, 128, 16, 300, 1200),
@@ -286,9 +319,11 @@ def test_dynamic_split_grid(dt, hq, hkv, d, bs, S, maxlen):
     takes pieces from a counter in the workspace, in whatever order the CTAs free up; batches of
     up to 256 sequences cut the last piece-length of every context into quarter pieces (tail
     pieces), larger ones (300) keep uniform pieces, as does a workspace sized without room for the
-    tail pieces.  A piece's arithmetic does not depend on which CTA takes it, so repeated calls
-    agree bit for bit; the counter is zeroed by the call (the workspace starts filled with 0x7f
-    bytes); against the oracle, with empty and one-token contexts among long ones."""
+    tail pieces.  The workspace starts filled with 0x7f bytes, so the first call finds no tag
+    beside the counter and hands the pieces out in the fixed order (CTA b: pieces b, b + grid, ...);
+    its merge leaves the counter at 0 and the tag set, so the later calls take pieces from the
+    counter.  A piece's arithmetic does not depend on which CTA takes it, so all calls agree bit for
+    bit; against the oracle, with empty and one-token contexts among long ones."""
     lens = wl.uniform_ints(wl.derive_seed(77, hq + d + S), S, 1, maxlen)
     lens[[3, 20, 21]] = 0
     lens[[10, 30]] = 1
@@ -313,6 +348,7 @@ def test_dynamic_split_grid(dt, hq, hkv, d, bs, S, maxlen):
                 first = got
                 check(got, ref, dt, f"dynamic split grid {part}")
             assert np.array_equal(got, first)
+            assert_counter_armed(ws)
     check(dev.run("auto"), ref, dt, "dispatcher")
     assert pa.pa_device_errors(clear=True) == 0
 

@@ -138,6 +138,48 @@ def test_shared_prefix_edges(case):
     assert pa.pa_device_errors(clear=True) == 0
 
 
+def test_workspace_shared_with_split_decode():
+    """One workspace for split-K decode calls and shared-prefix calls in turn.  The split-K calls
+    run the dynamic grid (200 sequences x 4 KV heads, 256-token pieces), whose merge leaves the
+    counter at the workspace's start at zero with its tag set; the shared-prefix call runs its
+    suffix on the dynamic grid over whole units with a counter at the same place, zeroed with the
+    tag before its prefix pass and left where its claims stopped, so the next split-K call finds
+    no tag and takes the fixed order.  Every split-K call gives the same bits (and the oracle's
+    values), the shared-prefix call the oracle's values."""
+    lens = 512 + wl.uniform_ints(wl.derive_seed(29, 1), 200, 0, 700)
+    lens[[3, 77]] = 512
+    w = shared_case(29, lens, 32, hq=4, hkv=4, d=64)
+    kc, vc, q, bt, cl = dev_inputs(w)
+    b = w.decode
+    maxL = int(b.context_lens.max())
+    nbytes = max(pa.pa_decode_shared_prefix_workspace_size(200, 4, 64, maxL, 512),
+                 pa.pa_decode_workspace_size(200, 4, 64, maxL, 256))
+    ws = torch.full((nbytes,), 0x7F, dtype=torch.uint8, device="cuda")
+
+    def split():
+        out = torch.full_like(q, float("nan"))
+        pa.pa_decode_splitk(out, q, kc, vc, bt, cl, maxL, b.scale, ws, 256)
+        torch.cuda.synchronize()
+        return bits_of(out)
+
+    def tag():
+        return int(ws[8:16].cpu().numpy().view(np.uint64)[0])
+
+    ref = reference(w)
+    first = split()                     # no tag yet: the fixed order
+    check(first, ref, wl.BF16, "split-K, fresh workspace")
+    assert tag() == 0x7FC0A5177FC02C32
+    assert np.array_equal(split(), first)   # from the counter
+    out = torch.full_like(q, float("nan"))
+    pa.pa_decode_shared_prefix(out, q, kc, vc, bt, cl, maxL, b.scale, 512, ws)
+    torch.cuda.synchronize()
+    check(bits_of(out), ref, wl.BF16, "shared prefix on the split-K workspace")
+    assert tag() == 0
+    assert np.array_equal(split(), first)   # the fixed order again
+    assert np.array_equal(split(), first)   # from the counter
+    assert pa.pa_device_errors(clear=True) == 0
+
+
 @pytest.mark.parametrize("dt,hq,hkv,d,bs", [(wl.BF16, 8, 8, 128, 16), (wl.F16, 32, 8, 128, 16), (wl.BF16, 64, 8, 64, 16),
                                             (wl.F16, 16, 8, 96, 8), (wl.BF16, 8, 4, 256, 32), (wl.BF16, 16, 4, 256, 16),
                                             (wl.F16, 4, 4, 64, 128)])
