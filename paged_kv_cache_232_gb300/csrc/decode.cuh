@@ -348,9 +348,14 @@ __device__ __forceinline__ float head_sum(float x) {
 }
 
 // One 16-token chunk of K and V (the ring stage at kt, nvalid tokens valid): q.K for the G
-// heads, the online-softmax update of (m_run, l_run) and o, and P.V into o.  Shared by
-// decode_kernel and decode_kernel_persistent; the caller waits for the stage and releases it.
-template <int D, int G, bool BF16>
+// heads, the online-softmax update of (m_run, l_run) and o, and P.V into o.  Shared by the three
+// decode kernels; the caller waits for the stage and releases it.  PACKED: the products on packed
+// fp32 pairs (fma.rn.f32x2, half the FMA instructions: q.K sums the even and the odd columns of a
+// 16-byte chunk apart and adds the two at the end; P.V updates two columns per instruction).
+// GB300: 4 x 32K tokens at 32 q / 8 KV heads 104.4 -> 96.2 us, 64 x U[100,2048] at 16 / 8 heads
+// 53.8 -> 53.2; the persistent one-pass grid (batch 256) keeps the scalar form (164.9 against
+// 166.3 us packed).
+template <int D, int G, bool BF16, bool PACKED = true>
 __device__ __forceinline__ void consume_chunk(const uint32_t kt, const int nvalid,
                                               const float (&qf)[G][DecodeCfg<D, G, BF16>::CPL][8],
                                               const int (&chunk_col)[DecodeCfg<D, G, BF16>::CPL], const int lane,
@@ -368,16 +373,35 @@ __device__ __forceinline__ void consume_chunk(const uint32_t kt, const int nvali
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
         const int t = tg + 4 * i;
+        float2 a2[G];  // PACKED: the even and the odd columns apart, added at the end
+#pragma unroll
+        for (int h = 0; h < G; ++h) a2[h] = make_float2(0.f, 0.f);
 #pragma unroll
         for (int j = 0; j < C::CPL; ++j) {
             const int half = chunk_col[j] >> 6, c = (chunk_col[j] >> 3) & 7;
-            uint4 raw = lds128(kt + half * C::SLAB_BYTES + swz128(t, c));
-            float kf[8];
-            unpack8<BF16>(raw, kf);
+            const uint4 raw = lds128(kt + half * C::SLAB_BYTES + swz128(t, c));
+            if constexpr (PACKED) {
+                const float2 k0 = F16x2<BF16>::unpack(raw.x), k1 = F16x2<BF16>::unpack(raw.y);
+                const float2 k2 = F16x2<BF16>::unpack(raw.z), k3 = F16x2<BF16>::unpack(raw.w);
 #pragma unroll
-            for (int h = 0; h < G; ++h)
+                for (int h = 0; h < G; ++h) {
+                    a2[h] = ffma2(make_float2(qf[h][j][0], qf[h][j][1]), k0, a2[h]);
+                    a2[h] = ffma2(make_float2(qf[h][j][2], qf[h][j][3]), k1, a2[h]);
+                    a2[h] = ffma2(make_float2(qf[h][j][4], qf[h][j][5]), k2, a2[h]);
+                    a2[h] = ffma2(make_float2(qf[h][j][6], qf[h][j][7]), k3, a2[h]);
+                }
+            } else {
+                float kf[8];
+                unpack8<BF16>(raw, kf);
 #pragma unroll
-                for (int e = 0; e < 8; ++e) acc[h * 4 + i] = fmaf(qf[h][j][e], kf[e], acc[h * 4 + i]);
+                for (int h = 0; h < G; ++h)
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) acc[h * 4 + i] = fmaf(qf[h][j][e], kf[e], acc[h * 4 + i]);
+            }
+        }
+        if constexpr (PACKED) {
+#pragma unroll
+            for (int h = 0; h < G; ++h) acc[h * 4 + i] = a2[h].x + a2[h].y;
         }
     }
     const int base = transpose_reduce<G>(acc, lane);
@@ -429,14 +453,30 @@ __device__ __forceinline__ void consume_chunk(const uint32_t kt, const int nvali
     for (int i = 0; i < C::TPL; ++i) {
         const int t = tgp + C::TGP * i;
         if (t < nvalid) {
-            uint4 raw = lds128(vt + half * C::SLAB_BYTES + swz128(t, c));
-            float vf[8];
-            unpack8<BF16>(raw, vf);
+            const uint4 raw = lds128(vt + half * C::SLAB_BYTES + swz128(t, c));
+            if constexpr (PACKED) {
+                const float2 v0 = F16x2<BF16>::unpack(raw.x), v1 = F16x2<BF16>::unpack(raw.y);
+                const float2 v2 = F16x2<BF16>::unpack(raw.z), v3 = F16x2<BF16>::unpack(raw.w);
 #pragma unroll
-            for (int h = 0; h < G; ++h) {
-                const float pr = pw[t * G + h];
+                for (int h = 0; h < G; ++h) {
+                    const float pr = pw[t * G + h];
+                    const float2 p2 = make_float2(pr, pr);
+                    const float2 r0 = ffma2(p2, v0, make_float2(o[h][0], o[h][1]));
+                    const float2 r1 = ffma2(p2, v1, make_float2(o[h][2], o[h][3]));
+                    const float2 r2 = ffma2(p2, v2, make_float2(o[h][4], o[h][5]));
+                    const float2 r3 = ffma2(p2, v3, make_float2(o[h][6], o[h][7]));
+                    o[h][0] = r0.x; o[h][1] = r0.y; o[h][2] = r1.x; o[h][3] = r1.y;
+                    o[h][4] = r2.x; o[h][5] = r2.y; o[h][6] = r3.x; o[h][7] = r3.y;
+                }
+            } else {
+                float vf[8];
+                unpack8<BF16>(raw, vf);
 #pragma unroll
-                for (int e = 0; e < 8; ++e) o[h][e] = fmaf(pr, vf[e], o[h][e]);
+                for (int h = 0; h < G; ++h) {
+                    const float pr = pw[t * G + h];
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) o[h][e] = fmaf(pr, vf[e], o[h][e]);
+                }
             }
         }
     }
@@ -938,7 +978,7 @@ decode_kernel_persistent(const DecodeParams p, const __grid_constant__ CUtensorM
             if (!__all_sync(0xffffffffu, arrived)) { ok = false; break; }  // leave the loop warp-uniformly
             const uint32_t kt = ring + st * C::STAGE_BYTES;
             const int nvalid = min(C::BS, L - t0 - b * C::BS);
-            consume_chunk<D, G, BF16>(kt, nvalid, qf, chunk_col, lane, my_h, rep, pw, aw, m_run, l_run, o);
+            consume_chunk<D, G, BF16, false>(kt, nvalid, qf, chunk_col, lane, my_h, rep, pw, aw, m_run, l_run, o);
             __syncwarp();
             if (lane == 0) mbar_arrive(bar_empty + 8 * st);
         }
