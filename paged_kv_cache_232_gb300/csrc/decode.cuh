@@ -98,16 +98,52 @@ __device__ __forceinline__ int pieces_of(const DecodeParams& p, int L) {
 }
 
 // Folds the shared-prefix partials of output row `row` into a merge in progress: raises the
-// running maximum M (base 2) first (pass 0), then adds each partial's weight l_k 2^(m_k - M) to
-// the sum and its output (normalised) times that weight (pass 1).  Partials with l = 0 (no key
-// of the piece visible) are skipped.
-__device__ __forceinline__ float prefix_max(const DecodeParams& p, size_t row, float M) {
+// running maximum M (base 2) first (prefix_max), then adds each partial's weight l_k 2^(m_k - M)
+// to the sum and its output (normalised) times that weight (prefix_add).  Partials with l = 0 (no
+// key of the piece visible) are skipped.  Up to kPfFast pieces, prefix_load reads all of a row's
+// l, m and output pair at once beforehand (one round trip to L2 for the fold, not two per piece);
+// with more pieces the two passes read them piece by piece.  Same arithmetic either way.
+constexpr int kPfFast = 4;
+struct PrefixRow {
+    int n;  // pieces held; 0: read piece by piece
+    float l[kPfFast], m[kPfFast];
+    float2 o[kPfFast];
+};
+__device__ __forceinline__ void prefix_load(const DecodeParams& p, size_t row, int d, int D, PrefixRow& r) {
+    r.n = p.pf_parts <= kPfFast ? p.pf_parts : 0;
+#pragma unroll
+    for (int k = 0; k < kPfFast; ++k)
+        if (k < r.n) {
+            const size_t i = row * p.pf_parts + k;
+            r.l[k] = p.pf_l[i];
+            r.m[k] = p.pf_m[i];
+            r.o[k] = *reinterpret_cast<const float2*>(p.pf_o + i * D + d);
+        }
+}
+__device__ __forceinline__ float prefix_max(const DecodeParams& p, const PrefixRow& r, size_t row, float M) {
+    if (r.n > 0) {
+#pragma unroll
+        for (int k = 0; k < kPfFast; ++k)
+            if (k < r.n && r.l[k] > 0.f) M = fmaxf(M, r.m[k]);
+        return M;
+    }
     for (int k = 0; k < p.pf_parts; ++k)
         if (p.pf_l[row * p.pf_parts + k] > 0.f) M = fmaxf(M, p.pf_m[row * p.pf_parts + k]);
     return M;
 }
-__device__ __forceinline__ void prefix_add(const DecodeParams& p, size_t row, int d, int D, float M, float& Lsum,
-                                           float& o0, float& o1) {
+__device__ __forceinline__ void prefix_add(const DecodeParams& p, const PrefixRow& r, size_t row, int d, int D,
+                                           float M, float& Lsum, float& o0, float& o1) {
+    if (r.n > 0) {
+#pragma unroll
+        for (int k = 0; k < kPfFast; ++k)
+            if (k < r.n && r.l[k] > 0.f) {
+                const float wt = r.l[k] * ex2(r.m[k] - M);
+                Lsum += wt;
+                o0 = fmaf(r.o[k].x, wt, o0);
+                o1 = fmaf(r.o[k].y, wt, o1);
+            }
+        return;
+    }
     for (int k = 0; k < p.pf_parts; ++k) {
         const size_t i = row * p.pf_parts + k;
         const float lk = p.pf_l[i];
@@ -740,7 +776,11 @@ decode_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmK, con
         float M = -INFINITY;
 #pragma unroll
         for (int w = 0; w < C::NCW; ++w) M = fmaxf(M, mm[w * G + h]);
-        if (fold) M = prefix_max(p, row, M);
+        PrefixRow pfr;
+        if (fold) {
+            prefix_load(p, row, d, D, pfr);
+            M = prefix_max(p, pfr, row, M);
+        }
         float Lsum = 0.f, o0 = 0.f, o1 = 0.f;
         if (M != -INFINITY) {
 #pragma unroll
@@ -750,7 +790,7 @@ decode_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmK, con
                 o0 = fmaf(mo[(w * G + h) * D + d], wt, o0);
                 o1 = fmaf(mo[(w * G + h) * D + d + 1], wt, o1);
             }
-            if (fold) prefix_add(p, row, d, D, M, Lsum, o0, o1);
+            if (fold) prefix_add(p, pfr, row, d, D, M, Lsum, o0, o1);
         }
         const float inv = (Lsum > 0.f) ? 1.f / Lsum : 0.f;
         if (direct) {
@@ -1029,7 +1069,11 @@ decode_kernel_persistent(const DecodeParams p, const __grid_constant__ CUtensorM
             float M = -INFINITY;
 #pragma unroll
             for (int w = 0; w < C::NCW; ++w) M = fmaxf(M, mm[w * G + h]);
-            if (p.pf_parts > 0) M = prefix_max(p, row, M);
+            PrefixRow pfr;
+            if (p.pf_parts > 0) {
+                prefix_load(p, row, d, D, pfr);
+                M = prefix_max(p, pfr, row, M);
+            }
             float Lsum = 0.f, o0 = 0.f, o1 = 0.f;
             if (M != -INFINITY) {
 #pragma unroll
@@ -1039,7 +1083,7 @@ decode_kernel_persistent(const DecodeParams p, const __grid_constant__ CUtensorM
                     o0 = fmaf(mo[(w * G + h) * D + d], wt, o0);
                     o1 = fmaf(mo[(w * G + h) * D + d + 1], wt, o1);
                 }
-                if (p.pf_parts > 0) prefix_add(p, row, d, D, M, Lsum, o0, o1);
+                if (p.pf_parts > 0) prefix_add(p, pfr, row, d, D, M, Lsum, o0, o1);
             }
             const float inv = (Lsum > 0.f) ? 1.f / Lsum : 0.f;
             if (d < p.hd)
@@ -1485,7 +1529,11 @@ decode_kernel_dyn(const DecodeParams p, const __grid_constant__ CUtensorMap tmK,
             float M = -INFINITY;
 #pragma unroll
             for (int w = 0; w < C::NCW; ++w) M = fmaxf(M, mm[w * G + h]);
-            if (fold) M = prefix_max(p, row, M);
+            PrefixRow pfr;
+            if (fold) {
+                prefix_load(p, row, d, D, pfr);
+                M = prefix_max(p, pfr, row, M);
+            }
             float Lsum = 0.f, o0 = 0.f, o1 = 0.f;
             if (M != -INFINITY) {
 #pragma unroll
@@ -1495,7 +1543,7 @@ decode_kernel_dyn(const DecodeParams p, const __grid_constant__ CUtensorMap tmK,
                     o0 = fmaf(mo[(w * G + h) * D + d], wt, o0);
                     o1 = fmaf(mo[(w * G + h) * D + d + 1], wt, o1);
                 }
-                if (fold) prefix_add(p, row, d, D, M, Lsum, o0, o1);
+                if (fold) prefix_add(p, pfr, row, d, D, M, Lsum, o0, o1);
             }
             const float inv = (Lsum > 0.f) ? 1.f / Lsum : 0.f;
             if (direct) {
