@@ -185,6 +185,32 @@ int pa_decode(void* out, const void* q, const void* k_cache, const void* v_cache
               int dtype, void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * pa_decode_write -- one decode step's KV write and decode in one call: row s of key / value
+ * (the step's new token of sequence s, [num_seqs, n_kv_heads, head_dim]) is written into slot
+ * slot_mapping[s] of k_cache / v_cache (-1: no row), then every sequence is decoded over its
+ * context_lens[s] tokens, that row included.  Results (cache and out) are those of
+ * pa_reshape_and_cache(key, value, ..., slot_mapping, num_seqs, ...) followed by pa_decode.
+ * Source: mini_engine, "Custom CUDA kernels" (the KV-cache write and the paged decode of a step)
+ * and "Roadmap" (folding small per-step kernels together); miniserve, "Engine" (slot mapping).
+ *
+ *  Arguments as pa_decode, plus key, value ([num_seqs, n_kv_heads, head_dim], dtype, 16-byte
+ *  aligned) and slot_mapping ([num_seqs] int64 on the device, -1 = none).  slot_mapping[s], when
+ *  not -1, must be the slot of token context_lens[s] - 1 of sequence s (block_tables[s][(L - 1) /
+ *  block_size] * block_size + (L - 1) % block_size): on the persistent one-pass grid (batches of
+ *  two waves and more at group size 1 or 2) the CTA that decodes (s, g) writes head g's part of
+ *  the row itself just before loading the 16-token chunk that holds that token, so no separate
+ *  write launch precedes the decode; a slot elsewhere, or outside [0, num_blocks * block_size),
+ *  sets PA_DEVERR_SLOT (an outside slot writes nothing).  Every other grid launches the KV-write
+ *  kernel first.  Returns as pa_decode, plus PA_ERR_NULL / PA_ERR_ALIGN for key, value or
+ *  slot_mapping.
+ */
+int pa_decode_write(void* out, const void* q, void* k_cache, void* v_cache, const int32_t* block_tables,
+                    int max_blocks_per_seq, const int32_t* context_lens, int max_context_len, int num_seqs,
+                    int n_q_heads, int n_kv_heads, int head_dim, int block_size, int64_t num_blocks, float scale,
+                    int dtype, const void* key, const void* value, const int64_t* slot_mapping, void* workspace,
+                    size_t workspace_bytes, void* stream);
+
+/*
  * The dispatcher's decision for these sizes on the current device, without
  * launching: returns 1 for the one-pass kernel, 2 for split-K, or a negative
  * status (PA_ERR_SHAPE / PA_ERR_UNSUPPORTED as pa_decode, PA_ERR_CUDA).

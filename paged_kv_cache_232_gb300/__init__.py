@@ -24,7 +24,7 @@ EXPORTED = (
     "pa_reshape_and_cache", "pa_decode_workspace_size", "pa_decode", "pa_decode_plan", "pa_decode_v1",
     "pa_decode_splitk", "pa_prefill_chunk", "pa_device_errors", "pa_status_string", "pa_version",
     "pa_decode_splitk_static", "pa_rope_table", "pa_rope_reshape_and_cache", "pa_decode_shared_prefix",
-    "pa_decode_shared_prefix_workspace_size", "pa_prefill_chunk_small_m",
+    "pa_decode_shared_prefix_workspace_size", "pa_prefill_chunk_small_m", "pa_decode_write",
 )
 STATIC_SCRATCH_BYTES = 16 << 20
 
@@ -66,6 +66,9 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
     L.pa_decode.restype = i32
     L.pa_decode_plan.argtypes = [i32, i32, i32, i32, i32, i32, i32, ctypes.POINTER(i32)]
     L.pa_decode_plan.restype = i32
+    L.pa_decode_write.argtypes = [vp, vp, vp, vp, vp, i32, vp, i32, i32, i32, i32, i32, i32, i64, f32, i32, vp, vp, vp,
+                                  vp, sz, vp]
+    L.pa_decode_write.restype = i32
     L.pa_decode_v1.argtypes = [vp, vp, vp, vp, vp, i32, vp, i32, i32, i32, i32, i32, i64, f32, i32, vp]
     L.pa_decode_v1.restype = i32
     L.pa_decode_splitk.argtypes = [vp, vp, vp, vp, vp, i32, vp, i32, i32, i32, i32, i32, i32, i64, f32, i32, i32, vp,
@@ -225,6 +228,25 @@ def pa_decode(out, q, k_cache, v_cache, block_tables, context_lens, max_context_
     st = load().pa_decode(po, pq, pk, pv, pbt, mb, pcl, int(max_context_len), S, hq, hkv, d, bs, nb, float(scale), dt,
                           wp, wb, _stream(stream, q.device))
     _check(st, "pa_decode")
+
+
+def pa_decode_write(out, q, k_cache, v_cache, block_tables, context_lens, max_context_len: int, scale: float,
+                    key, value, slot_mapping, workspace=None, stream=None) -> None:
+    """One decode step: key / value [S, Hkv, D] (sequence s's new token) into the caches at
+    slot_mapping [S] (int64, -1 skips; otherwise the slot of token context_lens[s] - 1), then the
+    decode as pa_decode, over contexts that include those rows."""
+    torch = _torch()
+    dt, nb, bs, hkv, d, S, hq, mb, (po, pq, pk, pv, pbt, pcl) = _decode_common(out, q, k_cache, v_cache, block_tables,
+                                                                             context_lens)
+    if tuple(key.shape) != (S, hkv, d) or tuple(value.shape) != (S, hkv, d):
+        raise ValueError("key / value must be [num_seqs, n_kv_heads, head_dim]")
+    if tuple(slot_mapping.shape) != (S,):
+        raise ValueError("slot_mapping must hold one slot per sequence")
+    wp, wb = (workspace.data_ptr(), workspace.numel() * workspace.element_size()) if workspace is not None else (None, 0)
+    st = load().pa_decode_write(po, pq, pk, pv, pbt, mb, pcl, int(max_context_len), S, hq, hkv, d, bs, nb, float(scale),
+                                dt, _dev(key, "key", q.dtype), _dev(value, "value", q.dtype),
+                                _dev(slot_mapping, "slot_mapping", torch.int64), wp, wb, _stream(stream, q.device))
+    _check(st, "pa_decode_write")
 
 
 def pa_decode_v1(out, q, k_cache, v_cache, block_tables, context_lens, scale: float, stream=None) -> None:

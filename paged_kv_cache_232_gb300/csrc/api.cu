@@ -147,11 +147,33 @@ struct PrefixPartials {
                        // taking them from this counter (zeroed on the stream before the prefix pass)
 };
 
+// pa_decode_write: one new K/V row per sequence (row s of key / value) for slot_mapping[s].
+struct NewRows {
+    const void* key;
+    const void* value;
+    const int64_t* slot_mapping;
+};
+
+// The KV-write kernel over num_tokens rows of row_vecs 16-byte chunks.
+int launch_kv_write(const void* key, const void* value, void* k_cache, void* v_cache, const int64_t* slot_mapping,
+                    int64_t num_tokens, int row_vecs, int64_t num_blocks, int block_size, const DeviceState* dev,
+                    cudaStream_t stream) {
+    // one thread per 16-byte chunk of the (K row ++ V row) pair, at most 512 (then each loops)
+    const int threads = 2 * row_vecs < 512 ? 2 * row_vecs : 512;
+    const int64_t iters = (num_tokens + pa::kKvWriteRowsPerIter - 1) / pa::kKvWriteRowsPerIter;
+    const int64_t max_grid = (int64_t)dev->sm_count * (2048 / threads);
+    const int grid = (int)(iters < max_grid ? iters : max_grid);
+    pa::kv_write_kernel<<<grid, threads, 0, stream>>>(
+        static_cast<const uint4*>(key), static_cast<const uint4*>(value), static_cast<uint4*>(k_cache),
+        static_cast<uint4*>(v_cache), slot_mapping, num_tokens, row_vecs, num_blocks * block_size, dev->err);
+    return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
 int decode_impl(void* out, const void* q, const void* k_cache, const void* v_cache, const int32_t* block_tables,
                 int max_blocks_per_seq, const int32_t* context_lens, int max_context_len, int num_seqs,
                 int n_q_heads, int n_kv_heads, int head_dim, int block_size, int64_t num_blocks, float scale,
                 int dtype, int part_tokens, void* workspace, size_t workspace_bytes, cudaStream_t stream,
-                const PrefixPartials* pf = nullptr) {
+                const PrefixPartials* pf = nullptr, const NewRows* nr = nullptr) {
     int st = check_decode(out, q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens, num_seqs,
                           n_q_heads, n_kv_heads, head_dim, block_size, num_blocks, dtype);
     if (st != PA_OK || num_seqs == 0) return st;
@@ -286,6 +308,24 @@ int decode_impl(void* out, const void* q, const void* k_cache, const void* v_cac
     CUtensorMap tk, tv;
     if ((st = encode_cache_map(&tk, k_cache, dtype, num_blocks, block_size, n_kv_heads, head_dim)) != PA_OK) return st;
     if ((st = encode_cache_map(&tv, v_cache, dtype, num_blocks, block_size, n_kv_heads, head_dim)) != PA_OK) return st;
+    if (nr) {
+        // pa_decode_write: the persistent grid writes each unit's new row itself, just before it
+        // loads the chunk holding it; the other grids get the KV-write kernel launched first
+        const int row_vecs = n_kv_heads * head_dim * 2 / 16;
+        if (p.persist) {
+            p.new_k = static_cast<const uint4*>(nr->key);
+            p.new_v = static_cast<const uint4*>(nr->value);
+            p.new_slots = nr->slot_mapping;
+            p.k_cache_w = static_cast<uint4*>(const_cast<void*>(k_cache));
+            p.v_cache_w = static_cast<uint4*>(const_cast<void*>(v_cache));
+            p.row_vecs = row_vecs;
+            p.n_slots = (long long)num_blocks * block_size;
+        } else if ((st = launch_kv_write(nr->key, nr->value, const_cast<void*>(k_cache), const_cast<void*>(v_cache),
+                                         nr->slot_mapping, num_seqs, row_vecs, num_blocks, block_size, dev,
+                                         stream)) != PA_OK) {
+            return st;
+        }
+    }
     cudaError_t e = pa::launch_decode(dtype == PA_BF16, kernel_dim(head_dim), n_q_heads / n_kv_heads, p, tk, tv, grid, reduce,
                                       stream);
     // a piece grid whose merge did not launch has left the counter wherever it stopped: clear the
@@ -395,16 +435,8 @@ int pa_reshape_and_cache(const void* key, const void* value, void* k_cache, void
     DeviceState* dev = nullptr;
     int st = device_state(&dev);
     if (st != PA_OK) return st;
-    const int row_vecs = (int)(row_bytes / 16);
-    // one thread per 16-byte chunk of the (K row ++ V row) pair, at most 512 (then each loops)
-    const int threads = 2 * row_vecs < 512 ? 2 * row_vecs : 512;
-    const int64_t iters = (num_tokens + pa::kKvWriteRowsPerIter - 1) / pa::kKvWriteRowsPerIter;
-    const int64_t max_grid = (int64_t)dev->sm_count * (2048 / threads);
-    const int grid = (int)(iters < max_grid ? iters : max_grid);
-    pa::kv_write_kernel<<<grid, threads, 0, static_cast<cudaStream_t>(stream)>>>(
-        static_cast<const uint4*>(key), static_cast<const uint4*>(value), static_cast<uint4*>(k_cache),
-        static_cast<uint4*>(v_cache), slot_mapping, num_tokens, row_vecs, num_blocks * block_size, dev->err);
-    return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+    return launch_kv_write(key, value, k_cache, v_cache, slot_mapping, num_tokens, (int)(row_bytes / 16), num_blocks,
+                           block_size, dev, static_cast<cudaStream_t>(stream));
 }
 
 int pa_rope_table(float* out, int64_t max_position, int head_dim, double theta) {
@@ -533,6 +565,31 @@ int pa_decode(void* out, const void* q, const void* k_cache, const void* v_cache
     return pa_decode_splitk(out, q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens, max_context_len,
                             num_seqs, n_q_heads, n_kv_heads, head_dim, block_size, num_blocks, scale, dtype, part,
                             workspace, workspace_bytes, stream);
+}
+
+int pa_decode_write(void* out, const void* q, void* k_cache, void* v_cache, const int32_t* block_tables,
+                    int max_blocks_per_seq, const int32_t* context_lens, int max_context_len, int num_seqs,
+                    int n_q_heads, int n_kv_heads, int head_dim, int block_size, int64_t num_blocks, float scale,
+                    int dtype, const void* key, const void* value, const int64_t* slot_mapping, void* workspace,
+                    size_t workspace_bytes, void* stream) {
+    if (max_context_len < 0 || (int64_t)max_context_len > (int64_t)max_blocks_per_seq * block_size)
+        return PA_ERR_BOUNDS;
+    if (num_seqs > 0) {
+        if (!key || !value || !slot_mapping) return PA_ERR_NULL;
+        if (!aligned16(key) || !aligned16(value)) return PA_ERR_ALIGN;
+    }
+    int part = 0;
+    const int which = pa_decode_plan(num_seqs, n_q_heads, n_kv_heads, head_dim, block_size, max_context_len, dtype,
+                                     &part);
+    if (which < 0) return which;
+    const NewRows nr{key, value, slot_mapping};
+    if (which == 1)
+        return decode_impl(out, q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens,
+                           max_blocks_per_seq * block_size, num_seqs, n_q_heads, n_kv_heads, head_dim, block_size,
+                           num_blocks, scale, dtype, 0, nullptr, 0, static_cast<cudaStream_t>(stream), nullptr, &nr);
+    return decode_impl(out, q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens, max_context_len,
+                       num_seqs, n_q_heads, n_kv_heads, head_dim, block_size, num_blocks, scale, dtype, part,
+                       workspace, workspace_bytes, static_cast<cudaStream_t>(stream), nullptr, &nr);
 }
 
 static int prefill_impl(void* out, const void* q, const void* k_cache, const void* v_cache,

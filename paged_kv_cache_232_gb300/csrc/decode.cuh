@@ -73,6 +73,17 @@ struct DecodeParams {
     const float* pf_m;         // [S * Hq][pf_parts]
     const float* pf_l;
     const float* pf_o;         // [S * Hq][pf_parts][D]
+    // pa_decode_write on the persistent grid: sequence s's new K and V rows (new_k / new_v row s,
+    // row_vecs 16-byte chunks over all KV heads) go into slot new_slots[s] of the cache (-1: none)
+    // by the CTA that decodes (s, g), head g's part, before that unit's last 16-token chunk -- the
+    // one holding token context_lens[s] - 1, the slot's token -- is loaded.  new_k null: no write.
+    const uint4* new_k;
+    const uint4* new_v;
+    const int64_t* new_slots;
+    uint4* k_cache_w;
+    uint4* v_cache_w;
+    int row_vecs;
+    long long n_slots;         // num_blocks * block_size
 };
 
 // The dynamic grid's "counter is at zero" mark in the workspace's control region: the bit
@@ -840,12 +851,15 @@ decode_kernel_persistent(const DecodeParams p, const __grid_constant__ CUtensorM
         const int n = lpt_units(p, reinterpret_cast<int*>(smem), list, C::LIST_MAX);
         if (threadIdx.x == 0) flags[0] = n;
     }
+    // the new rows of pa_decode_write written (one arrival per consumer warp)
+    const uint32_t bar_wdone = ring + C::P_FLAG_OFF + 8;
     if (threadIdx.x == 0) {
         flags[1] = 0;
         for (int i = 0; i < C::NST; ++i) {
             mbar_init(bar_full + 8 * i, 1);
             mbar_init(bar_empty + 8 * i, 1);
         }
+        mbar_init(bar_wdone, C::NCW);
         fence_barrier_init();
     }
     fence_proxy_async_smem();  // the ordering scratch (ring) is written by TMA next
@@ -883,6 +897,7 @@ decode_kernel_persistent(const DecodeParams p, const __grid_constant__ CUtensorM
         const bool half8 = p.cpb_log2 < 0;
         const int per_load = half8 ? 16 : 32;  // chunks whose table entries one warp-wide load covers
         bool ok = true;
+        bool written = p.new_k == nullptr;  // the consumer warps' new rows seen
         int n_issued = 0;  // blocks (ring stages) whose loads were issued, over all units
         for (int k = 0; k < n_units && ok; ++k) {
             const Unit u = unit_at(k, false);
@@ -912,6 +927,11 @@ decode_kernel_persistent(const DecodeParams p, const __grid_constant__ CUtensorM
                         // chunk's first row in its block
                         const int row0 = half8 ? 0 : ((c0 + b0 + j) & ((1 << p.cpb_log2) - 1)) * C::BS;
                         if (gb >= C::NST && !mbar_wait(bar_empty + 8 * st, ph ^ 1, p.err)) ok = false;
+                        // a unit's last chunk holds its sequence's new row: written first
+                        if (ok && !written && b0 + j == u.nblk - 1) {
+                            ok = mbar_wait(bar_wdone, 0, p.err);
+                            written = true;
+                        }
                         if (ok) {
                             const uint32_t dst = ring + st * C::STAGE_BYTES;
                             mbar_arrive_expect_tx(bar_full + 8 * st, C::STAGE_BYTES);
@@ -973,6 +993,42 @@ decode_kernel_persistent(const DecodeParams p, const __grid_constant__ CUtensorM
     const int dg = lane % C::CR, tgp = lane / C::CR;  // P.V layout
     float* pw = p_buf + warp * C::BS * G;
     float* aw = a_buf + warp * 8;
+
+    if (p.new_k) {
+        // pa_decode_write: this CTA's units' new K and V rows into the cache (head g's chunks of
+        // row s for unit (s, g)), made visible to the TMA loads (async proxy) before the producer,
+        // which waits for every warp's arrival, loads a unit's last chunk
+        const int hv = p.hd / 8;  // 16-byte chunks of one head's row
+        const int bs = p.cpb_log2 >= 0 ? 16 << p.cpb_log2 : 8;
+        for (int idx = (int)threadIdx.x; idx < n_units * 2 * hv; idx += C::NCW * 32) {
+            const int k = idx / (2 * hv), r = idx - k * 2 * hv;
+            const int kv = r / hv, c = r - kv * hv;
+            const int s = list[3 * k], g = list[3 * k + 1];
+            const long long slot = p.new_slots[s];
+            if (slot < 0) continue;
+            if (slot >= p.n_slots) {
+                if (r == 0) flag_error(p.err, PA_DEVERR_SLOT);
+                continue;
+            }
+            if (r == 0) {
+                // the slot must be that of the context's last token, the one the last chunk holds
+                int L = __ldg(p.context_lens + s);
+                L = L < 0 ? 0 : min(L, cap);
+                const int e = L > 0 ? (L - 1) / bs : 0;
+                const long long want = L > 0 && e < p.max_blocks_per_seq
+                                           ? (long long)__ldg(p.block_tables + (size_t)s * p.max_blocks_per_seq + e) * bs + (L - 1) % bs
+                                           : -1;
+                if (slot != want) flag_error(p.err, PA_DEVERR_SLOT);
+            }
+            const size_t from = (size_t)s * p.row_vecs + (size_t)g * hv + c;
+            const size_t to = (size_t)slot * p.row_vecs + (size_t)g * hv + c;
+            if (kv == 0) p.k_cache_w[to] = __ldg(p.new_k + from);
+            else p.v_cache_w[to] = __ldg(p.new_v + from);
+        }
+        asm volatile("fence.proxy.async.global;" ::: "memory");
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar_wdone);
+    }
 
     bool ok = true;
     int base_blk = 0;  // ring index of the unit's first block
