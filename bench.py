@@ -371,6 +371,7 @@ def prepare(args, name, dev, with_host=False):
                                                                               q=q_rope),
                            rope_write_bytes(w), "hbm"))
     S, which, dec_logical, dec_launches, part, prefix = 0, 0, 0, 0, 0, 0
+    fused = False
     if b is not None:
         S, hq, D = b.q.shape
         if rope is None:
@@ -410,6 +411,14 @@ def prepare(args, name, dev, with_host=False):
                              device=dev)
             dec_fn = lambda: pa.pa_decode_splitk(out[:S], q[:S], kc, vc, bt, cl, maxL, b.scale, ws, part)
         stages.append(("decode", dec_fn, dec_unique, "hbm"))
+        if (args.step_path == "fused" and wr is not None and rope is None and pre is None and which in (1, 2)
+                and args.decode_path in ("auto", "plain") and wr.key.shape[0] == S):
+            # the step as one call: pa_decode_write puts each sequence's new row into the cache and
+            # decodes (on the persistent grid the decode CTAs write the rows themselves)
+            stages = [("decode_write", lambda: pa.pa_decode_write(out[:S], q[:S], kc, vc, bt, cl, maxL, b.scale, key,
+                                                                  val, sm, ws),
+                       write_bytes(wr, p) + dec_unique, "hbm")]
+            fused = True
     else:
         # write only: the step's result lives in the cache; the end-to-end leg reads back the
         # first written K row as its completion check
@@ -433,8 +442,11 @@ def prepare(args, name, dev, with_host=False):
         stages.append(("prefill", lambda: pa.pa_prefill_chunk(out[S:], q[S:], kc, vc, pbt, qsl, sl, pre.max_q_len,
                                                               pre.scale),
                        prefill_flops(pre, hq, D), "tensor"))
-    c.stages, c.out, c.h_dev = stages, out, h_dev
-    c.launches = (1 if wr is not None else 0) + dec_launches + (1 if pre is not None else 0)
+    c.stages, c.out, c.h_dev, c.fused = stages, out, h_dev, fused
+    # (a fused step on the one-pass grid: batches this large run its persistent form, which writes
+    # the rows itself; the other grids launch the KV-write kernel first)
+    c.launches = ((1 if wr is not None and not (fused and which == 1) else 0) + dec_launches
+                  + (1 if pre is not None else 0))
     wbytes = 0 if wr is None else (rope_write_bytes(w) if rope is not None else write_bytes(wr, p))
     c.step_bytes = wbytes + (decode_bytes(b, p) if (b is not None and args.unified) else dec_logical) + (
         prefill_bytes(pre, p) if pre is not None else 0)
@@ -447,7 +459,8 @@ def prepare(args, name, dev, with_host=False):
                          else (f"shared prefix of {prefix} tokens on the tensor cores + suffix "
                                + ("one-pass" if dec_launches == 2 else f"split-K/{part}") if which == 3
                                else ("one-pass" if which == 1 else f"split-K/{part}"))
-                         + ("" if args.decode_path in ("auto", "plain") else " (forced)"))
+                         + ("" if args.decode_path in ("auto", "plain") else " (forced)")
+                         + (" with the KV write in the same call (pa_decode_write)" if fused else ""))
     return c
 
 
@@ -643,6 +656,18 @@ def run_ours(args, rank, world, local_rank):
     }
     if clocks:
         res["clocks"] = clocks
+    if c.fused:
+        # the same step as two calls (pa_reshape_and_cache, then pa_decode), for its per-kernel times
+        sep = argparse.Namespace(**vars(args))
+        sep.step_path = "separate"
+        cs = prepare(sep, args.workload, dev)
+        whs, _, _ = time_steps(cs, args.steps, args.warmup, world, local_rank, flush, stream, per_stage=False)
+        sts, _, _ = time_steps(cs, args.steps, args.warmup, world, local_rank, flush, stream, per_stage=True)
+        sms, _, sbd, _ = summarize(cs, sts, world, peaks, None, whole_ms=whs[:, 0])
+        res["separate_step"] = {"us_per_step": round(sms * 1e3, 2), "breakdown": sbd,
+                                "note": "pa_reshape_and_cache then pa_decode, two launches; the breakdown with an "
+                                        "event between them"}
+        del cs
     w_head, k_head = c.w, c.k
     del c, h_out, e2e_step, up_dst, up_src, arena
     if args.all_configs and args.workload == "step256":
@@ -820,6 +845,9 @@ def main(argv=None):
     ap.add_argument("--decode-path", choices=["auto", "plain", "v1", "splitk"], default="auto",
                     help="force the one-pass or split-K decode kernel instead of the library's dispatcher "
                          "(plain: the dispatcher without the shared-prefix pass)")
+    ap.add_argument("--step-path", choices=["fused", "separate"], default="fused",
+                    help="a step with a KV write and a decode: one pa_decode_write call (fused) or "
+                         "pa_reshape_and_cache then pa_decode (separate, timed launch by launch)")
     ap.add_argument("--prefix-piece", type=int, default=0,
                     help="shared-prefix pass: keys per CTA (multiple of 128; 0 = the library's choice)")
     ap.add_argument("--partition", type=int, default=0, help="split-K piece length in tokens (with --decode-path splitk)")
