@@ -53,7 +53,9 @@ extern "C" {
 #define PA_ERR_WORKSPACE (-7)   /* split-K workspace missing or smaller than pa_decode_workspace_size() */
 
 /* bits of the per-device error word (pa_device_errors) */
-#define PA_DEVERR_SLOT 1u    /* a slot_mapping entry outside [0, num_blocks*block_size) and not -1 */
+#define PA_DEVERR_SLOT 1u    /* a slot_mapping entry outside [0, num_blocks*block_size) and not -1; for
+                                pa_decode_write on the persistent grid also one that is not the slot of
+                                its sequence's last context token */
 #define PA_DEVERR_BLOCK 2u   /* a block-table entry outside [0, num_blocks) was needed */
 #define PA_DEVERR_LENGTH 4u  /* a context / kv length outside its allowed range */
 #define PA_DEVERR_TIMEOUT 8u /* a pipeline wait in a kernel exceeded its time limit; the kernel gave up */

@@ -555,6 +555,9 @@ int pa_decode(void* out, const void* q, const void* k_cache, const void* v_cache
               int dtype, void* workspace, size_t workspace_bytes, void* stream) {
     if (max_context_len < 0 || (int64_t)max_context_len > (int64_t)max_blocks_per_seq * block_size)
         return PA_ERR_BOUNDS;
+    if (num_seqs == 0)  // an empty batch: the shapes checked, nothing launched
+        return check_decode(out, q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens, 0, n_q_heads,
+                            n_kv_heads, head_dim, block_size, num_blocks, dtype);
     int part = 0;
     const int which = pa_decode_plan(num_seqs, n_q_heads, n_kv_heads, head_dim, block_size, max_context_len, dtype,
                                      &part);
@@ -574,10 +577,11 @@ int pa_decode_write(void* out, const void* q, void* k_cache, void* v_cache, cons
                     size_t workspace_bytes, void* stream) {
     if (max_context_len < 0 || (int64_t)max_context_len > (int64_t)max_blocks_per_seq * block_size)
         return PA_ERR_BOUNDS;
-    if (num_seqs > 0) {
-        if (!key || !value || !slot_mapping) return PA_ERR_NULL;
-        if (!aligned16(key) || !aligned16(value)) return PA_ERR_ALIGN;
-    }
+    if (num_seqs == 0)  // an empty batch: the shapes checked, nothing launched
+        return check_decode(out, q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens, 0, n_q_heads,
+                            n_kv_heads, head_dim, block_size, num_blocks, dtype);
+    if (!key || !value || !slot_mapping) return PA_ERR_NULL;
+    if (!aligned16(key) || !aligned16(value)) return PA_ERR_ALIGN;
     int part = 0;
     const int which = pa_decode_plan(num_seqs, n_q_heads, n_kv_heads, head_dim, block_size, max_context_len, dtype,
                                      &part);

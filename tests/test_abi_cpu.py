@@ -74,6 +74,22 @@ def test_validation_rejects_before_any_device_work(lib):
     assert lib.pa_reshape_and_cache(vp, vp, vp, vp, vp, 4, 1, 3, 16, 10, 1, None) == -3
 
 
+def test_decode_write_validation_rejects_before_any_device_work(lib):
+    """pa_decode_write: the write's own arguments are checked before the decode's plan (no device
+    call): a missing key / value / slot_mapping, a misaligned key, a context bound past the table."""
+    vp = ctypes.c_void_p(16)   # never dereferenced: validation fails first
+    call = lambda key=vp, val=vp, sm=vp, maxL=100: lib.pa_decode_write(
+        vp, vp, vp, vp, vp, 8, vp, maxL, 1, 8, 8, 128, 16, 10, 0.1, 1, key, val, sm, vp, 1 << 30, None)
+    assert call(key=None) == -1
+    assert call(val=None) == -1
+    assert call(sm=None) == -1
+    assert call(key=ctypes.c_void_p(8)) == -6
+    assert call(maxL=129) == -5
+    # nothing to decode: nothing written either
+    assert lib.pa_decode_write(None, None, None, None, None, 8, None, 0, 0, 8, 8, 128, 16, 10, 0.1, 1, None, None,
+                               None, None, 0, None) == 0
+
+
 def test_rope_table_matches_the_formula_and_validates(lib):
     """pa_rope_table is host code: row m = [cos(m f_i) ..., sin(m f_i) ...], f_i = theta^(-2i/D),
     computed in double and stored as float; compared with numpy's float64 cos / sin."""
