@@ -309,10 +309,11 @@ int decode_impl(void* out, const void* q, const void* k_cache, const void* v_cac
     if ((st = encode_cache_map(&tk, k_cache, dtype, num_blocks, block_size, n_kv_heads, head_dim)) != PA_OK) return st;
     if ((st = encode_cache_map(&tv, v_cache, dtype, num_blocks, block_size, n_kv_heads, head_dim)) != PA_OK) return st;
     if (nr) {
-        // pa_decode_write: the persistent grid writes each unit's new row itself, just before it
-        // loads the chunk holding it; the other grids get the KV-write kernel launched first
+        // pa_decode_write: the persistent and the dynamic grids write each unit's new row
+        // themselves, just before loading the chunk that holds it; the other grids get the
+        // KV-write kernel launched first
         const int row_vecs = n_kv_heads * head_dim * 2 / 16;
-        if (p.persist) {
+        if (p.persist || p.dyn) {
             p.new_k = static_cast<const uint4*>(nr->key);
             p.new_v = static_cast<const uint4*>(nr->value);
             p.new_slots = nr->slot_mapping;

@@ -44,12 +44,17 @@ static cudaError_t launch_decode_t(const DecodeParams& p, const CUtensorMap& tmK
     if (p.dyn) {
         // group sizes 1 and 2 only (at 4 the piece loop spills and the static grid is faster)
         if constexpr (G <= 2) {
-            auto kern = decode_kernel_dyn<D, G, BF16>;
-            static std::atomic<unsigned long long> s_dyn{0};
             static_assert(C::DYN_SMAX == kDynTailMaxSeqs, "tail-piece batch limit");
-            e = smem_limit_once(reinterpret_cast<const void*>(kern), C::D_SMEM_BYTES, s_dyn);
-            if (e != cudaSuccess) return e;
-            e = launch(kern, C::D_SMEM_BYTES);
+            if (p.new_k) {
+                // pa_decode_write: the instantiation that writes the step's rows (decode_write.cu)
+                e = launch_dyn_write<D, G, BF16>(p, tmK, tmV, grid, st);
+            } else {
+                auto kern = decode_kernel_dyn<D, G, BF16>;
+                static std::atomic<unsigned long long> s_dyn{0};
+                e = smem_limit_once(reinterpret_cast<const void*>(kern), C::D_SMEM_BYTES, s_dyn);
+                if (e != cudaSuccess) return e;
+                e = launch(kern, C::D_SMEM_BYTES);
+            }
         } else {
             return cudaErrorInvalidValue;
         }

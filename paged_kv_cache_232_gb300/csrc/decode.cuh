@@ -73,10 +73,11 @@ struct DecodeParams {
     const float* pf_m;         // [S * Hq][pf_parts]
     const float* pf_l;
     const float* pf_o;         // [S * Hq][pf_parts][D]
-    // pa_decode_write on the persistent grid: sequence s's new K and V rows (new_k / new_v row s,
-    // row_vecs 16-byte chunks over all KV heads) go into slot new_slots[s] of the cache (-1: none)
-    // by the CTA that decodes (s, g), head g's part, before that unit's last 16-token chunk -- the
-    // one holding token context_lens[s] - 1, the slot's token -- is loaded.  new_k null: no write.
+    // pa_decode_write on the persistent and the dynamic grids: sequence s's new K and V rows
+    // (new_k / new_v row s, row_vecs 16-byte chunks over all KV heads) go into slot new_slots[s] of
+    // the cache (-1: none), head g's part by the CTA that decodes the last chunk of (s, g) -- the
+    // one holding token context_lens[s] - 1, the slot's token -- before it loads that chunk.
+    // new_k null: no write.
     const uint4* new_k;
     const uint4* new_v;
     const int64_t* new_slots;
@@ -1256,7 +1257,7 @@ __device__ __forceinline__ void dyn_piece_counts(const DecodeParams& p, int cap,
 // order of accumulation does not depend on which items a CTA took) and every ring stage keeps one
 // owning warp; both sides count each stage's uses for the barrier parities, as the skipped ring
 // indices never touch a stage.  The per-chunk work is decode_kernel's.
-template <int D, int G, bool BF16>
+template <int D, int G, bool BF16, bool WRITE = false>
 __global__ void __launch_bounds__(DecodeCfg<D, G, BF16>::THREADS,
                                   D == 256 ? (G <= 2 ? 2 : 1) : ((G <= 4) ? 3 : (D == 64 ? 2 : 1)))
 decode_kernel_dyn(const DecodeParams p, const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV) {
@@ -1348,6 +1349,7 @@ decode_kernel_dyn(const DecodeParams p, const __grid_constant__ CUtensorMap tmK,
             item = __shfl_sync(0xffffffffu, item, 0);
             const bool end = (long long)item >= total;
             int s = -1, g = 0, piece = 0, t_begin = 0, t_end = 0, n_parts = 0;
+            int L_item = -1;  // the item's sequence's clamped context length
             if (!end && tail) {
                 const bool full = (long long)item < n_full;
                 const int r = full ? item : (int)((long long)item - n_full);
@@ -1363,6 +1365,7 @@ decode_kernel_dyn(const DecodeParams p, const __grid_constant__ CUtensorMap tmK,
                 s = lo;
                 const int L = o_len[s], base = min(L, p.prefix_tokens), Ls = L - base;
                 const int f = o_cumA[s + 1] - o_cumA[s];
+                L_item = L;
                 if (full) {
                     piece = e - o_cumA[s];
                     t_begin = base + piece * p.part_tokens;
@@ -1385,6 +1388,7 @@ decode_kernel_dyn(const DecodeParams p, const __grid_constant__ CUtensorMap tmK,
                     if (piece == 0 && g == 0 && lane == 0) flag_error(p.err, PA_DEVERR_LENGTH);
                     L = L < 0 ? 0 : cap;
                 }
+                L_item = L;
                 const int base = min(L, p.prefix_tokens);
                 t_begin = min(L, base + piece * p.part_tokens);
                 t_end = min(L, t_begin + p.part_tokens);
@@ -1411,6 +1415,44 @@ decode_kernel_dyn(const DecodeParams p, const __grid_constant__ CUtensorMap tmK,
             ok = __shfl_sync(0xffffffffu, ok, 0);
             ++nq;
             if (end || !ok) break;
+            // WRITE (pa_decode_write): the item that ends at its sequence's context length (the one
+            // holding the last token, or the empty piece of an empty context) writes head g's part of the
+            // sequence's new K and V rows before the chunk holding that token is loaded (generic
+            // stores, then the proxy fence, then the TMA); the rows' loads go out now, behind the
+            // item's earlier chunks
+            const bool row_item = WRITE && t_end == L_item;
+            const int hv = p.hd / 8;  // 16-byte chunks of one head's row
+            long long nslot = -1;
+            uint4 nrow[2];
+            if (row_item) {
+                nslot = __ldg(p.new_slots + s);
+                if (nslot >= p.n_slots) {
+                    if (lane == 0) flag_error(p.err, PA_DEVERR_SLOT);
+                    nslot = -1;
+                }
+                if (nslot >= 0) {
+#pragma unroll
+                    for (int i2 = 0; i2 < 2; ++i2) {
+                        const int c = lane + 32 * i2, kv = c / hv, cc = c - kv * hv;
+                        if (c < 2 * hv) nrow[i2] = __ldg((kv ? p.new_v : p.new_k) + (size_t)s * p.row_vecs + (size_t)g * hv + cc);
+                    }
+                }
+            }
+            // the row into its slot; `want` = the slot of token L - 1 (-1: none)
+            auto store_row = [&](long long want) {
+                if (nslot >= 0) {
+#pragma unroll
+                    for (int i2 = 0; i2 < 2; ++i2) {
+                        const int c = lane + 32 * i2, kv = c / hv, cc = c - kv * hv;
+                        if (c < 2 * hv) (kv ? p.v_cache_w : p.k_cache_w)[nslot * p.row_vecs + (long long)g * hv + cc] = nrow[i2];
+                    }
+                    asm volatile("fence.proxy.async.global;" ::: "memory");
+                    if (lane == 0 && nslot != want) flag_error(p.err, PA_DEVERR_SLOT);
+                }
+                __syncwarp();
+            };
+            if constexpr (WRITE)
+                if (row_item && nblk == 0) store_row(-1);
             // the item's chunks into ring indices r0 .. r0 + nblk - 1; 16-token chunk c of the
             // sequence: table entry c >> cpb_log2, rows 16 (c mod 2^cpb_log2) + 0..15 (blocks of 8:
             // entries 2c and 2c + 1, the second only if the context reaches it)
@@ -1431,6 +1473,13 @@ decode_kernel_dyn(const DecodeParams p, const __grid_constant__ CUtensorMap tmK,
                     const int blk = __shfl_sync(0xffffffffu, my, half8 ? 2 * j : j);
                     const int blk_b = __shfl_sync(0xffffffffu, my, (2 * j + 1) & 31);  // half8 only
                     const int st = (r0 + b0 + j) % C::NST;
+                    if constexpr (WRITE) {
+                        if (row_item && b0 + j == nblk - 1) {
+                            const int tl = L_item - 1;  // the last token, in this chunk
+                            store_row(half8 ? (long long)((tl & 15) < 8 ? blk : blk_b) * 8 + (tl & 7)
+                                            : (long long)blk * (16 << p.cpb_log2) + (tl & ((16 << p.cpb_log2) - 1)));
+                        }
+                    }
                     if (lane == 0) {
                         const int row0 = half8 ? 0 : ((blk0 + b0 + j) & ((1 << p.cpb_log2) - 1)) * C::BS;
                         if ((fused >> st) & 1) ok = mbar_wait(bar_empty + 8 * st, ((fpar >> st) & 1) ^ 1, p.err);

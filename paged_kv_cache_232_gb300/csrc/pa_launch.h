@@ -45,6 +45,12 @@ inline cudaError_t launch_dependent(Kern kern, unsigned grid, unsigned block, si
     return cudaLaunchKernelEx(&cfg, kern, args...);
 }
 
+// The dynamic split-K grid that also writes pa_decode_write's rows (decode_kernel_dyn with
+// WRITE; instantiated in decode_write.cu for group sizes 1 and 2 and head_dim 64, 128 and 256).
+template <int D, int G, bool BF16>
+cudaError_t launch_dyn_write(const DecodeParams& p, const CUtensorMap& tmK, const CUtensorMap& tmV, int grid,
+                             cudaStream_t st);
+
 // Launch the decode piece kernel for (dtype, head_dim, group) on `grid` CTAs; when
 // params.part_tokens > 0 and any sequence has more than one piece, also launch the reduce.
 // Bytes of the decode kernel's ring for head_dim (64, 128 or 256).
