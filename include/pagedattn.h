@@ -54,8 +54,8 @@ extern "C" {
 
 /* bits of the per-device error word (pa_device_errors) */
 #define PA_DEVERR_SLOT 1u    /* a slot_mapping entry outside [0, num_blocks*block_size) and not -1; for
-                                pa_decode_write on the persistent grid also one that is not the slot of
-                                its sequence's last context token */
+                                pa_decode_write on the persistent and dynamic grids also one that is not
+                                the slot of its sequence's last context token */
 #define PA_DEVERR_BLOCK 2u   /* a block-table entry outside [0, num_blocks) was needed */
 #define PA_DEVERR_LENGTH 4u  /* a context / kv length outside its allowed range */
 #define PA_DEVERR_TIMEOUT 8u /* a pipeline wait in a kernel exceeded its time limit; the kernel gave up */
@@ -199,12 +199,12 @@ int pa_decode(void* out, const void* q, const void* k_cache, const void* v_cache
  *  aligned) and slot_mapping ([num_seqs] int64 on the device, -1 = none).  slot_mapping[s], when
  *  not -1, must be the slot of token context_lens[s] - 1 of sequence s (block_tables[s][(L - 1) /
  *  block_size] * block_size + (L - 1) % block_size): on the persistent one-pass grid (batches of
- *  two waves and more at group size 1 or 2) the CTA that decodes (s, g) writes head g's part of
- *  the row itself just before loading the 16-token chunk that holds that token, so no separate
- *  write launch precedes the decode; a slot elsewhere, or outside [0, num_blocks * block_size),
- *  sets PA_DEVERR_SLOT (an outside slot writes nothing).  Every other grid launches the KV-write
- *  kernel first.  Returns as pa_decode, plus PA_ERR_NULL / PA_ERR_ALIGN for key, value or
- *  slot_mapping.
+ *  two waves and more at group size 1 or 2) and on the dynamic split-K grid (group size 1 or 2,
+ *  more pieces than resident CTAs) the CTA that loads the 16-token chunk holding that token of
+ *  (s, g) writes head g's part of the row itself just before, so no separate write launch
+ *  precedes the decode; a slot elsewhere, or outside [0, num_blocks * block_size), sets
+ *  PA_DEVERR_SLOT (an outside slot writes nothing).  The other grids launch the KV-write kernel
+ *  first.  Returns as pa_decode, plus PA_ERR_NULL / PA_ERR_ALIGN for key, value or slot_mapping.
  */
 int pa_decode_write(void* out, const void* q, void* k_cache, void* v_cache, const int32_t* block_tables,
                     int max_blocks_per_seq, const int32_t* context_lens, int max_context_len, int num_seqs,

@@ -2,8 +2,8 @@
 into slot_mapping[s] (the slot of its last context token, -1 for none), then every sequence is
 decoded over a context that includes that row.  It must leave the caches and the output bit for
 bit as pa_reshape_and_cache followed by pa_decode does, whichever grid the dispatcher picks (the
-persistent one-pass grid writes the rows from inside the decode CTAs; every other grid launches
-the KV-write kernel first), and match the oracle's write-then-decode.  Source: mini_engine,
+persistent one-pass grid and the dynamic split-K grid write the rows from inside the decode CTAs;
+the other grids launch the KV-write kernel first), and match the oracle's write-then-decode.  Source: mini_engine,
 "Custom CUDA kernels" (the KV-cache write and the paged decode of a step); miniserve, "Engine"
 (slot mapping)."""
 import numpy as np
@@ -89,11 +89,13 @@ def test_decode_write_repeated_calls_bitwise():
     assert pa.pa_device_errors(clear=True) == 0
 
 
-def test_decode_write_flags_slots_it_cannot_place():
-    """On the persistent grid: a slot past the pool writes nothing and sets PA_DEVERR_SLOT, as the
-    KV-write kernel does; an in-pool slot that is not the sequence's last token is still written
-    (the caches match the separate write) and also sets PA_DEVERR_SLOT."""
-    w = _case("step256")
+@pytest.mark.parametrize("name", ["step256", "decode64"])
+def test_decode_write_flags_slots_it_cannot_place(name):
+    """On the persistent grid (batch 256) and the dynamic grid (batch 64): a slot past the pool
+    writes nothing and sets PA_DEVERR_SLOT, as the KV-write kernel does; an in-pool slot that is
+    not the sequence's last token is still written (the caches match the separate write) and also
+    sets PA_DEVERR_SLOT."""
+    w = _case(name)
     p, b, wr = w.pool, w.decode, w.write
     slots = wr.slot_mapping.copy()
     live = np.flatnonzero(slots >= 0)
