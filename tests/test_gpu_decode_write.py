@@ -3,9 +3,9 @@ into slot_mapping[s] (the slot of its last context token, -1 for none), then eve
 decoded over a context that includes that row.  It must leave the caches and the output bit for
 bit as pa_reshape_and_cache followed by pa_decode does, whichever grid the dispatcher picks (the
 persistent one-pass grid and the dynamic split-K grid write the rows from inside the decode CTAs;
-the other grids launch the KV-write kernel first), and match the oracle's write-then-decode.  Source: mini_engine,
-"Custom CUDA kernels" (the KV-cache write and the paged decode of a step); miniserve, "Engine"
-(slot mapping)."""
+the other grids launch the KV-write kernel first), and match the oracle's write-then-decode.
+Source: mini_engine, "Custom CUDA kernels" (the KV-cache write and the paged decode of a step);
+miniserve, "Engine" (slot mapping)."""
 import numpy as np
 import pytest
 import torch
