@@ -1248,8 +1248,11 @@ __device__ __forceinline__ void dyn_piece_counts(const DecodeParams& p, int cap,
 }
 
 // The dynamic split-K grid (p.dyn): gridDim.x CTAs, one per resident slot, take work items --
-// the split-K pieces, highest piece index first as in decode_kernel's grid -- from a counter the
-// launcher zeroes.  The producer warp fetches an item, publishes it through a small queue in
+// the split-K pieces, highest piece index first as in decode_kernel's grid, or with tail pieces
+// the full pieces and then the tail pieces -- from a counter in the workspace, which the previous
+// call's merge left at zero with its tag set (DecodeParams::dyn_tag; without the tag the CTAs
+// take the items in a fixed order).  WRITE: the instantiation that also writes pa_decode_write's
+// rows.  The producer warp fetches an item, publishes it through a small queue in
 // shared memory and streams its chunks into the ring, the next item's while the consumers merge
 // this one; the SMs that stream faster take more pieces, so the grid ends evenly, and no CTA pays
 // its start-up more than once.  Each item starts on a ring index that is a multiple of the
