@@ -37,8 +37,11 @@ def _oracle_step(cache_k, cache_v, key, val, sm, q, b, lens, p):
     return k2, v2, ex, cd
 
 
-@pytest.mark.parametrize("path", ["auto", "splitk"])
+@pytest.mark.parametrize("path", ["auto", "splitk", "fused"])
 def test_decode_step_graph_replay(path):
+    """auto: pa_reshape_and_cache then pa_decode (the persistent one-pass grid); splitk: the same
+    with 256-token pieces (the dynamic split-K grid); fused: one pa_decode_write call, whose decode
+    CTAs write the rows."""
     w = wl.make_workload(4)
     p, b, wr = w.pool, w.decode, w.write
     kc, vc = to_dev(p.k_cache, p.dtype), to_dev(p.v_cache, p.dtype)
@@ -52,6 +55,9 @@ def test_decode_step_graph_replay(path):
     ws = torch.zeros(max(16, pa.pa_decode_workspace_size(S, hq, D, maxL, 256)), dtype=torch.uint8, device="cuda")
 
     def step():
+        if path == "fused":
+            pa.pa_decode_write(out, q, kc, vc, bt, cl, maxL, b.scale, key, val, sm, ws)
+            return
         pa.pa_reshape_and_cache(key, val, kc, vc, sm)
         if path == "auto":
             pa.pa_decode(out, q, kc, vc, bt, cl, maxL, b.scale, ws)
@@ -78,6 +84,12 @@ def test_decode_step_graph_replay(path):
 
     # next step: new inputs written into the captured buffers, same graph
     q2, key2, val2, sm2, lens2 = _new_inputs(w, 232_777)
+    if path == "fused":
+        # pa_decode_write's rows sit at each context's last token: move the live slots there
+        last = lens2.astype(np.int64) - 1
+        at_last = b.block_tables[np.arange(b.num_seqs), last // p.block_size].astype(np.int64) * p.block_size + \
+            last % p.block_size
+        sm2 = np.where(sm2 >= 0, at_last, -1).astype(np.int64)
     before_k, before_v = bits_of(kc), bits_of(vc)
     q.copy_(to_dev(q2, p.dtype))
     key.copy_(to_dev(key2, p.dtype))
